@@ -1,0 +1,208 @@
+/*
+ * libtpoverlap -- tensor-parallel linear layers whose GEMM overlaps the movement
+ * of its operand or result chunks, on one GB300 (sm_103a).
+ *
+ * The tp "ranks" of a tensor-parallel group are simulated as tp chunk buffers in
+ * one GPU's memory.  Three operations are provided:
+ *
+ *   AG+GEMM   Y = allgather_rows(X_0 .. X_tp-1) . W^T, rows in rank order.
+ *             TransformerEngine issue "curious about atomic_gemm_overlap_ag",
+ *             listing of CommOverlapP2PBase::atomic_gemm_overlap_ag: a ring of
+ *             chunk send/recv steps fills the gathered buffer, a per-chunk
+ *             producer counter marks each chunk ready, and one GEMM consumes
+ *             the chunks as their counters flip.
+ *   GEMM+RS   Y = sum_r X_r . W_r^T, rank b receives row block b.
+ *             TransformerEngine PR "Comm+GEMM overlap API updated to support
+ *             cuBlasMp backend", sequence diagram, GEMM + reduce-scatter path.
+ *   GEMM+AR   Y = sum_r X_r . W_r^T in full, produced in row chunks.
+ *             nvFuser PR "Reference implementation for Linear+Allreduce with
+ *             overlapping": row-parallel linear, per-chunk matmul then
+ *             all-reduce SUM.
+ *
+ * Conventions (TN layout, as the listing's transa/transb and m/n naming):
+ *   n  rows of Y (tokens), m  columns of Y (output features),
+ *   k  the GLOBAL contraction length.  For AG every X_r is [n/tp, k]; for RS and
+ *      AR every rank holds a K-slice, X_r [n, k/tp] and W_r [m, k/tp].
+ *   All matrices are dense row-major; X and W are "K-major" (the contraction
+ *   index is contiguous); Y is always bf16.
+ *   bf16 buffers hold IEEE bfloat16, e4m3 buffers OCP FP8 E4M3 codes.
+ *
+ * Ownership: the caller owns every X, W, Y buffer and the stream.  The context
+ * owns the staging buffer (the gathered X), the per-chunk counters, the device
+ * error word and the trace buffer; all are allocated by tpo_ctx_create and
+ * nothing is allocated by the per-call entry points.
+ *
+ * Calls are stream-ordered and asynchronous: they validate their arguments on
+ * the host, enqueue work on `stream` (a cudaStream_t passed as void*, NULL for
+ * the legacy default stream) and return.  Inputs must stay valid until the
+ * stream reaches the call.  Argument errors are reported synchronously before
+ * anything is enqueued.  A device-side failure (a bounded wait that ran out) is
+ * recorded in the context's error word and reported by the next
+ * tpo_sync_status; until then the word is sticky and later calls on the
+ * context abort early.  Every entry point sets a thread-local message readable
+ * through tpo_last_error when it fails.
+ *
+ * A context is not thread-safe: calls on one context must come from one host
+ * thread at a time.  Calls that overlap on the GPU (different streams) must use
+ * different contexts.
+ */
+#ifndef TPOVERLAP_H
+#define TPOVERLAP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tpo_ctx tpo_ctx; /* opaque */
+
+/* Input element type (Y is always bf16). */
+typedef enum { TPO_BF16 = 0, TPO_FP8_E4M3 = 1 } tpo_dtype;
+
+typedef enum {
+  TPO_OK = 0,
+  TPO_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or option */
+  TPO_ERR_UNSUPPORTED = 2, /* valid request outside the tiling this build supports */
+  TPO_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  TPO_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out */
+  TPO_ERR_OOM = 5          /* device allocation failed in tpo_ctx_create */
+} tpo_status;
+
+/* Operation limits of this build. */
+#define TPO_MAX_TP 16
+#define TPO_MAX_ROW_CHUNKS 64
+#define TPO_BLOCK_M 128 /* rows of one output tile */
+#define TPO_BLOCK_N 256 /* columns of one output tile */
+
+/*
+ * Create a context for one problem size on the current CUDA device.
+ *   tp     number of simulated ranks, 1..16
+ *   n      rows of Y, a multiple of tp*128
+ *   k      global contraction length: a multiple of 64 (bf16) or 128 (e4m3);
+ *          for RS/AR also k % tp == 0 and k/tp a multiple of 64
+ *   m      columns of Y, a multiple of 256
+ *   dtype  a tpo_dtype value
+ * Allocates the staging buffer (n*k elements), counters, error word and trace
+ * buffer on the current device.  Returns NULL on any error (no half-built
+ * context is ever returned); tpo_last_error says why.
+ * The signature follows the context-handle pattern of the cuBLASMp backend in
+ * TransformerEngine PR "Comm+GEMM overlap API updated to support cuBlasMp
+ * backend" (nvte_comm_gemm_ctx_create ... nvte_comm_gemm_ctx_destroy).
+ */
+tpo_ctx* tpo_ctx_create(int tp, int64_t n, int64_t k, int64_t m, int dtype);
+
+/* Release everything the context owns (synchronises with its pending work).
+ * tpo_ctx_destroy(NULL) is a no-op returning TPO_OK. */
+tpo_status tpo_ctx_destroy(tpo_ctx* ctx);
+
+/*
+ * AG+GEMM: Y[n, m] = gather(X_0..X_tp-1)[n, k] . W[m, k]^T, Y rows in rank order.
+ *   x      host array of tp device pointers; x[r] is rank r's chunk [n/tp, k]
+ *   w      device pointer, [m, k]
+ *   y      device pointer, [n, m] bf16
+ *   d_scale_inv_x, d_scale_inv_w
+ *          e4m3 contexts: device pointers to one fp32 each (the per-tensor
+ *          scale_inv of all X_r together and of W); the product is multiplied
+ *          by both in fp32 before rounding.  bf16 contexts: must be NULL.
+ *   stream cudaStream_t
+ * Semantics (listing of atomic_gemm_overlap_ag): the observer rank `self_rank`
+ * (option, default 0) holds its own chunk and receives the others in ring
+ * order self-1, self-2, ... (mod tp).  A producer role copies each arriving
+ * chunk into its rank-order slot of the staging buffer and publishes the
+ * slot's counter with release semantics; the GEMM role acquire-waits on that
+ * counter before its first tensor-memory load of the slot.  Y is written in
+ * rank order directly (no rotation buffer).  All pointers 16-byte aligned.
+ * The result is bit-identical in every mode (option "mode").
+ */
+tpo_status tpo_ag_gemm(tpo_ctx* ctx, const void* const* x, const void* w, void* y,
+                       const float* d_scale_inv_x, const float* d_scale_inv_w, void* stream);
+
+/*
+ * GEMM+RS: y[b] = rows [b*n/tp, (b+1)*n/tp) of sum_r X_r . W_r^T.
+ *   x   host array of tp device pointers, X_r [n, k/tp]
+ *   w   host array of tp device pointers, W_r [m, k/tp]
+ *   y   host array of tp device pointers, y[b] [n/tp, m] bf16
+ * The partial products are summed in a fixed ring order inside one GEMM:
+ * the output rows owned by rank b accumulate ranks b+1, b+2, ..., b (mod tp),
+ * the order of a ring reduce-scatter that ends at the owner, in fp32, with a
+ * single rounding to bf16 in the epilogue.  bf16 contexts only.
+ */
+tpo_status tpo_gemm_rs(tpo_ctx* ctx, const void* const* x, const void* const* w, void* const* y,
+                       void* stream);
+
+/*
+ * GEMM+AR (row-parallel linear): Y[n, m] = sum_r X_r . W_r^T.
+ *   x, w          as tpo_gemm_rs
+ *   y             device pointer [n, m] bf16
+ *   n_row_chunks  1..64; n must be a multiple of n_row_chunks*tp*128
+ * Output tiles are produced chunk by chunk (row chunk 0 first).  Inside row
+ * chunk c, the rows of the chunk's i-th of tp equal parts sum ranks i+1, ...,
+ * i (mod tp), the per-part order of a ring all-reduce of that chunk.  After
+ * every tile of chunk c is stored, the chunk's done counter (see
+ * tpo_ar_done_counters) reaches its target with release semantics.  bf16 only.
+ */
+tpo_status tpo_gemm_ar(tpo_ctx* ctx, const void* const* x, const void* const* w, void* y,
+                       int n_row_chunks, void* stream);
+
+/*
+ * Options (integers).  Keys:
+ *   "producer_sms"     CTAs given to the chunk producer in overlapped AG (>=1)
+ *   "gemm_ctas"        CTAs given to the GEMM (0 = all SMs not producing)
+ *   "mode"             AG schedule: 0 overlapped (one launch, producer and GEMM
+ *                      co-resident), 1 sequential (copy to completion, then the
+ *                      same GEMM), 2 GEMM only (staging and counters must hold a
+ *                      previous call's chunks), 3 producer only (no GEMM; y is
+ *                      not written)
+ *   "seq_copy_ctas"    CTAs of the copy in sequential mode (0 = all SMs)
+ *   "self_rank"        observer rank for the ring order, 0..tp-1
+ *   "wait_timeout_ms"  bound of every device-side wait (default 2000)
+ *   "trace"            1 = record device timestamps (tpo_read_trace)
+ *   "debug_skip_chunk" slot whose counter the producer never publishes (-1 off)
+ *   "debug_delay_ns"   producer spin before each publish
+ *   "debug_last_step"  producer stops after this ring step (-1 = all steps)
+ * Environment variables TPO_<KEY in upper case> override the defaults at
+ * create time.  Unknown keys or out-of-range values: TPO_ERR_INVALID_ARG.
+ */
+tpo_status tpo_set_opt(tpo_ctx* ctx, const char* key, int64_t value);
+tpo_status tpo_get_opt(tpo_ctx* ctx, const char* key, int64_t* value);
+
+/* Wait for all work this context enqueued, read and clear the device error
+ * word.  Returns TPO_OK or the recorded failure (TPO_ERR_TIMEOUT); after a
+ * failure the counters are re-zeroed so the context is usable again. */
+tpo_status tpo_sync_status(tpo_ctx* ctx);
+
+/* Details of the last device failure seen by tpo_sync_status: code, site,
+ * block index, slot (4 words). */
+tpo_status tpo_last_device_error(tpo_ctx* ctx, uint32_t out[4]);
+
+/* Thread-local message of the last failing call on this thread ("" if none). */
+const char* tpo_last_error(void);
+
+/* Read-only device pointer to the staging buffer [n, k] (the gathered X in rank
+ * order), for inspection after a synchronised AG call. */
+const void* tpo_staging_ptr(tpo_ctx* ctx);
+
+/* Device pointer to the AR done counters (TPO_MAX_ROW_CHUNKS uint32 words) and
+ * the value chunk c's counter reaches when the last tpo_gemm_ar call has
+ * stored all of chunk c. */
+const uint32_t* tpo_ar_done_counters(tpo_ctx* ctx, uint32_t* target);
+
+/* Trace words (uint64 nanoseconds of the device global timer), valid after
+ * tpo_sync_status when option "trace" was 1; reset by each traced call. */
+#define TPO_TRACE_START 0      /* earliest CTA start */
+#define TPO_TRACE_END 1        /* latest CTA end */
+#define TPO_TRACE_PUBLISH 2    /* + slot: latest producer publish of the slot */
+#define TPO_TRACE_ACQUIRE 18   /* + slot: earliest GEMM acquire of the slot */
+#define TPO_TRACE_WAIT_NS 34   /* total ns GEMM CTAs spent waiting on counters */
+#define TPO_TRACE_CHUNK_DONE 35 /* + chunk: AR chunk completion time */
+#define TPO_TRACE_WORDS 128
+tpo_status tpo_read_trace(tpo_ctx* ctx, uint64_t* out, int cap);
+
+/* Library build string (compiler, target architecture). */
+const char* tpo_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TPOVERLAP_H */

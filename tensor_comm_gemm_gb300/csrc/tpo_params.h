@@ -1,0 +1,104 @@
+// Launch parameters shared by the host launcher (ctx.cu) and the fused kernel
+// (kernels.cu).  Private to libtpoverlap.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "tpoverlap.h"
+
+namespace tpo {
+
+// Tile shape: one CTA computes a BM x BN output tile; every pipeline stage holds
+// a BM x 128-byte slice of A and a BN x 128-byte slice of B (64 bf16 or 128 e4m3
+// contraction elements), the width of one 128-byte swizzle row.
+constexpr int BM = TPO_BLOCK_M;
+constexpr int BN = TPO_BLOCK_N;
+constexpr int BK_BYTES = 128;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK_BYTES;  // 16 KiB
+constexpr int B_STAGE_BYTES = BN * BK_BYTES;  // 32 KiB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int NUM_THREADS = 192;              // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_COLS = 32;                  // columns per epilogue store box
+constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;  // 32 rows x 32 bf16
+constexpr int TMEM_COLS = 512;                // two BN-column fp32 accumulators
+
+// Producer (chunk copy) role: bulk copies through a ring of shared buffers.
+constexpr int COPY_PIECE = 16384;
+constexpr int COPY_BUFS = 12;
+constexpr int COPY_LAG = 6;
+
+// Shared memory map (offsets from a 1024-byte aligned base).
+constexpr int SMEM_STAGES = 0;
+constexpr int SMEM_EPI = SMEM_STAGES + STAGES * STAGE_BYTES;            // 196608
+constexpr int SMEM_BARS = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;     // 212992
+constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + COPY_BUFS;
+constexpr int SMEM_TMEM_SLOT = SMEM_BARS + NUM_BARS * 8;
+constexpr int SMEM_USED = SMEM_TMEM_SLOT + 16;
+constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for aligning the base
+static_assert(COPY_BUFS * COPY_PIECE <= STAGES * STAGE_BYTES, "copy ring must fit the stage area");
+static_assert(SMEM_ALLOC <= 232448, "exceeds the per-CTA shared memory limit");
+
+enum Op : int { OP_AG = 0, OP_RS = 1, OP_AR = 2 };
+
+// Device error word layout: [0] code, [1] site, [2] block, [3] slot/extra.
+enum DevErr : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1 };
+enum Site : uint32_t {
+  SITE_COUNTER = 1,    // GEMM TMA thread waiting on a chunk counter
+  SITE_EMPTY = 2,      // TMA thread waiting for a free stage
+  SITE_FULL = 3,       // MMA thread waiting for a loaded stage
+  SITE_TMEM_EMPTY = 4, // MMA thread waiting for a drained accumulator
+  SITE_TMEM_FULL = 5,  // epilogue waiting for a finished accumulator
+  SITE_COPY = 6,       // producer waiting for a bulk load
+  SITE_DRAIN = 7       // clean-up waits after a failure
+};
+
+// Per-context device words (one allocation).
+struct DevWords {
+  uint32_t counters[TPO_MAX_TP];        // per-slot chunk counters (monotonic)
+  uint32_t err[4];
+  uint32_t ar_done[TPO_MAX_ROW_CHUNKS]; // per-row-chunk done counters (monotonic)
+  uint32_t pad[12];
+  unsigned long long trace[TPO_TRACE_WORDS];
+};
+
+struct Params {
+  CUtensorMap mapA[TPO_MAX_TP];  // AG: [0] staging [n,k], [1] X_self; RS/AR: X_r
+  CUtensorMap mapB[TPO_MAX_TP];  // AG: [0] W; RS/AR: W_r
+  CUtensorMap mapY[TPO_MAX_TP];  // AG/AR: [0] Y; RS: y[b]
+  const uint8_t* src[TPO_MAX_TP];  // producer sources X_r
+  uint8_t* staging;
+  DevWords* words;
+  const float* scale_x;
+  const float* scale_w;
+  long long chunk_bytes;
+  unsigned long long timeout_ns;
+  unsigned long long delay_ns;
+  uint32_t target;        // counter value of a chunk published by this call
+  uint32_t ar_target;     // AR done-counter value once this call stored the chunk
+  int op;
+  int fp8;
+  int tp;
+  int self_rank;
+  int num_producers;      // CTAs [0, num_producers) run the producer role
+  int num_gemm;           // CTAs [num_producers, +num_gemm) run the GEMM role
+  int rows_per_group;     // AG: rows per slot; RS: rows per block; AR: rows per chunk
+  int row_tiles;          // BM tiles per group
+  int col_tiles;          // BN tiles across m
+  int num_groups;         // AG: tp slots; RS: tp blocks; AR: row chunks
+  int kb_per_seg;         // 128-byte K blocks per segment
+  int num_segs;           // AG: 1; RS/AR: tp
+  int gate;               // 1: wait on chunk counters before loading a slot
+  int skip_slot;          // debug: never publish this slot (-1 off)
+  int last_step;          // debug: producer stops after this ring step (-1 all)
+  int trace_on;
+};
+
+// Host-side launch helpers defined next to the kernel (kernels.cu).
+cudaError_t configure_kernel();
+cudaError_t max_blocks_per_sm(int* n);
+cudaError_t launch_fused(const Params& p, int grid, bool cooperative, cudaStream_t stream);
+
+}  // namespace tpo
