@@ -1,0 +1,619 @@
+// Fused persistent kernel of libtpoverlap (sm_103a).
+//
+// One launch carries two roles, split by block index:
+//
+//  * producer CTAs [0, num_producers): the ring-order chunk producer.  Each
+//    arriving rank chunk is a contiguous byte range; every producer CTA moves
+//    its share with bulk asynchronous copies (global -> shared -> global, 16 KiB
+//    pieces through a ring of shared buffers, full-line coalesced writes) and
+//    then adds 1 to the slot's counter with release semantics.  This is the role
+//    of userbuffers_send/recv plus producer() in TransformerEngine's
+//    atomic_gemm_overlap_ag listing (issue "curious about
+//    atomic_gemm_overlap_ag"), with the copy moved onto a few SMs.
+//
+//  * GEMM CTAs: a persistent tcgen05 GEMM.  Warp 0 issues TMA loads (after an
+//    acquire-wait on the slot's counter for gathered rows), warp 1 issues
+//    tcgen05.mma from one thread into a double-buffered fp32 accumulator in
+//    tensor memory, warps 2..5 drain the accumulator (tcgen05.ld), round to
+//    bf16 and TMA-store the tile.  This replaces the counter-gated cuBLAS
+//    atomic GEMM of the same listing.  For GEMM+RS / GEMM+AR the K loop of a
+//    tile walks the ranks' K-slices in a fixed ring order into one accumulator.
+//
+// Every wait (mbarrier, chunk counter) is bounded by the device global timer.
+// On expiry the waiting thread records the failure in the context's error word
+// and the CTA winds down: it waits for its own copies in flight, lets issued
+// MMAs finish, frees its tensor memory and exits.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tpo_params.h"
+
+namespace tpo {
+
+// ------------------------------------------------------------------ helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long gtime() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool aborted(const Params& p) {
+  return *reinterpret_cast<volatile uint32_t*>(&p.words->err[0]) != 0u;
+}
+
+__device__ void raise_error(const Params& p, uint32_t code, uint32_t site, uint32_t extra) {
+  if (atomicCAS(&p.words->err[0], 0u, code) == 0u) {
+    p.words->err[1] = site;
+    p.words->err[2] = blockIdx.x;
+    p.words->err[3] = extra;
+    __threadfence();
+  }
+}
+
+// ------------------------------------------------------------------ mbarrier
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+// Bounded wait for the phase of parity `parity` to complete.  With
+// `honor_abort`, a failure recorded by any CTA also ends the wait (false).
+__device__ bool mbar_wait(const Params& p, uint32_t bar, uint32_t parity, uint32_t site, bool honor_abort) {
+  if (mbar_test(bar, parity)) return true;
+  const unsigned long long t0 = gtime();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 15u) == 0u) {
+      if (honor_abort && aborted(p)) return false;
+      if (gtime() - t0 > p.timeout_ns) {
+        raise_error(p, DEV_TIMEOUT, site, blockIdx.x);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ bulk copies / TMA
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// ------------------------------------------------------------------ release / acquire
+
+__device__ __forceinline__ void red_add_release(uint32_t* ptr, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add_release(uint32_t* ptr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+// ------------------------------------------------------------------ tcgen05
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA with
+// the 128-byte swizzle: rows of 128 bytes, 8-row swizzle atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);  // start address, 16-byte units
+  d |= static_cast<uint64_t>(1) << 16;                 // leading byte offset (unused when swizzled)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;         // stride byte offset: one 8-row atom
+  d |= static_cast<uint64_t>(1) << 46;                 // descriptor version (tcgen05)
+  d |= static_cast<uint64_t>(2) << 61;                 // swizzle mode: 128 bytes
+  return d;
+}
+
+// Instruction descriptor: dense, fp32 accumulator, K-major A and B,
+// A/B bf16 (kind::f16) or e4m3 (kind::f8f6f4), M = BM, N = BN.
+__host__ __device__ constexpr uint32_t make_idesc(bool fp8) {
+  return (1u << 4) | ((fp8 ? 0u : 1u) << 7) | ((fp8 ? 0u : 1u) << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "setp.ne.b32 P, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, P;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_e4m3(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "setp.ne.b32 P, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, P;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ tile schedule
+
+struct Tile {
+  int a_map;  // AG: 0 staging, 1 X_self
+  int a_row;  // row coordinate of the A tile in its map
+  int gate;   // slot whose counter gates the A loads, or -1
+  int y_map;  // output map index
+  int y_row;  // row coordinate of the output tile in its map
+  int col;    // first output column (= first W row)
+  int seg0;   // RS/AR: rank of the first K segment
+  int group;  // AR: row chunk
+};
+
+// Tiles are ordered group by group (AG: ring step, RS: owner block, AR: row
+// chunk); inside a group column-tile-major so that consecutive CTAs share the
+// same W tile.  Every role of a CTA walks the same sequence t = g, g+G, ...
+__device__ __forceinline__ Tile tile_at(const Params& p, int t) {
+  const int per_group = p.row_tiles * p.col_tiles;
+  const int grp = t / per_group;
+  const int rem = t - grp * per_group;
+  const int c = rem / p.row_tiles;
+  const int r = rem - c * p.row_tiles;
+  Tile T;
+  T.col = c * BN;
+  T.group = grp;
+  if (p.op == OP_AG) {
+    const int slot = ((p.self_rank - grp) % p.tp + p.tp) % p.tp;
+    // ring step 0 is the observer's own chunk: read in place, nothing to wait on
+    T.a_map = (grp == 0) ? 1 : 0;
+    T.a_row = (grp == 0) ? r * BM : slot * p.rows_per_group + r * BM;
+    T.gate = (grp == 0 || !p.gate) ? -1 : slot;
+    T.y_map = 0;
+    T.y_row = slot * p.rows_per_group + r * BM;
+    T.seg0 = 0;
+  } else if (p.op == OP_RS) {
+    T.a_map = -1;
+    T.a_row = grp * p.rows_per_group + r * BM;
+    T.gate = -1;
+    T.y_map = grp;
+    T.y_row = r * BM;
+    T.seg0 = (grp + 1) % p.tp;  // ring reduce-scatter: the owner's own slice comes last
+  } else {
+    const int local = r * BM;
+    const int owner = (local * p.tp) / p.rows_per_group;  // part of the chunk owned in a ring all-reduce
+    T.a_map = -1;
+    T.a_row = grp * p.rows_per_group + local;
+    T.gate = -1;
+    T.y_map = 0;
+    T.y_row = T.a_row;
+    T.seg0 = (owner + 1) % p.tp;
+  }
+  return T;
+}
+
+// ------------------------------------------------------------------ producer role
+
+__device__ __forceinline__ uint32_t piece_bytes(const Params& p, long long piece) {
+  const long long rem = p.chunk_bytes - piece * COPY_PIECE;
+  return static_cast<uint32_t>(rem < COPY_PIECE ? rem : COPY_PIECE);
+}
+
+// Copy pieces [lo, hi) of one chunk; `seq` numbers this CTA's loads across
+// chunks (buffer = seq % COPY_BUFS, phase parity = (seq / COPY_BUFS) & 1).
+__device__ bool copy_pieces(const Params& p, const uint8_t* src, uint8_t* dst, long long lo, long long hi,
+                            uint32_t sbase, uint32_t bars, unsigned long long seq) {
+  const long long np = hi - lo;
+  constexpr long long AHEAD = COPY_BUFS - COPY_LAG;
+  auto issue = [&](long long i) {
+    const unsigned long long s = seq + i;
+    const uint32_t b = static_cast<uint32_t>(s % COPY_BUFS);
+    const uint32_t bytes = piece_bytes(p, lo + i);
+    mbar_expect_tx(bars + 8u * b, bytes);
+    bulk_load(sbase + b * COPY_PIECE, src + (lo + i) * COPY_PIECE, bytes, bars + 8u * b);
+  };
+  for (long long i = 0; i < np && i < AHEAD; ++i) issue(i);
+  for (long long i = 0; i < np; ++i) {
+    const unsigned long long s = seq + i;
+    const uint32_t b = static_cast<uint32_t>(s % COPY_BUFS);
+    if (!mbar_wait(p, bars + 8u * b, static_cast<uint32_t>((s / COPY_BUFS) & 1u), SITE_COPY, true)) {
+      for (long long j = i; j < np && j < i + AHEAD; ++j) {  // loads still in flight
+        const unsigned long long sj = seq + j;
+        mbar_wait(p, bars + 8u * static_cast<uint32_t>(sj % COPY_BUFS),
+                  static_cast<uint32_t>((sj / COPY_BUFS) & 1u), SITE_DRAIN, false);
+      }
+      bulk_wait<0>();
+      return false;
+    }
+    bulk_store(dst + (lo + i) * COPY_PIECE, sbase + b * COPY_PIECE, piece_bytes(p, lo + i));
+    bulk_commit();
+    if (i + AHEAD < np) {
+      bulk_wait_read<COPY_LAG>();  // the store that last read buffer (i + AHEAD) % COPY_BUFS is done
+      issue(i + AHEAD);
+    }
+  }
+  return true;
+}
+
+__device__ void producer_role(const Params& p, uint8_t* smem) {
+  if (threadIdx.x != 0) return;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + SMEM_BARS + 8u * (2 * STAGES + 5);
+  for (int b = 0; b < COPY_BUFS; ++b) mbar_init(bars + 8u * b, 1);
+  fence_barrier_init();
+
+  const long long pieces = (p.chunk_bytes + COPY_PIECE - 1) / COPY_PIECE;
+  const long long P = p.num_producers, pid = blockIdx.x;
+  const long long lo = pieces * pid / P, hi = pieces * (pid + 1) / P;
+  unsigned long long seq = 0;
+  // Ring steps 1 .. tp-1 in arrival order, then step 0 (the observer's own
+  // chunk, which the GEMM reads in place, copied last into its slot).
+  for (int si = 0; si < p.tp; ++si) {
+    const int step = (si + 1) % p.tp;
+    if (p.last_step >= 0 && step > p.last_step) continue;
+    const int slot = ((p.self_rank - step) % p.tp + p.tp) % p.tp;
+    const uint8_t* src = p.src[slot];
+    uint8_t* dst = p.staging + static_cast<long long>(slot) * p.chunk_bytes;
+    if (!copy_pieces(p, src, dst, lo, hi, sbase, bars, seq)) return;
+    seq += static_cast<unsigned long long>(hi - lo);
+    bulk_wait<0>();  // this CTA's writes of the chunk are complete
+    fence_proxy_async_global();
+    if (p.delay_ns) {
+      const unsigned long long t0 = gtime();
+      while (gtime() - t0 < p.delay_ns) __nanosleep(256);
+    }
+    if (slot != p.skip_slot) red_add_release(&p.words->counters[slot], 1u);
+    if (p.trace_on) atomicMax(&p.words->trace[TPO_TRACE_PUBLISH + slot], gtime());
+  }
+}
+
+// ------------------------------------------------------------------ GEMM role
+
+__device__ bool wait_counter(const Params& p, int slot) {
+  const uint32_t* c = &p.words->counters[slot];
+  const unsigned long long t0 = gtime();
+  bool waited = false;
+  while (static_cast<int>(ld_acquire(c) - p.target) < 0) {
+    waited = true;
+    if (aborted(p)) return false;
+    if (gtime() - t0 > p.timeout_ns) {
+      raise_error(p, DEV_TIMEOUT, SITE_COUNTER, static_cast<uint32_t>(slot));
+      return false;
+    }
+    __nanosleep(64);
+  }
+  fence_proxy_async_global();  // order the acquire before the tensor (async-proxy) loads
+  if (p.trace_on) {
+    const unsigned long long t1 = gtime();
+    atomicMin(&p.words->trace[TPO_TRACE_ACQUIRE + slot], t1);
+    if (waited) atomicAdd(&p.words->trace[TPO_TRACE_WAIT_NS], t1 - t0);
+  }
+  return true;
+}
+
+struct Bars {
+  uint32_t full0, empty0, tfull0, tempty0, drain;
+};
+
+__device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, int g, int G, int total_tiles, int nkb) {
+  const int kelems = p.fp8 ? BK_BYTES : BK_BYTES / 2;
+  uint32_t ready = 0;
+  uint32_t it = 0;
+  bool ok = true;
+  for (int t = g; t < total_tiles && ok; t += G) {
+    const Tile T = tile_at(p, t);
+    if (T.gate >= 0 && !((ready >> T.gate) & 1u)) {
+      if (!wait_counter(p, T.gate)) {
+        ok = false;
+        break;
+      }
+      ready |= 1u << T.gate;
+    }
+    for (int i = 0; i < nkb; ++i) {
+      const uint32_t stage = it % STAGES;
+      if (!mbar_wait(p, B.empty0 + 8u * stage, ((it / STAGES) & 1u) ^ 1u, SITE_EMPTY, true)) {
+        ok = false;
+        break;
+      }
+      const int seg = i / p.kb_per_seg;
+      const int kk = i - seg * p.kb_per_seg;
+      const int amap = (p.op == OP_AG) ? T.a_map : (T.seg0 + seg) % p.tp;
+      const int bmap = (p.op == OP_AG) ? 0 : amap;
+      const uint32_t sa = sbase + SMEM_STAGES + stage * STAGE_BYTES;
+      const uint32_t full = B.full0 + 8u * stage;
+      mbar_expect_tx(full, STAGE_BYTES);
+      tma_load_2d(sa, &p.mapA[amap], full, kk * kelems, T.a_row);
+      tma_load_2d(sa + A_STAGE_BYTES, &p.mapB[bmap], full, kk * kelems, T.col);
+      ++it;
+    }
+  }
+  if (!ok) {  // loads already issued must land before the CTA releases its shared memory
+    const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
+    for (uint32_t j = first; j < it; ++j)
+      mbar_wait(p, B.full0 + 8u * (j % STAGES), (j / STAGES) & 1u, SITE_DRAIN, false);
+  }
+}
+
+__device__ void mma_role(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
+                         int total_tiles, int nkb) {
+  const uint32_t idesc = make_idesc(p.fp8 != 0);
+  uint32_t it = 0, lt = 0;
+  bool ok = true;
+  for (int t = g; t < total_tiles; t += G, ++lt) {
+    const uint32_t acc = lt & 1u;
+    if (!mbar_wait(p, B.tempty0 + 8u * acc, ((lt >> 1) & 1u) ^ 1u, SITE_TMEM_EMPTY, true)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d = tmem + acc * BN;
+    for (int i = 0; i < nkb; ++i, ++it) {
+      const uint32_t stage = it % STAGES;
+      if (!mbar_wait(p, B.full0 + 8u * stage, (it / STAGES) & 1u, SITE_FULL, true)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sa = sbase + SMEM_STAGES + stage * STAGE_BYTES;
+      const uint64_t da = smem_desc_sw128(sa);
+      const uint64_t db = smem_desc_sw128(sa + A_STAGE_BYTES);
+      // four MMAs of K = 32 bytes each cover the 128-byte K block
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint32_t accum = (i > 0 || kk > 0) ? 1u : 0u;
+        if (p.fp8)
+          mma_e4m3(d, da + 2u * kk, db + 2u * kk, idesc, accum);
+        else
+          mma_bf16(d, da + 2u * kk, db + 2u * kk, idesc, accum);
+      }
+      mma_commit(B.empty0 + 8u * stage);  // frees the stage once these MMAs have read it
+    }
+    if (!ok) break;
+    mma_commit(B.tfull0 + 8u * acc);  // accumulator ready for the epilogue
+  }
+  if (!ok) {  // every MMA issued so far must complete before tensor memory is freed
+    mma_commit(B.drain);
+    mbar_wait(p, B.drain, 0u, SITE_DRAIN, false);
+  }
+}
+
+__device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, const Bars& B, int g, int G,
+                              int total_tiles) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3;  // tensor-memory lanes this warp may read: [32*quad, 32*quad+32)
+  const uint32_t ebase = smem_u32(smem + SMEM_EPI + (warp - 2) * 2 * EPI_BUF_BYTES);
+  const float scale = p.fp8 ? (__ldg(p.scale_x) * __ldg(p.scale_w)) : 1.0f;
+  uint32_t lt = 0, nst = 0;
+  for (int t = g; t < total_tiles; t += G, ++lt) {
+    const Tile T = tile_at(p, t);
+    const uint32_t acc = lt & 1u;
+    const uint32_t bar = B.tfull0 + 8u * acc, par = (lt >> 1) & 1u;
+    int ok = (lane == 0) ? (mbar_wait(p, bar, par, SITE_TMEM_FULL, true) ? 1 : 0) : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
+    while (!mbar_test(bar, par)) {
+    }  // already complete: gives every lane the barrier's ordering
+    tc_fence_after();
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN / EPI_COLS; ++c, ++nst) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c * EPI_COLS, r);
+      tmem_wait_ld();
+      if (c == BN / EPI_COLS - 1) {  // accumulator fully read: hand it back to the MMA warp
+        tc_fence_before();
+        mbar_arrive(B.tempty0 + 8u * acc);
+      }
+      uint32_t packed[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const __nv_bfloat162 h =
+            __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * scale, __uint_as_float(r[2 * j + 1]) * scale);
+        packed[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      const uint32_t buf = ebase + (nst & 1u) * EPI_BUF_BYTES;
+      if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer two boxes ago has read it
+      __syncwarp();
+      // row `lane` of a 32 x 64-byte box in the 64-byte swizzle layout the
+      // output tensor map expects (16-byte chunk index XOR (row / 2) % 4)
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const uint32_t addr = buf + lane * 64 + (static_cast<uint32_t>(ch ^ ((lane >> 1) & 3)) << 4);
+        st_shared_v4(addr, packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.mapY[T.y_map], buf, T.col + c * EPI_COLS, T.y_row + quad * 32);
+        bulk_commit();
+      }
+    }
+    if (p.op == OP_AR && lane == 0) {  // this warp's rows of the tile are in memory: count them
+      bulk_wait<0>();
+      fence_proxy_async_global();
+      const uint32_t old = atom_add_release(&p.words->ar_done[T.group], 1u);
+      if (p.trace_on && old + 1u == p.ar_target) p.words->trace[TPO_TRACE_CHUNK_DONE + T.group] = gtime();
+    }
+  }
+  if (lane == 0) bulk_wait<0>();
+  __syncwarp();
+}
+
+__device__ void gemm_role(const Params& p, uint8_t* smem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  Bars B;
+  B.full0 = sbase + SMEM_BARS;
+  B.empty0 = B.full0 + 8u * STAGES;
+  B.tfull0 = B.empty0 + 8u * STAGES;
+  B.tempty0 = B.tfull0 + 16u;
+  B.drain = B.tempty0 + 16u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_TMEM_SLOT);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(B.full0 + 8u * s, 1);
+      mbar_init(B.empty0 + 8u * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(B.tfull0 + 8u * a, 1);
+      mbar_init(B.tempty0 + 8u * a, EPI_WARPS * 32);
+    }
+    mbar_init(B.drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+  const int g = blockIdx.x - p.num_producers, G = p.num_gemm;
+  const int total_tiles = p.num_groups * p.row_tiles * p.col_tiles;
+  const int nkb = p.num_segs * p.kb_per_seg;
+  if (warp == 0) {
+    if (lane == 0) tma_role(p, sbase, B, g, G, total_tiles, nkb);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) mma_role(p, sbase, tmem, B, g, G, total_tiles, nkb);
+    __syncwarp();
+  } else {
+    epilogue_role(p, smem, tmem, B, g, G, total_tiles);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) fused_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  if (p.trace_on && threadIdx.x == 0) atomicMin(&p.words->trace[TPO_TRACE_START], gtime());
+  if (static_cast<int>(blockIdx.x) < p.num_producers) {
+    producer_role(p, smem);
+  } else if (static_cast<int>(blockIdx.x) < p.num_producers + p.num_gemm) {
+    gemm_role(p, smem);
+  }
+  if (p.trace_on && threadIdx.x == 0) atomicMax(&p.words->trace[TPO_TRACE_END], gtime());
+}
+
+// ------------------------------------------------------------------ host side launch
+
+cudaError_t configure_kernel() {
+  return cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+}
+
+cudaError_t max_blocks_per_sm(int* n) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fused_kernel, NUM_THREADS, SMEM_ALLOC);
+}
+
+cudaError_t launch_fused(const Params& p, int grid, bool cooperative, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cooperative ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fused_kernel, p);
+}
+
+}  // namespace tpo
