@@ -1,0 +1,577 @@
+// Host side of libtpoverlap: context, argument validation, tensor maps and the
+// launch schedule of each operation.  See include/tpoverlap.h for the contract.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cctype>
+#include <cstdarg>
+#include <cstddef>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "tpo_params.h"
+#include "tpoverlap.h"
+
+using tpo::Params;
+
+namespace {
+
+thread_local std::string g_err;
+
+tpo_status fail(tpo_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+tpo_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(TPO_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D row-major tensor [outer, inner] of `elem` bytes per element.
+bool encode2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem, uint64_t inner, uint64_t outer,
+              uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * static_cast<uint64_t>(elem)};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct OptDesc {
+  const char* key;
+  int64_t lo, hi;
+};
+
+}  // namespace
+
+struct tpo_ctx {
+  int tp = 0;
+  int64_t n = 0, k = 0, m = 0;
+  int dtype = 0;
+  int device = 0;
+  int num_sms = 0;
+  int max_coop_grid = 0;
+  // options
+  int64_t producer_sms = 8, gemm_ctas = 0, mode = 0, seq_copy_ctas = 0, self_rank = 0, wait_timeout_ms = 2000,
+          trace = 0, debug_skip_chunk = -1, debug_delay_ns = 0, debug_last_step = -1;
+  // device memory
+  uint8_t* staging = nullptr;
+  size_t staging_bytes = 0;
+  tpo::DevWords* words = nullptr;
+  uint32_t target = 0;     // counter value meaning "published by the latest call"
+  uint32_t ar_target = 0;  // AR done-counter value after the latest call
+  int ar_chunks = 0;       // row-chunk count of the latest AR call
+  cudaStream_t aux = nullptr;
+  cudaEvent_t last = nullptr;
+  bool has_last = false;
+  uint32_t last_dev_err[4] = {0, 0, 0, 0};
+  // tensor-map cache: the Params of the latest call of each op, keyed by pointers
+  Params cache[3];
+  const void* cache_key[3][3 * TPO_MAX_TP + 1];
+  bool cache_valid[3] = {false, false, false};
+};
+
+namespace {
+
+int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
+  struct E {
+    const char* k;
+    int64_t tpo_ctx::*f;
+    int64_t lo, hi;
+  };
+  const E table[] = {
+      {"producer_sms", &tpo_ctx::producer_sms, 1, 1024},
+      {"gemm_ctas", &tpo_ctx::gemm_ctas, 0, 1 << 20},
+      {"mode", &tpo_ctx::mode, 0, 3},
+      {"seq_copy_ctas", &tpo_ctx::seq_copy_ctas, 0, 1 << 20},
+      {"self_rank", &tpo_ctx::self_rank, 0, TPO_MAX_TP - 1},
+      {"wait_timeout_ms", &tpo_ctx::wait_timeout_ms, 1, 600000},
+      {"trace", &tpo_ctx::trace, 0, 1},
+      {"debug_skip_chunk", &tpo_ctx::debug_skip_chunk, -1, TPO_MAX_TP - 1},
+      {"debug_delay_ns", &tpo_ctx::debug_delay_ns, 0, 1000000000},
+      {"debug_last_step", &tpo_ctx::debug_last_step, -1, TPO_MAX_TP - 1},
+  };
+  for (const E& e : table)
+    if (std::strcmp(e.k, key) == 0) {
+      *lo = e.lo;
+      *hi = e.hi;
+      if (std::strcmp(key, "self_rank") == 0 || std::strcmp(key, "debug_skip_chunk") == 0 ||
+          std::strcmp(key, "debug_last_step") == 0)
+        *hi = c->tp - 1;
+      return &(c->*(e.f));
+    }
+  return nullptr;
+}
+
+const char* kOptKeys[] = {"producer_sms",   "gemm_ctas", "mode",  "seq_copy_ctas",    "self_rank",
+                          "wait_timeout_ms", "trace",     "debug_skip_chunk", "debug_delay_ns", "debug_last_step"};
+
+void destroy_all(tpo_ctx* c) {
+  if (!c) return;
+  if (c->has_last) cudaEventSynchronize(c->last);
+  if (c->aux) cudaStreamSynchronize(c->aux);
+  if (c->staging) cudaFree(c->staging);
+  if (c->words) cudaFree(c->words);
+  if (c->last) cudaEventDestroy(c->last);
+  if (c->aux) cudaStreamDestroy(c->aux);
+  delete c;
+}
+
+// Fill the fields common to every launch.
+void base_params(const tpo_ctx* c, Params& p) {
+  p.words = c->words;
+  p.staging = c->staging;
+  p.timeout_ns = static_cast<unsigned long long>(c->wait_timeout_ms) * 1000000ull;
+  p.delay_ns = static_cast<unsigned long long>(c->debug_delay_ns);
+  p.skip_slot = static_cast<int>(c->debug_skip_chunk);
+  p.last_step = static_cast<int>(c->debug_last_step);
+  p.trace_on = static_cast<int>(c->trace);
+  p.self_rank = static_cast<int>(c->self_rank);
+  p.tp = c->tp;
+  p.fp8 = c->dtype == TPO_FP8_E4M3;
+}
+
+tpo_status reset_trace(tpo_ctx* c, cudaStream_t s) {
+  if (!c->trace) return TPO_OK;
+  unsigned long long* tr = c->words->trace;
+  cudaError_t e = cudaMemsetAsync(tr, 0, sizeof(unsigned long long) * TPO_TRACE_WORDS, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(tr + TPO_TRACE_START, 0xFF, sizeof(unsigned long long), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(tr + TPO_TRACE_ACQUIRE, 0xFF, sizeof(unsigned long long) * TPO_MAX_TP, s);
+  return e == cudaSuccess ? TPO_OK : cuda_fail(e, "trace reset");
+}
+
+tpo_status launch(tpo_ctx* c, const Params& p, int grid, bool coop, cudaStream_t s) {
+  cudaError_t e = tpo::launch_fused(p, grid, coop, s);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  e = cudaEventRecord(c->last, s);
+  if (e != cudaSuccess) return cuda_fail(e, "event record");
+  c->has_last = true;
+  return TPO_OK;
+}
+
+bool cache_lookup(tpo_ctx* c, int op, const void* const* key, int nkey, Params& p) {
+  if (!c->cache_valid[op]) return false;
+  for (int i = 0; i < nkey; ++i)
+    if (c->cache_key[op][i] != key[i]) return false;
+  std::memcpy(p.mapA, c->cache[op].mapA, sizeof(p.mapA));
+  std::memcpy(p.mapB, c->cache[op].mapB, sizeof(p.mapB));
+  std::memcpy(p.mapY, c->cache[op].mapY, sizeof(p.mapY));
+  return true;
+}
+
+void cache_store(tpo_ctx* c, int op, const void* const* key, int nkey, const Params& p) {
+  for (int i = 0; i < nkey; ++i) c->cache_key[op][i] = key[i];
+  std::memcpy(c->cache[op].mapA, p.mapA, sizeof(p.mapA));
+  std::memcpy(c->cache[op].mapB, p.mapB, sizeof(p.mapB));
+  std::memcpy(c->cache[op].mapY, p.mapY, sizeof(p.mapY));
+  c->cache_valid[op] = true;
+}
+
+int clamp_grid(int64_t want, int total_tiles) {
+  if (want > total_tiles) want = total_tiles;
+  return static_cast<int>(want < 1 ? 1 : want);
+}
+
+// Validation shared by RS and AR.
+tpo_status check_ksplit(tpo_ctx* c, const void* const* x, const void* const* w) {
+  if (c->dtype != TPO_BF16) return fail(TPO_ERR_UNSUPPORTED, "GEMM+RS/AR supports bf16 contexts only");
+  if (c->k % c->tp != 0 || (c->k / c->tp) % 64 != 0)
+    return fail(TPO_ERR_UNSUPPORTED, "k/tp must be an integer multiple of 64 (k=%lld, tp=%d)", (long long)c->k,
+                c->tp);
+  if (!x || !w) return fail(TPO_ERR_INVALID_ARG, "x and w must be arrays of tp device pointers");
+  for (int r = 0; r < c->tp; ++r)
+    if (!aligned16(x[r]) || !aligned16(w[r]))
+      return fail(TPO_ERR_INVALID_ARG, "x[%d] / w[%d] must be non-NULL and 16-byte aligned", r, r);
+  return TPO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tpo_last_error(void) { return g_err.c_str(); }
+
+const char* tpo_version(void) {
+  static char v[128];
+  std::snprintf(v, sizeof(v), "libtpoverlap 0.1 (nvcc %d.%d, sm_103a, tcgen05)", __CUDACC_VER_MAJOR__,
+                __CUDACC_VER_MINOR__);
+  return v;
+}
+
+tpo_ctx* tpo_ctx_create(int tp, int64_t n, int64_t k, int64_t m, int dtype) {
+  if (tp < 1 || tp > TPO_MAX_TP) {
+    fail(TPO_ERR_INVALID_ARG, "tp=%d out of range [1, %d]", tp, TPO_MAX_TP);
+    return nullptr;
+  }
+  if (dtype != TPO_BF16 && dtype != TPO_FP8_E4M3) {
+    fail(TPO_ERR_INVALID_ARG, "dtype=%d is neither TPO_BF16 (0) nor TPO_FP8_E4M3 (1)", dtype);
+    return nullptr;
+  }
+  if (n <= 0 || k <= 0 || m <= 0 || n > (1ll << 30) || k > (1ll << 30) || m > (1ll << 30)) {
+    fail(TPO_ERR_INVALID_ARG, "sizes must be in [1, 2^30] (n=%lld k=%lld m=%lld)", (long long)n, (long long)k,
+         (long long)m);
+    return nullptr;
+  }
+  if (n % (static_cast<int64_t>(tp) * tpo::BM) != 0) {
+    fail(TPO_ERR_UNSUPPORTED, "n=%lld must be a multiple of tp*%d=%lld", (long long)n, tpo::BM,
+         (long long)tp * tpo::BM);
+    return nullptr;
+  }
+  if (m % tpo::BN != 0) {
+    fail(TPO_ERR_UNSUPPORTED, "m=%lld must be a multiple of %d", (long long)m, tpo::BN);
+    return nullptr;
+  }
+  const int kq = dtype == TPO_BF16 ? 64 : 128;
+  if (k % kq != 0) {
+    fail(TPO_ERR_UNSUPPORTED, "k=%lld must be a multiple of %d for this dtype", (long long)k, kq);
+    return nullptr;
+  }
+  tpo_ctx* c = new tpo_ctx();
+  c->tp = tp;
+  c->n = n;
+  c->k = k;
+  c->m = m;
+  c->dtype = dtype;
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "no usable CUDA device");
+    destroy_all(c);
+    return nullptr;
+  }
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, c->device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, c->device);
+  if (major != 10 || minor != 3) {
+    fail(TPO_ERR_UNSUPPORTED, "this build targets sm_103a; device is sm_%d%d", major, minor);
+    destroy_all(c);
+    return nullptr;
+  }
+  if (!load_encode()) {
+    fail(TPO_ERR_CUDA, "driver entry point cuTensorMapEncodeTiled unavailable");
+    destroy_all(c);
+    return nullptr;
+  }
+  int per_sm = 0;
+  e = tpo::configure_kernel();
+  if (e == cudaSuccess) e = tpo::max_blocks_per_sm(&per_sm);
+  if (e != cudaSuccess || per_sm < 1) {
+    if (e != cudaSuccess)
+      cuda_fail(e, "kernel configuration");
+    else
+      fail(TPO_ERR_CUDA, "kernel does not fit on an SM");
+    destroy_all(c);
+    return nullptr;
+  }
+  c->max_coop_grid = per_sm * c->num_sms;
+  const int elem = dtype == TPO_BF16 ? 2 : 1;
+  c->staging_bytes = static_cast<size_t>(n) * static_cast<size_t>(k) * elem;
+  e = cudaMalloc(&c->staging, c->staging_bytes);
+  if (e != cudaSuccess) {
+    fail(TPO_ERR_OOM, "staging buffer of %zu bytes: %s", c->staging_bytes, cudaGetErrorString(e));
+    cudaGetLastError();
+    destroy_all(c);
+    return nullptr;
+  }
+  e = cudaMalloc(&c->words, sizeof(tpo::DevWords));
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->last, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->words, 0, sizeof(tpo::DevWords), c->aux);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c->aux);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "context set-up");
+    destroy_all(c);
+    return nullptr;
+  }
+  // environment overrides of the option defaults
+  for (const char* key : kOptKeys) {
+    char env[64] = "TPO_";
+    size_t j = 4;
+    for (const char* s = key; *s && j + 1 < sizeof(env); ++s) env[j++] = static_cast<char>(std::toupper(*s));
+    env[j] = 0;
+    if (const char* v = std::getenv(env)) {
+      if (tpo_set_opt(c, key, std::strtoll(v, nullptr, 10)) != TPO_OK) {
+        destroy_all(c);
+        return nullptr;
+      }
+    }
+  }
+  return c;
+}
+
+tpo_status tpo_ctx_destroy(tpo_ctx* c) {
+  destroy_all(c);
+  return TPO_OK;
+}
+
+tpo_status tpo_set_opt(tpo_ctx* c, const char* key, int64_t value) {
+  if (!c || !key) return fail(TPO_ERR_INVALID_ARG, "NULL context or key");
+  int64_t lo, hi;
+  int64_t* f = opt_slot(c, key, &lo, &hi);
+  if (!f) return fail(TPO_ERR_INVALID_ARG, "unknown option '%s'", key);
+  if (value < lo || value > hi)
+    return fail(TPO_ERR_INVALID_ARG, "option '%s'=%lld outside [%lld, %lld]", key, (long long)value, (long long)lo,
+                (long long)hi);
+  *f = value;
+  return TPO_OK;
+}
+
+tpo_status tpo_get_opt(tpo_ctx* c, const char* key, int64_t* value) {
+  if (!c || !key || !value) return fail(TPO_ERR_INVALID_ARG, "NULL argument");
+  int64_t lo, hi;
+  int64_t* f = opt_slot(c, key, &lo, &hi);
+  if (!f) return fail(TPO_ERR_INVALID_ARG, "unknown option '%s'", key);
+  *value = *f;
+  return TPO_OK;
+}
+
+tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y, const float* d_scale_inv_x,
+                       const float* d_scale_inv_w, void* stream) {
+  if (!c) return fail(TPO_ERR_INVALID_ARG, "NULL context");
+  if (!x) return fail(TPO_ERR_INVALID_ARG, "x must be an array of tp device pointers");
+  for (int r = 0; r < c->tp; ++r)
+    if (!aligned16(x[r])) return fail(TPO_ERR_INVALID_ARG, "x[%d] must be non-NULL and 16-byte aligned", r);
+  if (!aligned16(w) || !aligned16(y)) return fail(TPO_ERR_INVALID_ARG, "w and y must be non-NULL, 16-byte aligned");
+  const bool fp8 = c->dtype == TPO_FP8_E4M3;
+  if (fp8 && (!d_scale_inv_x || !d_scale_inv_w))
+    return fail(TPO_ERR_INVALID_ARG, "e4m3 contexts need both scale_inv device pointers");
+  if (!fp8 && (d_scale_inv_x || d_scale_inv_w))
+    return fail(TPO_ERR_INVALID_ARG, "bf16 contexts take no scale_inv pointers (pass NULL)");
+  if (c->self_rank >= c->tp) return fail(TPO_ERR_INVALID_ARG, "self_rank >= tp");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int elem = fp8 ? 1 : 2;
+  const int kel = tpo::BK_BYTES / elem;
+  const int64_t rows = c->n / c->tp;
+
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  base_params(c, p);
+  p.op = tpo::OP_AG;
+  const void* key[4] = {c->staging, x[c->self_rank], w, y};
+  if (!cache_lookup(c, tpo::OP_AG, key, 4, p)) {
+    const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    bool ok = encode2d(&p.mapA[0], c->staging, dt, elem, c->k, c->n, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode2d(&p.mapA[1], x[c->self_rank], dt, elem, c->k, rows, kel, tpo::BM,
+                       CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode2d(&p.mapB[0], w, dt, elem, c->k, c->m, kel, tpo::BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode2d(&p.mapY[0], y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->m, c->n, tpo::EPI_COLS, 32,
+                       CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!ok) return fail(TPO_ERR_INVALID_ARG, "tensor map encoding failed (pointer or size not TMA-compatible)");
+    cache_store(c, tpo::OP_AG, key, 4, p);
+  }
+  for (int r = 0; r < c->tp; ++r) p.src[r] = static_cast<const uint8_t*>(x[r]);
+  p.scale_x = d_scale_inv_x;
+  p.scale_w = d_scale_inv_w;
+  p.chunk_bytes = rows * c->k * elem;
+  p.rows_per_group = static_cast<int>(rows);
+  p.row_tiles = static_cast<int>(rows / tpo::BM);
+  p.col_tiles = static_cast<int>(c->m / tpo::BN);
+  p.num_groups = c->tp;
+  p.kb_per_seg = static_cast<int>(c->k * elem / tpo::BK_BYTES);
+  p.num_segs = 1;
+  p.gate = 1;
+  const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
+
+  tpo_status st = reset_trace(c, s);
+  if (st != TPO_OK) return st;
+  switch (c->mode) {
+    case 0: {  // overlapped: one cooperative launch, producer and GEMM co-resident
+      const int P = static_cast<int>(c->producer_sms);
+      const int G = clamp_grid(c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, tiles);
+      if (P < 1 || c->num_sms - P < 1 || P + G > c->max_coop_grid)
+        return fail(TPO_ERR_INVALID_ARG, "producer_sms=%d + gemm CTAs=%d exceed the %d co-resident CTAs", P, G,
+                    c->max_coop_grid);
+      c->target += static_cast<uint32_t>(P);
+      p.target = c->target;
+      p.num_producers = P;
+      p.num_gemm = G;
+      return launch(c, p, P + G, true, s);
+    }
+    case 1: {  // sequential: the copy to completion, then the same GEMM
+      const int Pc = static_cast<int>(c->seq_copy_ctas ? c->seq_copy_ctas : c->num_sms);
+      c->target += static_cast<uint32_t>(Pc);
+      p.target = c->target;
+      p.num_producers = Pc;
+      p.num_gemm = 0;
+      st = launch(c, p, Pc, false, s);
+      if (st != TPO_OK) return st;
+      p.num_producers = 0;
+      p.num_gemm = clamp_grid(c->gemm_ctas ? c->gemm_ctas : c->num_sms, tiles);
+      return launch(c, p, p.num_gemm, false, s);
+    }
+    case 2: {  // GEMM only: chunks published by an earlier call
+      p.target = c->target;
+      p.num_producers = 0;
+      p.num_gemm = clamp_grid(c->gemm_ctas ? c->gemm_ctas : c->num_sms, tiles);
+      return launch(c, p, p.num_gemm, false, s);
+    }
+    default: {  // producer only
+      const int P = static_cast<int>(c->producer_sms);
+      if (P > c->max_coop_grid) return fail(TPO_ERR_INVALID_ARG, "producer_sms too large");
+      c->target += static_cast<uint32_t>(P);
+      p.target = c->target;
+      p.num_producers = P;
+      p.num_gemm = 0;
+      return launch(c, p, P, false, s);
+    }
+  }
+}
+
+static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const void* const* w,
+                                void* const* yb, void* y, int n_chunks, cudaStream_t s) {
+  const int64_t kr = c->k / c->tp;
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  base_params(c, p);
+  p.op = op;
+  const void* key[3 * TPO_MAX_TP + 1];
+  int nkey = 0;
+  for (int r = 0; r < c->tp; ++r) {
+    key[nkey++] = x[r];
+    key[nkey++] = w[r];
+    key[nkey++] = (op == tpo::OP_RS) ? yb[r] : nullptr;
+  }
+  key[nkey++] = y;
+  if (!cache_lookup(c, op, key, nkey, p)) {
+    bool ok = true;
+    for (int r = 0; r < c->tp && ok; ++r) {
+      ok = encode2d(&p.mapA[r], x[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, c->n, 64, tpo::BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode2d(&p.mapB[r], w[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, c->m, 64, tpo::BN,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+      if (ok && op == tpo::OP_RS)
+        ok = encode2d(&p.mapY[r], yb[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->m, c->n / c->tp, tpo::EPI_COLS,
+                      32, CU_TENSOR_MAP_SWIZZLE_64B);
+    }
+    if (ok && op == tpo::OP_AR)
+      ok = encode2d(&p.mapY[0], y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->m, c->n, tpo::EPI_COLS, 32,
+                    CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!ok) return fail(TPO_ERR_INVALID_ARG, "tensor map encoding failed (pointer or size not TMA-compatible)");
+    cache_store(c, op, key, nkey, p);
+  }
+  const int groups = (op == tpo::OP_RS) ? c->tp : n_chunks;
+  p.rows_per_group = static_cast<int>(c->n / groups);
+  p.row_tiles = p.rows_per_group / tpo::BM;
+  p.col_tiles = static_cast<int>(c->m / tpo::BN);
+  p.num_groups = groups;
+  p.kb_per_seg = static_cast<int>(kr * 2 / tpo::BK_BYTES);
+  p.num_segs = c->tp;
+  p.gate = 0;
+  const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
+  tpo_status st = reset_trace(c, s);
+  if (st != TPO_OK) return st;
+  if (op == tpo::OP_AR) {
+    if (n_chunks != c->ar_chunks) {  // keep every chunk's done counter on the same target
+      cudaError_t e = cudaMemsetAsync(c->words->ar_done, 0, sizeof(c->words->ar_done), s);
+      if (e != cudaSuccess) return cuda_fail(e, "done-counter reset");
+      c->ar_target = 0;
+      c->ar_chunks = n_chunks;
+    }
+    c->ar_target += static_cast<uint32_t>(p.row_tiles * p.col_tiles * tpo::EPI_WARPS);
+    p.ar_target = c->ar_target;
+  }
+  p.num_producers = 0;
+  p.num_gemm = clamp_grid(c->gemm_ctas ? c->gemm_ctas : c->num_sms, tiles);
+  return launch(c, p, p.num_gemm, false, s);
+}
+
+tpo_status tpo_gemm_rs(tpo_ctx* c, const void* const* x, const void* const* w, void* const* y, void* stream) {
+  if (!c) return fail(TPO_ERR_INVALID_ARG, "NULL context");
+  tpo_status st = check_ksplit(c, x, w);
+  if (st != TPO_OK) return st;
+  if (!y) return fail(TPO_ERR_INVALID_ARG, "y must be an array of tp device pointers");
+  for (int r = 0; r < c->tp; ++r)
+    if (!aligned16(y[r])) return fail(TPO_ERR_INVALID_ARG, "y[%d] must be non-NULL and 16-byte aligned", r);
+  return ksplit_common(c, tpo::OP_RS, x, w, y, nullptr, c->tp, static_cast<cudaStream_t>(stream));
+}
+
+tpo_status tpo_gemm_ar(tpo_ctx* c, const void* const* x, const void* const* w, void* y, int n_row_chunks,
+                       void* stream) {
+  if (!c) return fail(TPO_ERR_INVALID_ARG, "NULL context");
+  tpo_status st = check_ksplit(c, x, w);
+  if (st != TPO_OK) return st;
+  if (!aligned16(y)) return fail(TPO_ERR_INVALID_ARG, "y must be non-NULL and 16-byte aligned");
+  if (n_row_chunks < 1 || n_row_chunks > TPO_MAX_ROW_CHUNKS)
+    return fail(TPO_ERR_INVALID_ARG, "n_row_chunks=%d outside [1, %d]", n_row_chunks, TPO_MAX_ROW_CHUNKS);
+  if (c->n % (static_cast<int64_t>(n_row_chunks) * c->tp * tpo::BM) != 0)
+    return fail(TPO_ERR_UNSUPPORTED, "n=%lld must be a multiple of n_row_chunks*tp*%d", (long long)c->n, tpo::BM);
+  return ksplit_common(c, tpo::OP_AR, x, w, nullptr, y, n_row_chunks, static_cast<cudaStream_t>(stream));
+}
+
+tpo_status tpo_sync_status(tpo_ctx* c) {
+  if (!c) return fail(TPO_ERR_INVALID_ARG, "NULL context");
+  cudaError_t e = cudaSuccess;
+  if (c->has_last) e = cudaEventSynchronize(c->last);
+  if (e != cudaSuccess) return cuda_fail(e, "synchronise");
+  uint32_t err[4];
+  e = cudaMemcpyAsync(err, c->words->err, sizeof(err), cudaMemcpyDeviceToHost, c->aux);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c->aux);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (err[0] == tpo::DEV_OK) return TPO_OK;
+  std::memcpy(c->last_dev_err, err, sizeof(err));
+  // make the context usable again: counters and error word back to zero
+  e = cudaMemsetAsync(c->words, 0, offsetof(tpo::DevWords, pad), c->aux);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c->aux);
+  if (e != cudaSuccess) return cuda_fail(e, "reset after device failure");
+  c->target = 0;
+  c->ar_target = 0;
+  c->ar_chunks = 0;
+  return fail(TPO_ERR_TIMEOUT, "device wait timed out (site %u, block %u, extra %u)", err[1], err[2], err[3]);
+}
+
+tpo_status tpo_last_device_error(tpo_ctx* c, uint32_t out[4]) {
+  if (!c || !out) return fail(TPO_ERR_INVALID_ARG, "NULL argument");
+  std::memcpy(out, c->last_dev_err, sizeof(c->last_dev_err));
+  return TPO_OK;
+}
+
+const void* tpo_staging_ptr(tpo_ctx* c) { return c ? c->staging : nullptr; }
+
+const uint32_t* tpo_ar_done_counters(tpo_ctx* c, uint32_t* target) {
+  if (!c) return nullptr;
+  if (target) *target = c->ar_target;
+  return c->words->ar_done;
+}
+
+tpo_status tpo_read_trace(tpo_ctx* c, uint64_t* out, int cap) {
+  if (!c || !out || cap < 1) return fail(TPO_ERR_INVALID_ARG, "bad arguments");
+  if (c->has_last) {
+    cudaError_t e = cudaEventSynchronize(c->last);
+    if (e != cudaSuccess) return cuda_fail(e, "synchronise");
+  }
+  const int nw = cap < TPO_TRACE_WORDS ? cap : TPO_TRACE_WORDS;
+  cudaError_t e = cudaMemcpyAsync(out, c->words->trace, sizeof(uint64_t) * nw, cudaMemcpyDeviceToHost, c->aux);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c->aux);
+  return e == cudaSuccess ? TPO_OK : cuda_fail(e, "read trace");
+}
+
+}  // extern "C"
