@@ -480,8 +480,7 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
     int ok = (lane == 0) ? (mbar_wait(p, bar, par, SITE_TMEM_FULL, true) ? 1 : 0) : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
-    while (!mbar_test(bar, par)) {
-    }  // already complete: gives every lane the barrier's ordering
+    mbar_wait(p, bar, par, SITE_TMEM_FULL, false);  // already complete: gives every lane its ordering
     tc_fence_after();
     const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
 #pragma unroll 1

@@ -1,0 +1,230 @@
+"""AG+GEMM on the GPU through the C ABI, against the CPU oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tensor_comm_gemm_gb300 import synth
+from tensor_comm_gemm_gb300 import tpoverlap as t
+from gpu_util import AgRun, assert_close, gather_tiles, host_bits, host_f64, staging_view, SAMPLE_TILES
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_ok):
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def ref_ag(wl):
+    return oracle.ag(oracle.gather(wl.x), wl.w[0], wl.scale_inv_x, wl.scale_inv_w)
+
+
+# (tp, n, k, m): several tiles per slot, ragged K (not a multiple of 256), tp=1 and tp=16
+SHAPES = [(2, 256, 256, 256), (3, 768, 192, 768), (1, 128, 64, 256), (5, 1280, 320, 512), (16, 2048, 64, 256),
+          (4, 1024, 1088, 1024)]
+
+
+@pytest.mark.parametrize("tp,n,k,m", SHAPES)
+def test_ag_full_parity_every_observer(tp, n, k, m):
+    wl = synth.make_ag(tp, n, k, m, seed=10 + tp, dist="uniform")
+    ref = ref_ag(wl)
+    run = AgRun(wl)
+    try:
+        first = None
+        for self_rank in sorted({0, tp - 1, tp // 2}):
+            t.tpo_set_opt(run.ctx, "self_rank", self_rank)
+            run.y.fill_(float("nan"))
+            run.run()
+            assert_close(host_f64(run.y), ref)
+            bits = host_bits(run.y)
+            if first is None:
+                first = bits
+            assert np.array_equal(bits, first), "result depends on the observer rank"
+    finally:
+        run.close()
+
+
+def test_workload_ag_tp2_full_parity():
+    wl = synth.workload(0)
+    run = AgRun(wl)
+    try:
+        run.run()
+        assert_close(host_f64(run.y), ref_ag(wl))
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("tp,n,k,m", [(2, 256, 256, 256), (4, 1024, 192, 512)])
+def test_staging_bit_exact_after_every_ring_step(tp, n, k, m):
+    wl = synth.make_ag(tp, n, k, m, seed=3, dist="uniform")
+    run = AgRun(wl)
+    nbytes = n * k * 2
+    try:
+        view = staging_view(run.ctx, nbytes)
+        t.tpo_set_opt(run.ctx, "mode", 3)          # producer only
+        for self_rank in range(tp):
+            t.tpo_set_opt(run.ctx, "self_rank", self_rank)
+            for step in range(tp):
+                view.fill_(0xAB)
+                torch.cuda.synchronize()
+                t.tpo_set_opt(run.ctx, "debug_last_step", step)
+                run.run()
+                got = view.cpu().numpy().view(np.uint16).reshape(n, k)
+                want = oracle.staging_after_step(wl.x, self_rank, step, 0xAB)
+                assert np.array_equal(got, want), (self_rank, step)
+        # a full overlapped call leaves exactly the rank-order gather
+        t.tpo_set_opt(run.ctx, "mode", 0)
+        t.tpo_set_opt(run.ctx, "debug_last_step", -1)
+        view.fill_(0xAB)
+        run.run()
+        got = view.cpu().numpy().view(np.uint16).reshape(n, k)
+        assert np.array_equal(got, oracle.gather(wl.x))
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("tp,n,k,m", [(2, 256, 256, 256), (4, 2048, 512, 768)])
+def test_overlapped_bit_identical_to_sequential(tp, n, k, m):
+    wl = synth.make_ag(tp, n, k, m, seed=4, dist="normal", sigma=k ** -0.25)
+    run = AgRun(wl)
+    try:
+        outs = {}
+        for mode, psms in [(0, 8), (1, 8), (2, 8), (0, 1), (0, 20)]:
+            t.tpo_set_opt(run.ctx, "mode", mode)
+            t.tpo_set_opt(run.ctx, "producer_sms", psms)
+            run.y.fill_(float("nan"))
+            run.run()
+            outs[(mode, psms)] = host_bits(run.y)
+        base = outs[(1, 8)]
+        for key, v in outs.items():
+            assert np.array_equal(v, base), key
+        assert_close(synth.bf16_bits_to_f32(base).astype(np.float64), ref_ag(wl))
+    finally:
+        run.close()
+
+
+def test_producer_delay_keeps_result_identical():
+    """A slow producer (spin before every publish) widens the window in which a
+    GEMM load could run ahead of its chunk; the result must not change."""
+    wl = synth.make_ag(4, 1024, 256, 512, seed=5, dist="uniform")
+    run = AgRun(wl)
+    try:
+        t.tpo_set_opt(run.ctx, "mode", 1)
+        run.run()
+        base = host_bits(run.y)
+        staging = staging_view(run.ctx, wl.n * wl.k * 2)
+        t.tpo_set_opt(run.ctx, "mode", 0)
+        t.tpo_set_opt(run.ctx, "debug_delay_ns", 200000)
+        for _ in range(3):
+            staging.fill_(0xFF)          # NaN pattern: a premature read shows up in Y
+            run.y.fill_(0)
+            run.run()
+            assert np.array_equal(host_bits(run.y), base)
+    finally:
+        run.close()
+
+
+def test_identity_and_one_hot_weights_are_exact():
+    tp, n, k = 2, 512, 256
+    wl = synth.make_ag(tp, n, k, k, seed=6, dist="normal")
+    g = oracle.gather(wl.x)
+    rng = np.random.default_rng(0)
+    perm = rng.permutation(k)
+    onehot = np.zeros((2 * k, k), dtype=np.float32)       # m = 2k columns, two one-hots each
+    onehot[np.arange(k), perm] = 1.0
+    onehot[k + np.arange(k), np.arange(k)] = 1.0
+    for w, want in [(np.eye(k, dtype=np.float32), g), (onehot, np.concatenate([g[:, perm], g], 1))]:
+        wl2 = synth.Workload("onehot", "ag", "bf16", tp, n, k, w.shape[0], wl.x, [synth.f32_to_bf16_bits(w)])
+        run = AgRun(wl2)
+        try:
+            run.run()
+            assert np.array_equal(host_bits(run.y), want)
+        finally:
+            run.close()
+
+
+def test_trace_orders_publish_before_acquire():
+    wl = synth.make_ag(4, 4096, 1024, 1024, seed=8, dist="uniform")
+    run = AgRun(wl)
+    try:
+        t.tpo_set_opt(run.ctx, "trace", 1)
+        t.tpo_set_opt(run.ctx, "self_rank", 1)
+        run.run()
+        tr = t.tpo_read_trace(run.ctx)
+        order = oracle.ring_order(4, 1)
+        pubs = [tr[t.TPO_TRACE_PUBLISH + s] for s in order]
+        assert all(p > 0 for p in pubs)
+        assert pubs[1] <= pubs[2] <= pubs[3]            # ring steps published in arrival order
+        for s in order[1:]:                              # a gated slot is read only after its publish
+            acq = tr[t.TPO_TRACE_ACQUIRE + s]
+            if acq != 2 ** 64 - 1:
+                assert acq >= tr[t.TPO_TRACE_PUBLISH + s] - 2000  # timer samples of different SMs
+        assert tr[t.TPO_TRACE_START] <= tr[t.TPO_TRACE_END]
+    finally:
+        run.close()
+
+
+def test_skipped_chunk_times_out_and_context_recovers():
+    wl = synth.make_ag(4, 1024, 256, 512, seed=9, dist="uniform")
+    run = AgRun(wl)
+    try:
+        t.tpo_set_opt(run.ctx, "wait_timeout_ms", 50)
+        t.tpo_set_opt(run.ctx, "debug_skip_chunk", 2)     # never published: the GEMM must give up
+        t.tpo_ag_gemm(run.ctx, run.xs, run.w, run.y)
+        assert t.tpo_sync_status(run.ctx) == 4
+        code, site, _, extra = t.tpo_last_device_error(run.ctx)
+        assert code == 1 and site in (1, 2, 3, 4, 5)
+        t.tpo_set_opt(run.ctx, "debug_skip_chunk", -1)
+        t.tpo_set_opt(run.ctx, "wait_timeout_ms", 2000)
+        run.run()
+        assert_close(host_f64(run.y), ref_ag(wl))
+    finally:
+        run.close()
+
+
+def test_call_argument_errors():
+    wl = synth.make_ag(2, 256, 256, 256, seed=1, dist="uniform")
+    run = AgRun(wl)
+    try:
+        base = run.y.view(torch.uint8).reshape(-1)
+        with pytest.raises(t.TpoError) as e:
+            t.tpo_ag_gemm(run.ctx, run.xs, run.w, base[8:].data_ptr())
+        assert e.value.status == 1
+        with pytest.raises(t.TpoError) as e:
+            t.tpo_ag_gemm(run.ctx, [run.xs[0], 0], run.w, run.y)
+        assert e.value.status == 1
+        sx = torch.ones(1, device="cuda")
+        with pytest.raises(t.TpoError) as e:
+            t.tpo_ag_gemm(run.ctx, run.xs, run.w, run.y, sx, sx)
+        assert e.value.status == 1
+        with pytest.raises(t.TpoError):
+            t.tpo_set_opt(run.ctx, "self_rank", 2)
+        with pytest.raises(t.TpoError):
+            t.tpo_set_opt(run.ctx, "no_such_option", 1)
+        with pytest.raises(t.TpoError) as e:
+            t.tpo_gemm_ar(run.ctx, run.xs, [run.w, run.w], run.y, 3)   # n % (3*tp*128) != 0
+        assert e.value.status == 2
+    finally:
+        run.close()
+
+
+@pytest.mark.slow
+def test_workload_ag_tp4_4096_sampled_parity():
+    wl = synth.workload(1)
+    run = AgRun(wl)
+    try:
+        run.run()
+        y = host_f64(run.y)
+        bits = host_bits(run.y)
+        tiles = synth.sample_tiles(wl.n, wl.m, 16, SAMPLE_TILES, seed=1000 + wl.seed)
+        ref = oracle.ag(oracle.gather(wl.x), wl.w[0], tiles=tiles)
+        assert_close(gather_tiles(y, tiles), ref)
+        t.tpo_set_opt(run.ctx, "mode", 1)
+        run.y.fill_(0)
+        run.run()
+        assert np.array_equal(host_bits(run.y), bits)
+    finally:
+        run.close()

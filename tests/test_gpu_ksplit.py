@@ -1,0 +1,134 @@
+"""GEMM+RS and row-parallel GEMM+AR on the GPU through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tensor_comm_gemm_gb300 import synth
+from tensor_comm_gemm_gb300 import tpoverlap as t
+from gpu_util import KsplitRun, assert_close, gather_tiles, host_bits, host_f64, SAMPLE_TILES
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_ok):
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+# (tp, n, k, m): ragged per-rank K (k/tp not a multiple of 128), tp = 1, asymmetric shapes
+RS_SHAPES = [(2, 256, 256, 256), (3, 768, 192, 512), (1, 256, 64, 256), (4, 1024, 1280, 768), (8, 2048, 512, 256)]
+
+
+@pytest.mark.parametrize("tp,n,k,m", RS_SHAPES)
+def test_rs_full_parity(tp, n, k, m):
+    wl = synth.make_ksplit("rs", tp, n, k, m, seed=20 + tp, dist="uniform")
+    ref = oracle.rs_blocks(oracle.ksplit(wl.x, wl.w), tp)
+    run = KsplitRun(wl)
+    try:
+        for yb in run.yb:
+            yb.fill_(float("nan"))
+        run.rs()
+        for b in range(tp):
+            assert_close(host_f64(run.yb[b]), ref[b])
+        first = [host_bits(y) for y in run.yb]
+        run.rs()
+        assert all(np.array_equal(host_bits(y), f) for y, f in zip(run.yb, first))
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("tp,n,k,m,chunks", [(2, 1024, 256, 256, 4), (3, 2304, 384, 512, 2), (1, 512, 128, 512, 4),
+                                             (2, 512, 1024, 256, 1)])
+def test_ar_full_parity_and_done_counters(tp, n, k, m, chunks):
+    wl = synth.make_ksplit("ar", tp, n, k, m, seed=30 + tp, dist="uniform", n_row_chunks=chunks)
+    ref = oracle.ksplit(wl.x, wl.w)
+    run = KsplitRun(wl)
+    try:
+        for rep in range(2):
+            run.y.fill_(float("nan"))
+            t.tpo_set_opt(run.ctx, "trace", 1)
+            run.ar(chunks)
+            assert_close(host_f64(run.y), ref)
+            ptr, target = t.tpo_ar_done_counters(run.ctx)
+            tiles_per_chunk = (n // chunks // 128) * (m // 256)
+            assert target == (rep + 1) * tiles_per_chunk * 4
+            torch.cuda.synchronize()
+            cnt = np.frombuffer(_read_device_words(ptr, chunks), dtype=np.uint32)
+            assert np.all(cnt == target)
+            tr = t.tpo_read_trace(run.ctx)
+            done = [tr[t.TPO_TRACE_CHUNK_DONE + c] for c in range(chunks)]
+            assert all(d > 0 for d in done)
+    finally:
+        run.close()
+
+
+def _read_device_words(ptr, count):
+    class _Arr:
+        __cuda_array_interface__ = {"shape": (count,), "typestr": "<u4", "data": (ptr, True), "version": 3}
+    return torch.as_tensor(_Arr(), device="cuda").cpu().numpy().tobytes()
+
+
+def test_ar_single_chunk_equals_rs_blocks_bitwise():
+    """With one row chunk the all-reduce rows of part b sum the ranks in the same
+    ring order as reduce-scatter block b, so the results agree bit for bit."""
+    tp, n, k, m = 4, 1024, 512, 512
+    wl = synth.make_ksplit("rs", tp, n, k, m, seed=41, dist="normal", sigma=k ** -0.25)
+    run = KsplitRun(wl)
+    try:
+        run.rs()
+        run.ar(1)
+        assert np.array_equal(host_bits(run.y), np.concatenate([host_bits(y) for y in run.yb], 0))
+    finally:
+        run.close()
+
+
+def test_ksplit_rejects_fp8_and_bad_shapes():
+    wl = synth.make_ksplit("rs", 2, 256, 256, 256, seed=1, dist="uniform")
+    run = KsplitRun(wl)
+    try:
+        with pytest.raises(t.TpoError) as e:
+            t.tpo_gemm_ar(run.ctx, run.xs, run.ws, run.y, 0)
+        assert e.value.status == 1
+        with pytest.raises(t.TpoError) as e:
+            t.tpo_gemm_rs(run.ctx, run.xs, run.ws, [run.yb[0], 0])
+        assert e.value.status == 1
+    finally:
+        run.close()
+    ctx = t.tpo_ctx_create(2, 256, 256, 256, t.TPO_FP8_E4M3)
+    try:
+        x = torch.zeros((256, 128), dtype=torch.uint8, device="cuda")
+        with pytest.raises(t.TpoError) as e:
+            t.tpo_gemm_rs(ctx, [x, x], [x, x], [x, x])
+        assert e.value.status == 2
+    finally:
+        t.tpo_ctx_destroy(ctx)
+
+
+@pytest.mark.slow
+def test_workload_ar_tp2_8192_sampled_parity():
+    wl = synth.workload(2)
+    run = KsplitRun(wl)
+    try:
+        run.ar(wl.n_row_chunks)
+        tiles = synth.sample_tiles(wl.n, wl.m, 16, SAMPLE_TILES, seed=1000 + wl.seed)
+        ref = oracle.ksplit(wl.x, wl.w, tiles=tiles)
+        assert_close(gather_tiles(host_f64(run.y), tiles), ref)
+    finally:
+        run.close()
+
+
+@pytest.mark.slow
+def test_workload_rs_tp8_sampled_parity():
+    wl = synth.workload(3)
+    run = KsplitRun(wl)
+    try:
+        run.rs()
+        full = torch.cat(run.yb, 0)
+        tiles = synth.sample_tiles(wl.n, wl.m, 16, SAMPLE_TILES, seed=1000 + wl.seed)
+        ref = oracle.ksplit(wl.x, wl.w, tiles=tiles)
+        assert_close(gather_tiles(host_f64(full), tiles), ref)
+    finally:
+        run.close()
