@@ -1,0 +1,470 @@
+"""Benchmark of libtpoverlap on GB300.
+
+One step = one overlapped AG+GEMM call of the 4096^3 workload (tp = 4 simulated
+ranks, X_r [1024, 4096], W [4096, 4096], bf16 in, Y [4096, 4096] bf16 out):
+ring-order chunk producer, per-chunk release counters, counter-gated tcgen05
+GEMM, rank-order epilogue, in one launch.  The line also reports the same
+call in sequential mode (copy, then GEMM), the GEMM alone, the producer alone,
+and the other workloads (row-parallel GEMM+AR, GEMM+RS, FP8 AG+GEMM) measured
+the same way.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tpo|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs an independent
+replica on its own GPU: the simulated ranks live in one GPU's memory, so the
+path has no exchange between GPUs ("replicas only"); value = work of all
+ranks / slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from tensor_comm_gemm_gb300 import synth  # noqa: E402
+
+METRIC = "overlapped AG+GEMM / GEMM+RS TFLOP/s on 1 GB300; % of dense tensor peak"
+HEADLINE = 1  # the 4096^3 AG+GEMM workload
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+L2_FLUSH_BYTES = 256 << 20
+
+
+def describe(idx):
+    op, dt, tp, n, k, m, ch = synth.WORKLOAD_SHAPES[idx]
+    if op == "ag":
+        return "AG+GEMM %s tp=%d: X_r [%d,%d], W [%d,%d] -> Y [%d,%d] bf16" % (dt, tp, n // tp, k, m, k, n, m)
+    if op == "rs":
+        return "GEMM+RS bf16 tp=%d: X_r [%d,%d], W_r [%d,%d] -> %d blocks [%d,%d]" % (
+            tp, n, k // tp, m, k // tp, tp, n // tp, m)
+    return "row-parallel GEMM+AR bf16 tp=%d, %d row chunks: X_r [%d,%d], W_r [%d,%d] -> Y [%d,%d]" % (
+        tp, ch, n, k // tp, m, k // tp, n, m)
+
+
+def kernel_sha() -> str:
+    """Hash of the kernel sources; DRAM traffic figures taken with ncu are only
+    reported while they still describe the kernel as built."""
+    h = hashlib.sha256()
+    for f in ("kernels.cu", "tpo_params.h"):
+        with open(os.path.join(ROOT, "tensor_comm_gemm_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "tpo_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t_begin=None, t_end=None):
+        """Median SM clock and the throttle reasons seen by samples taken between
+        t_begin and t_end (host wall-clock seconds)."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        import datetime
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    clk, cmax = float(parts[1]), float(parts[2])
+                except ValueError:
+                    continue
+                if t_begin is not None and not (t_begin - 0.05 <= ts <= t_end + 0.05):
+                    continue
+                sm.append(clk)
+                smax.append(cmax)
+                try:
+                    power.append(float(parts[3]))
+                except ValueError:
+                    pass
+                for nm, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def gpu_arm(args, rank, world, local_rank, dist):
+    import torch
+    from tensor_comm_gemm_gb300 import build as tb
+    from tensor_comm_gemm_gb300 import tpoverlap as t
+
+    tb.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks, peak_kind = load_peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def time_steps(fn, steps, warmup, flush_l2=True):
+        """Per-step CUDA-event durations (ms) on the launching stream, with the L2
+        flushed (a 256 MiB write) before every step, outside the events."""
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(steps):
+            if flush_l2:
+                flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def mean(v):
+        return sum(v) / len(v)
+
+    def check(ctx):
+        st = t.tpo_sync_status(ctx)
+        if st != 0:
+            raise RuntimeError("device failure: " + t.tpo_last_error())
+
+    # ---- headline workload: AG+GEMM tp=4, 4096^3
+    wl = synth.workload(HEADLINE)
+    flops = synth.flops(HEADLINE)
+    xs = [to_dev(x) for x in wl.x]
+    w = to_dev(wl.w[0])
+    y = torch.empty((wl.n, wl.m), dtype=torch.bfloat16, device=dev)
+    ctx = t.tpo_ctx_create(wl.tp, wl.n, wl.k, wl.m, t.TPO_BF16)
+    if args.producer_sms:
+        t.tpo_set_opt(ctx, "producer_sms", args.producer_sms)
+    call = lambda: t.tpo_ag_gemm(ctx, xs, w, y, stream=stream)  # noqa: E731
+
+    def mode_times(mode, steps, warmup):
+        t.tpo_set_opt(ctx, "mode", mode)
+        v = time_steps(call, steps, warmup)
+        check(ctx)
+        return v
+
+    detail_steps = min(200, max(5, args.steps // 2))
+    seq = mode_times(1, detail_steps, 3)
+    gemm_only = mode_times(2, detail_steps, 3)
+    prod_only = mode_times(3, detail_steps, 3)
+    t.tpo_set_opt(ctx, "mode", 0)
+
+    # ---- the timed region: K overlapped steps, barrier + synchronize on both sides
+    for _ in range(args.warmup):
+        call()
+    check(ctx)
+    clocks = Clocks(local_rank)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)                    # let the sampler come up before the region starts
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("tpo_timed")
+    wall0 = time.time()
+    t0 = time.perf_counter()
+    evs = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    wall1 = time.time()
+    torch.cuda.nvtx.range_pop()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop(wall0, wall1)
+    check(ctx)
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = mean(step_ms)
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers: H2D inputs, call, D2H Y
+    hx = [torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory() for x in wl.x]
+    hw = torch.from_numpy(np.ascontiguousarray(wl.w[0]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    hy = torch.empty((wl.n, wl.m), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        for d, h in zip(xs, hx):
+            d.copy_(h, non_blocking=True)
+        w.copy_(hw, non_blocking=True)
+        call()
+        hy.copy_(y, non_blocking=True)
+
+    e2e_ms = mean(time_steps(e2e_step, detail_steps, 3))
+    check(ctx)
+    h2d = sum(x.nbytes for x in wl.x) + wl.w[0].nbytes
+    d2h = wl.n * wl.m * 2
+
+    # ---- roofline of the dominant kernel (the fused launch) from the events above
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = flops / (mean(step_ms) * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tj = json.load(f)
+        if tj.get("kernel_sha") == kernel_sha():
+            traffic = tj.get("ag_tp4_4096", {}).get("bytes_per_launch")
+    gemm_ms, seq_ms, prod_ms = mean(gemm_only), mean(seq), mean(prod_only)
+    producer_bytes = 2 * (wl.n * wl.k * 2)  # every chunk read once and written once
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded splitmix64 normal inputs, sigma = K^-1/4)",
+        "config": {"workload": "ag_tp4_4096: " + describe(HEADLINE), "mode": "overlapped (one launch)",
+                   "producer_sms": t.tpo_get_opt(ctx, "producer_sms"),
+                   "l2": "flushed before every step by a 256 MiB write outside the events",
+                   "parallelism": "replicas only (simulated ranks in one GPU's memory)"},
+        "gpu_launches": args.steps,
+        "wall_s_timed_region": round(wall, 4),
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_kind if peak_kind == "measured"
+                     else "fallback 1.9 PFLOP/s"},
+        "clocks": clk,
+        "detail": {
+            "sequential_ms": round(seq_ms, 5),
+            "sequential_tflops": round(flops / (seq_ms * 1e-3) / 1e12, 2),
+            "gemm_only_ms": round(gemm_ms, 5),
+            "gemm_only_tflops": round(flops / (gemm_ms * 1e-3) / 1e12, 2),
+            "producer_only_ms": round(prod_ms, 5),
+            "producer_only_gbs": round(producer_bytes / (prod_ms * 1e-3) / 1e9, 1),
+            "producer_frac_of_hbm": round(producer_bytes / (prod_ms * 1e-3) / 1e9 / hbm, 4),
+            "exposed_producer_frac": round((mean(step_ms) - gemm_ms) / gemm_ms, 4),
+        },
+    }
+    t.tpo_ctx_destroy(ctx)
+    del xs, w, y, hx, hw, hy
+
+    # ---- the other workloads, one line each inside "also"
+    if not args.headline_only:
+        result["also"] = other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch)
+
+    # ---- the oracle on the host cores, bounded sample
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    return result
+
+
+def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
+    out = {}
+    steps = min(40, max(5, args.steps // 2))
+    for idx in (2, 3, 4):
+        op, dt, tp, n, k, m, ch = synth.WORKLOAD_SHAPES[idx]
+        wl = synth.workload(idx)
+        flops = synth.flops(idx)
+        name = wl.name
+        if op == "ag":
+            xs = [to_dev(x) for x in wl.x]
+            w = to_dev(wl.w[0])
+            y = torch.empty((n, m), dtype=torch.bfloat16, device=dev)
+            sx = torch.tensor([wl.scale_inv_x], dtype=torch.float32, device=dev)
+            sw = torch.tensor([wl.scale_inv_w], dtype=torch.float32, device=dev)
+            ctx = t.tpo_ctx_create(tp, n, k, m, t.TPO_FP8_E4M3)
+            fn = lambda: t.tpo_ag_gemm(ctx, xs, w, y, sx, sw)  # noqa: E731
+            pk = peak * FP8_OVER_BF16
+        else:
+            xs = [to_dev(x) for x in wl.x]
+            ws = [to_dev(x) for x in wl.w]
+            ctx = t.tpo_ctx_create(tp, n, k, m, t.TPO_BF16)
+            if op == "rs":
+                yb = [torch.empty((n // tp, m), dtype=torch.bfloat16, device=dev) for _ in range(tp)]
+                fn = lambda: t.tpo_gemm_rs(ctx, xs, ws, yb)  # noqa: E731
+            else:
+                y = torch.empty((n, m), dtype=torch.bfloat16, device=dev)
+                fn = lambda: t.tpo_gemm_ar(ctx, xs, ws, y, ch)  # noqa: E731
+            pk = peak
+        ms = mean(time_steps(fn, steps, 3))
+        check(ctx)
+        rec = {"workload": describe(idx), "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+               "frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / pk, 4), "peak_tflops": pk}
+        if op == "ag":
+            t.tpo_set_opt(ctx, "mode", 1)
+            sms = mean(time_steps(fn, steps, 2))
+            t.tpo_set_opt(ctx, "mode", 2)
+            gms = mean(time_steps(fn, steps, 2))
+            check(ctx)
+            rec.update({"sequential_ms": round(sms, 4), "gemm_only_ms": round(gms, 4),
+                        "exposed_producer_frac": round((ms - gms) / gms, 4)})
+        out[name] = rec
+        t.tpo_ctx_destroy(ctx)
+        del fn
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+def cpu_baseline(wl, seconds):
+    """The oracle as it stands, on the host cores, over a bounded sample of the
+    workload's output tiles (16 x 16 each); throughput scaled to TFLOP/s."""
+    import oracle
+
+    g = oracle.gather(wl.x)
+    tile = 16
+    per_tile = 2.0 * tile * tile * wl.k
+    probe = synth.sample_tiles(wl.n, wl.m, tile, 32, seed=7)
+    t0 = time.perf_counter()
+    oracle.ag(g, wl.w[0], tiles=probe)
+    rate = len(probe) / max(time.perf_counter() - t0, 1e-6)
+    count = int(max(32, min(65536, rate * seconds)))
+    tiles = synth.sample_tiles(wl.n, wl.m, tile, count, seed=1000 + wl.seed)
+    t0 = time.perf_counter()
+    oracle.ag(g, wl.w[0], tiles=tiles)
+    dt = time.perf_counter() - t0
+    return {"value": per_tile * len(tiles) / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": "%d of %d output tiles of 16x16 (FP64 loops over k=%d), %.1f s" % (
+                len(tiles), (wl.n // tile) * (wl.m // tile), wl.k, dt)}
+
+
+def reference_arm(args):
+    """The oracle timed as the reference arm: every step is a bounded sample of
+    the headline workload's output tiles."""
+    import oracle
+
+    wl = synth.workload(HEADLINE)
+    g = oracle.gather(wl.x)
+    tile = 16
+    per_tile = 2.0 * tile * tile * wl.k
+    total_budget = 120.0
+    per_step = max(0.5, total_budget / max(1, args.steps + args.warmup))
+    probe = synth.sample_tiles(wl.n, wl.m, tile, 16, seed=7)
+    t0 = time.perf_counter()
+    oracle.ag(g, wl.w[0], tiles=probe)
+    rate = len(probe) / max(time.perf_counter() - t0, 1e-6)
+    count = int(max(16, min(65536, rate * per_step)))
+    times = []
+    for i in range(args.warmup + args.steps):
+        tiles = synth.sample_tiles(wl.n, wl.m, tile, count, seed=2000 + i)
+        t0 = time.perf_counter()
+        oracle.ag(g, wl.w[0], tiles=tiles)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = per_tile * count / (ms * 1e-3) / 1e12
+    sample = "%d of %d output tiles of 16x16 per step (FP64 loops over k=%d)" % (
+        count, (wl.n // tile) * (wl.m // tile), wl.k)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "ag_tp4_4096: " + describe(HEADLINE), "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="tpo", choices=["tpo", "reference"])
+    ap.add_argument("--producer-sms", type=int, default=0)
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = gpu_arm(args, rank, world, local_rank, dist)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -160,7 +160,8 @@ tpo_status tpo_gemm_ar(tpo_ctx* ctx, const void* const* x, const void* const* w,
  *   "trace"            1 = record device timestamps (tpo_read_trace)
  *   "debug_skip_chunk" slot whose counter the producer never publishes (-1 off)
  *   "debug_delay_ns"   producer spin before each publish
- *   "debug_last_step"  producer stops after this ring step (-1 = all steps)
+ *   "debug_last_step"  mode 3 only: the producer stops after this ring step
+ *                      (-1 = all steps)
  * Environment variables TPO_<KEY in upper case> override the defaults at
  * create time.  Unknown keys or out-of-range values: TPO_ERR_INVALID_ARG.
  */

@@ -66,11 +66,6 @@ bool encode2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-struct OptDesc {
-  const char* key;
-  int64_t lo, hi;
-};
-
 }  // namespace
 
 struct tpo_ctx {
@@ -87,7 +82,7 @@ struct tpo_ctx {
   uint8_t* staging = nullptr;
   size_t staging_bytes = 0;
   tpo::DevWords* words = nullptr;
-  uint32_t target = 0;     // counter value meaning "published by the latest call"
+  uint32_t target[TPO_MAX_TP] = {};  // per slot: counter value once the latest call published it
   uint32_t ar_target = 0;  // AR done-counter value after the latest call
   int ar_chunks = 0;       // row-chunk count of the latest AR call
   cudaStream_t aux = nullptr;
@@ -194,6 +189,18 @@ void cache_store(tpo_ctx* c, int op, const void* const* key, int nkey, const Par
   std::memcpy(c->cache[op].mapB, p.mapB, sizeof(p.mapB));
   std::memcpy(c->cache[op].mapY, p.mapY, sizeof(p.mapY));
   c->cache_valid[op] = true;
+}
+
+// Advance the expected counter value of every slot this call's producer is
+// meant to publish (all slots, or those of ring steps 0..debug_last_step) by
+// the number of producer CTAs, and copy the targets into the launch.
+void advance_targets(tpo_ctx* c, Params& p, int producers) {
+  for (int step = 0; step < c->tp; ++step) {
+    if (c->debug_last_step >= 0 && step > c->debug_last_step) continue;
+    const int slot = static_cast<int>(((c->self_rank - step) % c->tp + c->tp) % c->tp);
+    c->target[slot] += static_cast<uint32_t>(producers);
+  }
+  std::memcpy(p.target, c->target, sizeof(p.target));
 }
 
 int clamp_grid(int64_t want, int total_tiles) {
@@ -367,6 +374,8 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   if (!fp8 && (d_scale_inv_x || d_scale_inv_w))
     return fail(TPO_ERR_INVALID_ARG, "bf16 contexts take no scale_inv pointers (pass NULL)");
   if (c->self_rank >= c->tp) return fail(TPO_ERR_INVALID_ARG, "self_rank >= tp");
+  if (c->debug_last_step >= 0 && c->mode != 3)
+    return fail(TPO_ERR_INVALID_ARG, "debug_last_step applies to mode 3 (producer only)");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int elem = fp8 ? 1 : 2;
   const int kel = tpo::BK_BYTES / elem;
@@ -410,16 +419,14 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       if (P < 1 || c->num_sms - P < 1 || P + G > c->max_coop_grid)
         return fail(TPO_ERR_INVALID_ARG, "producer_sms=%d + gemm CTAs=%d exceed the %d co-resident CTAs", P, G,
                     c->max_coop_grid);
-      c->target += static_cast<uint32_t>(P);
-      p.target = c->target;
+      advance_targets(c, p, P);
       p.num_producers = P;
       p.num_gemm = G;
       return launch(c, p, P + G, true, s);
     }
     case 1: {  // sequential: the copy to completion, then the same GEMM
       const int Pc = static_cast<int>(c->seq_copy_ctas ? c->seq_copy_ctas : c->num_sms);
-      c->target += static_cast<uint32_t>(Pc);
-      p.target = c->target;
+      advance_targets(c, p, Pc);
       p.num_producers = Pc;
       p.num_gemm = 0;
       st = launch(c, p, Pc, false, s);
@@ -429,7 +436,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       return launch(c, p, p.num_gemm, false, s);
     }
     case 2: {  // GEMM only: chunks published by an earlier call
-      p.target = c->target;
+      std::memcpy(p.target, c->target, sizeof(p.target));
       p.num_producers = 0;
       p.num_gemm = clamp_grid(c->gemm_ctas ? c->gemm_ctas : c->num_sms, tiles);
       return launch(c, p, p.num_gemm, false, s);
@@ -437,8 +444,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
     default: {  // producer only
       const int P = static_cast<int>(c->producer_sms);
       if (P > c->max_coop_grid) return fail(TPO_ERR_INVALID_ARG, "producer_sms too large");
-      c->target += static_cast<uint32_t>(P);
-      p.target = c->target;
+      advance_targets(c, p, P);
       p.num_producers = P;
       p.num_gemm = 0;
       return launch(c, p, P, false, s);
@@ -542,7 +548,7 @@ tpo_status tpo_sync_status(tpo_ctx* c) {
   e = cudaMemsetAsync(c->words, 0, offsetof(tpo::DevWords, pad), c->aux);
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->aux);
   if (e != cudaSuccess) return cuda_fail(e, "reset after device failure");
-  c->target = 0;
+  std::memset(c->target, 0, sizeof(c->target));
   c->ar_target = 0;
   c->ar_chunks = 0;
   return fail(TPO_ERR_TIMEOUT, "device wait timed out (site %u, block %u, extra %u)", err[1], err[2], err[3]);

@@ -362,7 +362,7 @@ __device__ bool wait_counter(const Params& p, int slot) {
   const uint32_t* c = &p.words->counters[slot];
   const unsigned long long t0 = gtime();
   bool waited = false;
-  while (static_cast<int>(ld_acquire(c) - p.target) < 0) {
+  while (static_cast<int>(ld_acquire(c) - p.target[slot]) < 0) {
     waited = true;
     if (aborted(p)) return false;
     if (gtime() - t0 > p.timeout_ns) {

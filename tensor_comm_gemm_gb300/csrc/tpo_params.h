@@ -76,8 +76,9 @@ struct Params {
   long long chunk_bytes;
   unsigned long long timeout_ns;
   unsigned long long delay_ns;
-  uint32_t target;        // counter value of a chunk published by this call
+  uint32_t target[TPO_MAX_TP];  // per slot: counter value once this call has published it
   uint32_t ar_target;     // AR done-counter value once this call stored the chunk
+  uint32_t pad1;
   int op;
   int fp8;
   int tp;

@@ -67,7 +67,7 @@ def test_ar_full_parity_and_done_counters(tp, n, k, m, chunks):
 
 def _read_device_words(ptr, count):
     class _Arr:
-        __cuda_array_interface__ = {"shape": (count,), "typestr": "<u4", "data": (ptr, True), "version": 3}
+        __cuda_array_interface__ = {"shape": (count,), "typestr": "<u4", "data": (ptr, False), "version": 3}
     return torch.as_tensor(_Arr(), device="cuda").cpu().numpy().tobytes()
 
 
