@@ -203,6 +203,37 @@ tpo_status tpo_read_trace(tpo_ctx* ctx, uint64_t* out, int cap);
 /* Library build string (compiler, target architecture). */
 const char* tpo_version(void);
 
+/*
+ * AG+GEMM that allocates no device memory.  The pages have no counterpart of
+ * this entry point; it exists for callers that cannot call cudaMalloc when they
+ * run the layer: a serving process that reserved all device memory for its own
+ * pool at start-up, a runtime whose allocator forbids raw device allocations
+ * after initialisation so that its memory use stays fixed, or any code that
+ * only owns the buffers it is handed.  tpo_ctx_create allocates, so these
+ * callers cannot hold a context.
+ *
+ * Computes exactly what tpo_ag_gemm computes with a context's default options
+ * (overlapped schedule, observer rank 0, 8 producer CTAs, 2 s wait bound); the
+ * result is bit-identical to it.  Arguments as tpo_ctx_create (tp, n, k, m,
+ * dtype) plus tpo_ag_gemm (x, w, y, scale_inv pointers, stream).
+ *
+ * Scratch (the gathered staging buffer, the chunk counters and the error word)
+ * lives in a static device array of the library: TPO_NOALLOC_MAX_STAGING_BYTES
+ * plus a few hundred bytes, held by every GPU that loads the library until the
+ * process exits.  n*k*element size above that limit is rejected with
+ * TPO_ERR_INVALID_ARG and a message naming the limit.
+ * The first call on a device sets that device up (looks up the array's device
+ * address, configures the kernel); make it before any stream capture.
+ * Every call shares the array and clears its counters and error word on
+ * `stream` first; calls whose GPU work could overlap (other streams, other host
+ * threads) race on the array.  The call blocks until its work on `stream` has
+ * finished, then returns TPO_OK or TPO_ERR_TIMEOUT if a device wait ran out.
+ */
+#define TPO_NOALLOC_MAX_STAGING_BYTES (32ull << 20) /* 32 MiB */
+tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t m, int dtype, const void* const* x,
+                               const void* w, void* y, const float* d_scale_inv_x,
+                               const float* d_scale_inv_w, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

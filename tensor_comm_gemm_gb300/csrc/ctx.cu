@@ -223,6 +223,10 @@ tpo_status check_ksplit(tpo_ctx* c, const void* const* x, const void* const* w) 
 
 }  // namespace
 
+namespace tpo {
+void set_last_error(const char* msg) { g_err = msg; }
+}  // namespace tpo
+
 extern "C" {
 
 const char* tpo_last_error(void) { return g_err.c_str(); }

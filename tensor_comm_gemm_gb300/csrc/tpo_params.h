@@ -102,4 +102,7 @@ cudaError_t configure_kernel();
 cudaError_t max_blocks_per_sm(int* n);
 cudaError_t launch_fused(const Params& p, int grid, bool cooperative, cudaStream_t stream);
 
+// Sets the thread-local message returned by tpo_last_error (ctx.cu).
+void set_last_error(const char* msg);
+
 }  // namespace tpo

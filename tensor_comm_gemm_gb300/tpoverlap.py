@@ -25,7 +25,8 @@ TPO_MAX_TP, TPO_MAX_ROW_CHUNKS = 16, 64
 # Every symbol the public header declares.
 EXPORTS = ["tpo_ctx_create", "tpo_ctx_destroy", "tpo_ag_gemm", "tpo_gemm_rs", "tpo_gemm_ar", "tpo_set_opt",
            "tpo_get_opt", "tpo_sync_status", "tpo_last_device_error", "tpo_last_error", "tpo_staging_ptr",
-           "tpo_ar_done_counters", "tpo_read_trace", "tpo_version"]
+           "tpo_ar_done_counters", "tpo_read_trace", "tpo_version", "tpo_ag_gemm_noalloc"]
+TPO_NOALLOC_MAX_STAGING_BYTES = 32 << 20
 
 
 class TpoError(RuntimeError):
@@ -64,6 +65,8 @@ def lib(path: Optional[str] = None):
     L.tpo_ar_done_counters.restype = p
     L.tpo_read_trace.argtypes = [p, ctypes.POINTER(ctypes.c_uint64), i32]
     L.tpo_version.restype = ctypes.c_char_p
+    L.tpo_ag_gemm_noalloc.argtypes = [i32, i64, i64, i64, i32, p, p, p, p, p, p]
+    L.tpo_ag_gemm_noalloc.restype = ctypes.c_int
     for name in ("tpo_ctx_destroy", "tpo_ag_gemm", "tpo_gemm_rs", "tpo_gemm_ar", "tpo_set_opt", "tpo_get_opt",
                  "tpo_sync_status", "tpo_last_device_error", "tpo_read_trace"):
         getattr(L, name).restype = ctypes.c_int
@@ -165,3 +168,11 @@ def tpo_read_trace(ctx: int):
     out = (ctypes.c_uint64 * TPO_TRACE_WORDS)()
     _check(lib().tpo_read_trace(ctx, out, TPO_TRACE_WORDS))
     return list(out)
+
+
+def tpo_ag_gemm_noalloc(tp: int, n: int, k: int, m: int, dtype: int, x: Sequence, w, y, scale_inv_x=None,
+                        scale_inv_w=None, stream=None) -> None:
+    """AG+GEMM with no device allocation (scratch in the library's static
+    array); blocks until the call's work on the stream has finished."""
+    _check(lib().tpo_ag_gemm_noalloc(tp, n, k, m, dtype, _ptr_array(x), _ptr(w), _ptr(y), _ptr(scale_inv_x),
+                                     _ptr(scale_inv_w), _stream(stream)))
