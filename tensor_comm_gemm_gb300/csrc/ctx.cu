@@ -75,9 +75,11 @@ struct tpo_ctx {
   int device = 0;
   int num_sms = 0;
   int max_coop_grid = 0;
+  int max_pairs = 0;             // co-resident CTA pairs of the 2-SM variant
+  bool coop_clusters = true;     // cooperative launches accept cluster dimensions
   // options
   int64_t producer_sms = 8, gemm_ctas = 0, mode = 0, seq_copy_ctas = 0, self_rank = 0, wait_timeout_ms = 2000,
-          trace = 0, debug_skip_chunk = -1, debug_delay_ns = 0, debug_last_step = -1;
+          trace = 0, debug_skip_chunk = -1, debug_delay_ns = 0, debug_last_step = -1, cta_group = 0;
   // device memory
   uint8_t* staging = nullptr;
   size_t staging_bytes = 0;
@@ -91,7 +93,7 @@ struct tpo_ctx {
   uint32_t last_dev_err[4] = {0, 0, 0, 0};
   // tensor-map cache: the Params of the latest call of each op, keyed by pointers
   Params cache[3];
-  const void* cache_key[3][3 * TPO_MAX_TP + 1];
+  const void* cache_key[3][3 * TPO_MAX_TP + 2];
   bool cache_valid[3] = {false, false, false};
 };
 
@@ -114,6 +116,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
       {"debug_skip_chunk", &tpo_ctx::debug_skip_chunk, -1, TPO_MAX_TP - 1},
       {"debug_delay_ns", &tpo_ctx::debug_delay_ns, 0, 1000000000},
       {"debug_last_step", &tpo_ctx::debug_last_step, -1, TPO_MAX_TP - 1},
+      {"cta_group", &tpo_ctx::cta_group, 0, 2},
   };
   for (const E& e : table)
     if (std::strcmp(e.k, key) == 0) {
@@ -127,8 +130,9 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
   return nullptr;
 }
 
-const char* kOptKeys[] = {"producer_sms",   "gemm_ctas", "mode",  "seq_copy_ctas",    "self_rank",
-                          "wait_timeout_ms", "trace",     "debug_skip_chunk", "debug_delay_ns", "debug_last_step"};
+const char* kOptKeys[] = {"producer_sms",     "gemm_ctas",      "mode",           "seq_copy_ctas",
+                          "self_rank",        "wait_timeout_ms", "trace",          "debug_skip_chunk",
+                          "debug_delay_ns",   "debug_last_step", "cta_group"};
 
 void destroy_all(tpo_ctx* c) {
   if (!c) return;
@@ -165,7 +169,16 @@ tpo_status reset_trace(tpo_ctx* c, cudaStream_t s) {
 }
 
 tpo_status launch(tpo_ctx* c, const Params& p, int grid, bool coop, cudaStream_t s) {
+  if (coop && p.cta_group == 2 && !c->coop_clusters) coop = false;
   cudaError_t e = tpo::launch_fused(p, grid, coop, s);
+  if (e != cudaSuccess && coop && p.cta_group == 2) {
+    // Cooperative launches of clusters are not accepted here: launch without the
+    // attribute.  The grid never exceeds the co-resident pair count, so every
+    // CTA is still placed at once (and every wait stays bounded regardless).
+    cudaGetLastError();
+    c->coop_clusters = false;
+    e = tpo::launch_fused(p, grid, false, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   e = cudaEventRecord(c->last, s);
   if (e != cudaSuccess) return cuda_fail(e, "event record");
@@ -206,6 +219,27 @@ void advance_targets(tpo_ctx* c, Params& p, int producers) {
 int clamp_grid(int64_t want, int total_tiles) {
   if (want > total_tiles) want = total_tiles;
   return static_cast<int>(want < 1 ? 1 : want);
+}
+
+// Single-SM (1) or CTA-pair (2) MMA variant for a call whose tile groups are
+// `rows_per_group` rows and, for AR, whose ring-order parts are `part_rows`.
+// Pairs need every 256-row tile inside one group (and one part).
+int choose_cg(const tpo_ctx* c, int64_t rows_per_group, int64_t part_rows) {
+  const bool fits = c->max_pairs >= 1 && rows_per_group % (2 * tpo::BM) == 0 && part_rows % (2 * tpo::BM) == 0;
+  if (c->cta_group == 1) return 1;
+  if (c->cta_group == 2) return fits ? 2 : -1;
+  return fits ? 2 : 1;
+}
+
+// GEMM CTAs for a launch of `tiles` tiles with `producers` producer CTAs.
+int gemm_grid(const tpo_ctx* c, int cg, int64_t want, int producers, int tiles) {
+  if (cg == 1) return clamp_grid(want, tiles);
+  int64_t pairs = want / 2;
+  const int64_t room = c->max_pairs - producers / 2;
+  if (pairs > room) pairs = room;
+  if (pairs > tiles) pairs = tiles;
+  if (pairs < 1) pairs = 1;
+  return static_cast<int>(2 * pairs);
 }
 
 // Validation shared by RS and AR.
@@ -304,6 +338,10 @@ tpo_ctx* tpo_ctx_create(int tp, int64_t n, int64_t k, int64_t m, int dtype) {
     return nullptr;
   }
   c->max_coop_grid = per_sm * c->num_sms;
+  if (tpo::max_active_pairs(&c->max_pairs) != cudaSuccess) {
+    cudaGetLastError();
+    c->max_pairs = 0;  // pairs cannot be placed: the single-SM variant serves every call
+  }
   const int elem = dtype == TPO_BF16 ? 2 : 1;
   c->staging_bytes = static_cast<size_t>(n) * static_cast<size_t>(k) * elem;
   e = cudaMalloc(&c->staging, c->staging_bytes);
@@ -385,28 +423,32 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   const int kel = tpo::BK_BYTES / elem;
   const int64_t rows = c->n / c->tp;
 
+  const int cg = choose_cg(c, rows, rows);
+  if (cg < 0) return fail(TPO_ERR_UNSUPPORTED, "cta_group=2 needs n/tp a multiple of 256 and placeable CTA pairs");
+
   Params p;
   std::memset(&p, 0, sizeof(p));
   base_params(c, p);
   p.op = tpo::OP_AG;
-  const void* key[4] = {c->staging, x[c->self_rank], w, y};
-  if (!cache_lookup(c, tpo::OP_AG, key, 4, p)) {
+  p.cta_group = cg;
+  const void* key[5] = {c->staging, x[c->self_rank], w, y, reinterpret_cast<const void*>(static_cast<intptr_t>(cg))};
+  if (!cache_lookup(c, tpo::OP_AG, key, 5, p)) {
     const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     bool ok = encode2d(&p.mapA[0], c->staging, dt, elem, c->k, c->n, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
               encode2d(&p.mapA[1], x[c->self_rank], dt, elem, c->k, rows, kel, tpo::BM,
                        CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode2d(&p.mapB[0], w, dt, elem, c->k, c->m, kel, tpo::BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode2d(&p.mapB[0], w, dt, elem, c->k, c->m, kel, tpo::BN / cg, CU_TENSOR_MAP_SWIZZLE_128B) &&
               encode2d(&p.mapY[0], y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->m, c->n, tpo::EPI_COLS, 32,
                        CU_TENSOR_MAP_SWIZZLE_64B);
     if (!ok) return fail(TPO_ERR_INVALID_ARG, "tensor map encoding failed (pointer or size not TMA-compatible)");
-    cache_store(c, tpo::OP_AG, key, 4, p);
+    cache_store(c, tpo::OP_AG, key, 5, p);
   }
   for (int r = 0; r < c->tp; ++r) p.src[r] = static_cast<const uint8_t*>(x[r]);
   p.scale_x = d_scale_inv_x;
   p.scale_w = d_scale_inv_w;
   p.chunk_bytes = rows * c->k * elem;
   p.rows_per_group = static_cast<int>(rows);
-  p.row_tiles = static_cast<int>(rows / tpo::BM);
+  p.row_tiles = static_cast<int>(rows / (tpo::BM * cg));
   p.col_tiles = static_cast<int>(c->m / tpo::BN);
   p.num_groups = c->tp;
   p.kb_per_seg = static_cast<int>(c->k * elem / tpo::BK_BYTES);
@@ -416,11 +458,13 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
 
   tpo_status st = reset_trace(c, s);
   if (st != TPO_OK) return st;
+  const int64_t gemm_want = c->gemm_ctas ? c->gemm_ctas : c->num_sms;
   switch (c->mode) {
     case 0: {  // overlapped: one cooperative launch, producer and GEMM co-resident
-      const int P = static_cast<int>(c->producer_sms);
-      const int G = clamp_grid(c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, tiles);
-      if (P < 1 || c->num_sms - P < 1 || P + G > c->max_coop_grid)
+      int P = static_cast<int>(c->producer_sms);
+      if (cg == 2) P += P & 1;  // clusters of two: producers come in pairs too
+      const int G = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, P, tiles);
+      if (P < 1 || c->num_sms - P < cg || P + G > c->max_coop_grid)
         return fail(TPO_ERR_INVALID_ARG, "producer_sms=%d + gemm CTAs=%d exceed the %d co-resident CTAs", P, G,
                     c->max_coop_grid);
       advance_targets(c, p, P);
@@ -433,16 +477,18 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       advance_targets(c, p, Pc);
       p.num_producers = Pc;
       p.num_gemm = 0;
+      p.cta_group = 1;  // a producer-only launch needs no CTA pairs
       st = launch(c, p, Pc, false, s);
       if (st != TPO_OK) return st;
+      p.cta_group = cg;
       p.num_producers = 0;
-      p.num_gemm = clamp_grid(c->gemm_ctas ? c->gemm_ctas : c->num_sms, tiles);
+      p.num_gemm = gemm_grid(c, cg, gemm_want, 0, tiles);
       return launch(c, p, p.num_gemm, false, s);
     }
     case 2: {  // GEMM only: chunks published by an earlier call
       std::memcpy(p.target, c->target, sizeof(p.target));
       p.num_producers = 0;
-      p.num_gemm = clamp_grid(c->gemm_ctas ? c->gemm_ctas : c->num_sms, tiles);
+      p.num_gemm = gemm_grid(c, cg, gemm_want, 0, tiles);
       return launch(c, p, p.num_gemm, false, s);
     }
     default: {  // producer only
@@ -451,6 +497,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       advance_targets(c, p, P);
       p.num_producers = P;
       p.num_gemm = 0;
+      p.cta_group = 1;
       return launch(c, p, P, false, s);
     }
   }
@@ -459,11 +506,16 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
 static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const void* const* w,
                                 void* const* yb, void* y, int n_chunks, cudaStream_t s) {
   const int64_t kr = c->k / c->tp;
+  const int groups = (op == tpo::OP_RS) ? c->tp : n_chunks;
+  const int64_t rows_per_group = c->n / groups;
+  const int cg = choose_cg(c, rows_per_group, op == tpo::OP_AR ? rows_per_group / c->tp : rows_per_group);
+  if (cg < 0) return fail(TPO_ERR_UNSUPPORTED, "cta_group=2 needs 256-row tile groups and placeable CTA pairs");
   Params p;
   std::memset(&p, 0, sizeof(p));
   base_params(c, p);
   p.op = op;
-  const void* key[3 * TPO_MAX_TP + 1];
+  p.cta_group = cg;
+  const void* key[3 * TPO_MAX_TP + 2];
   int nkey = 0;
   for (int r = 0; r < c->tp; ++r) {
     key[nkey++] = x[r];
@@ -471,12 +523,13 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
     key[nkey++] = (op == tpo::OP_RS) ? yb[r] : nullptr;
   }
   key[nkey++] = y;
+  key[nkey++] = reinterpret_cast<const void*>(static_cast<intptr_t>(cg));
   if (!cache_lookup(c, op, key, nkey, p)) {
     bool ok = true;
     for (int r = 0; r < c->tp && ok; ++r) {
       ok = encode2d(&p.mapA[r], x[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, c->n, 64, tpo::BM,
                     CU_TENSOR_MAP_SWIZZLE_128B) &&
-           encode2d(&p.mapB[r], w[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, c->m, 64, tpo::BN,
+           encode2d(&p.mapB[r], w[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, c->m, 64, tpo::BN / cg,
                     CU_TENSOR_MAP_SWIZZLE_128B);
       if (ok && op == tpo::OP_RS)
         ok = encode2d(&p.mapY[r], yb[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->m, c->n / c->tp, tpo::EPI_COLS,
@@ -488,9 +541,8 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
     if (!ok) return fail(TPO_ERR_INVALID_ARG, "tensor map encoding failed (pointer or size not TMA-compatible)");
     cache_store(c, op, key, nkey, p);
   }
-  const int groups = (op == tpo::OP_RS) ? c->tp : n_chunks;
-  p.rows_per_group = static_cast<int>(c->n / groups);
-  p.row_tiles = p.rows_per_group / tpo::BM;
+  p.rows_per_group = static_cast<int>(rows_per_group);
+  p.row_tiles = p.rows_per_group / (tpo::BM * cg);
   p.col_tiles = static_cast<int>(c->m / tpo::BN);
   p.num_groups = groups;
   p.kb_per_seg = static_cast<int>(kr * 2 / tpo::BK_BYTES);
@@ -506,11 +558,12 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
       c->ar_target = 0;
       c->ar_chunks = n_chunks;
     }
-    c->ar_target += static_cast<uint32_t>(p.row_tiles * p.col_tiles * tpo::EPI_WARPS);
+    // one release per epilogue warp and 128-row share of every tile of the chunk
+    c->ar_target += static_cast<uint32_t>((rows_per_group / tpo::BM) * p.col_tiles * tpo::EPI_WARPS);
     p.ar_target = c->ar_target;
   }
   p.num_producers = 0;
-  p.num_gemm = clamp_grid(c->gemm_ctas ? c->gemm_ctas : c->num_sms, tiles);
+  p.num_gemm = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms, 0, tiles);
   return launch(c, p, p.num_gemm, false, s);
 }
 

@@ -15,7 +15,10 @@
 //    acquire-wait on the slot's counter for gathered rows), warp 1 issues
 //    tcgen05.mma from one thread into a double-buffered fp32 accumulator in
 //    tensor memory, warps 2..5 drain the accumulator (tcgen05.ld), round to
-//    bf16 and TMA-store the tile.  This replaces the counter-gated cuBLAS
+//    bf16 and TMA-store the tile.  In the pair variant (CG = 2) two CTAs of a
+//    cluster share one 256 x 256 tile through the 2-SM MMA: each loads its own
+//    128 rows of A and half of the B tile, the even CTA issues the MMAs, and
+//    each CTA's tensor memory receives its own 128 rows of the result.  This replaces the counter-gated cuBLAS
 //    atomic GEMM of the same listing.  For GEMM+RS / GEMM+AR the K loop of a
 //    tile walks the ranks' K-slices in a fixed ring order into one accumulator.
 //
@@ -188,10 +191,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 }
 
 // Instruction descriptor: dense, fp32 accumulator, K-major A and B,
-// A/B bf16 (kind::f16) or e4m3 (kind::f8f6f4), M = BM, N = BN.
-__host__ __device__ constexpr uint32_t make_idesc(bool fp8) {
+// A/B bf16 (kind::f16) or e4m3 (kind::f8f6f4), M = tile rows, N = BN.
+__host__ __device__ constexpr uint32_t make_idesc(bool fp8, int m) {
   return (1u << 4) | ((fp8 ? 0u : 1u) << 7) | ((fp8 ? 0u : 1u) << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-         (static_cast<uint32_t>(BM >> 4) << 24);
+         (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -227,6 +230,105 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+
+// ------------------------------------------------------------------ clusters (CTA pairs)
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// TMA load whose completion is signalled on a barrier that may live in the peer CTA.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_alloc_cg(uint32_t slot_smem, uint32_t ncols) {
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+                 : "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tmem_relinquish_cg() {
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc_cg(uint32_t taddr, uint32_t ncols) {
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// One MMA of K = 32 bytes; CG = 2 issues the 2-SM form (M = 256 over the pair).
+template <int CG>
+__device__ __forceinline__ void mma_cg(bool fp8, uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (CG == 1) {
+    if (fp8)
+      mma_e4m3(d, a, b, idesc, acc);
+    else
+      mma_bf16(d, a, b, idesc, acc);
+  } else {
+    if (fp8)
+      asm volatile(
+          "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, P;\n\t}" ::"r"(d),
+          "l"(a), "l"(b), "r"(idesc), "r"(acc)
+          : "memory");
+    else
+      asm volatile(
+          "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, P;\n\t}" ::"r"(d),
+          "l"(a), "l"(b), "r"(idesc), "r"(acc)
+          : "memory");
+  }
+}
+// Arrive on `bar` (same offset in every CTA of the group) once all prior MMAs completed.
+template <int CG>
+__device__ __forceinline__ void mma_commit_cg(uint32_t bar) {
+  if constexpr (CG == 1) {
+    mma_commit(bar);
+  } else {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(mask)
+        : "memory");
+  }
+}
+// Commit that arrives on this CTA's barrier only.
+template <int CG>
+__device__ __forceinline__ void mma_commit_local_cg(uint32_t bar) {
+  if constexpr (CG == 1)
+    mma_commit(bar);
+  else
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // ------------------------------------------------------------------ tile schedule
 
 struct Tile {
@@ -243,6 +345,7 @@ struct Tile {
 // Tiles are ordered group by group (AG: ring step, RS: owner block, AR: row
 // chunk); inside a group column-tile-major so that consecutive CTAs share the
 // same W tile.  Every role of a CTA walks the same sequence t = g, g+G, ...
+template <int TILE_M>
 __device__ __forceinline__ Tile tile_at(const Params& p, int t) {
   const int per_group = p.row_tiles * p.col_tiles;
   const int grp = t / per_group;
@@ -256,20 +359,20 @@ __device__ __forceinline__ Tile tile_at(const Params& p, int t) {
     const int slot = ((p.self_rank - grp) % p.tp + p.tp) % p.tp;
     // ring step 0 is the observer's own chunk: read in place, nothing to wait on
     T.a_map = (grp == 0) ? 1 : 0;
-    T.a_row = (grp == 0) ? r * BM : slot * p.rows_per_group + r * BM;
+    T.a_row = (grp == 0) ? r * TILE_M : slot * p.rows_per_group + r * TILE_M;
     T.gate = (grp == 0 || !p.gate) ? -1 : slot;
     T.y_map = 0;
-    T.y_row = slot * p.rows_per_group + r * BM;
+    T.y_row = slot * p.rows_per_group + r * TILE_M;
     T.seg0 = 0;
   } else if (p.op == OP_RS) {
     T.a_map = -1;
-    T.a_row = grp * p.rows_per_group + r * BM;
+    T.a_row = grp * p.rows_per_group + r * TILE_M;
     T.gate = -1;
     T.y_map = grp;
-    T.y_row = r * BM;
+    T.y_row = r * TILE_M;
     T.seg0 = (grp + 1) % p.tp;  // ring reduce-scatter: the owner's own slice comes last
   } else {
-    const int local = r * BM;
+    const int local = r * TILE_M;
     const int owner = (local * p.tp) / p.rows_per_group;  // part of the chunk owned in a ring all-reduce
     T.a_map = -1;
     T.a_row = grp * p.rows_per_group + local;
@@ -327,7 +430,7 @@ __device__ bool copy_pieces(const Params& p, const uint8_t* src, uint8_t* dst, l
 __device__ void producer_role(const Params& p, uint8_t* smem) {
   if (threadIdx.x != 0) return;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bars = sbase + SMEM_BARS + 8u * (2 * STAGES + 5);
+  const uint32_t bars = sbase + SMEM_BARS + 8u * BAR_COPY;
   for (int b = 0; b < COPY_BUFS; ++b) mbar_init(bars + 8u * b, 1);
   fence_barrier_init();
 
@@ -384,13 +487,16 @@ struct Bars {
   uint32_t full0, empty0, tfull0, tempty0, drain;
 };
 
-__device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, int g, int G, int total_tiles, int nkb) {
+template <int CG>
+__device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, uint32_t rank, int g, int G,
+                         int total_tiles, int nkb) {
+  using PP = Pipe<CG>;
   const int kelems = p.fp8 ? BK_BYTES : BK_BYTES / 2;
   uint32_t ready = 0;
   uint32_t it = 0;
   bool ok = true;
   for (int t = g; t < total_tiles && ok; t += G) {
-    const Tile T = tile_at(p, t);
+    const Tile T = tile_at<PP::TILE_M>(p, t);
     if (T.gate >= 0 && !((ready >> T.gate) & 1u)) {
       if (!wait_counter(p, T.gate)) {
         ok = false;
@@ -399,8 +505,8 @@ __device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, int g, 
       ready |= 1u << T.gate;
     }
     for (int i = 0; i < nkb; ++i) {
-      const uint32_t stage = it % STAGES;
-      if (!mbar_wait(p, B.empty0 + 8u * stage, ((it / STAGES) & 1u) ^ 1u, SITE_EMPTY, true)) {
+      const uint32_t stage = it % PP::STAGES;
+      if (!mbar_wait(p, B.empty0 + 8u * stage, ((it / PP::STAGES) & 1u) ^ 1u, SITE_EMPTY, true)) {
         ok = false;
         break;
       }
@@ -408,24 +514,41 @@ __device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, int g, 
       const int kk = i - seg * p.kb_per_seg;
       const int amap = (p.op == OP_AG) ? T.a_map : (T.seg0 + seg) % p.tp;
       const int bmap = (p.op == OP_AG) ? 0 : amap;
-      const uint32_t sa = sbase + SMEM_STAGES + stage * STAGE_BYTES;
+      const uint32_t sa = sbase + SMEM_STAGES + stage * PP::STAGE_BYTES;
       const uint32_t full = B.full0 + 8u * stage;
-      mbar_expect_tx(full, STAGE_BYTES);
-      tma_load_2d(sa, &p.mapA[amap], full, kk * kelems, T.a_row);
-      tma_load_2d(sa + A_STAGE_BYTES, &p.mapB[bmap], full, kk * kelems, T.col);
+      if constexpr (CG == 1) {
+        mbar_expect_tx(full, PP::STAGE_BYTES);
+        tma_load_2d(sa, &p.mapA[amap], full, kk * kelems, T.a_row);
+        tma_load_2d(sa + A_STAGE_BYTES, &p.mapB[bmap], full, kk * kelems, T.col);
+      } else {
+        // both halves complete on the even CTA's barrier, which expects the pair's bytes
+        if (rank == 0) mbar_expect_tx(full, 2 * PP::STAGE_BYTES);
+        const uint32_t full_leader = map_to_rank(full, 0);
+        tma_load_2d_pair(sa, &p.mapA[amap], full_leader, kk * kelems, T.a_row + BM * static_cast<int>(rank));
+        tma_load_2d_pair(sa + A_STAGE_BYTES, &p.mapB[bmap], full_leader, kk * kelems,
+                         T.col + PP::B_ROWS * static_cast<int>(rank));
+      }
       ++it;
     }
   }
   if (!ok) {  // loads already issued must land before the CTA releases its shared memory
-    const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
-    for (uint32_t j = first; j < it; ++j)
-      mbar_wait(p, B.full0 + 8u * (j % STAGES), (j / STAGES) & 1u, SITE_DRAIN, false);
+    if (CG == 1 || rank == 0) {
+      const uint32_t first = it > static_cast<uint32_t>(PP::STAGES) ? it - PP::STAGES : 0u;
+      for (uint32_t j = first; j < it; ++j)
+        mbar_wait(p, B.full0 + 8u * (j % PP::STAGES), (j / PP::STAGES) & 1u, SITE_DRAIN, false);
+    } else if (it > 0) {
+      // the odd CTA's loads signal the even CTA's barrier: give them time to land
+      const unsigned long long t0 = gtime();
+      while (gtime() - t0 < 200000ull) __nanosleep(1000);
+    }
   }
 }
 
+template <int CG>
 __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
                          int total_tiles, int nkb) {
-  const uint32_t idesc = make_idesc(p.fp8 != 0);
+  using PP = Pipe<CG>;
+  const uint32_t idesc = make_idesc(p.fp8 != 0, PP::TILE_M);
   uint32_t it = 0, lt = 0;
   bool ok = true;
   for (int t = g; t < total_tiles; t += G, ++lt) {
@@ -437,44 +560,42 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t tmem, const B
     tc_fence_after();
     const uint32_t d = tmem + acc * BN;
     for (int i = 0; i < nkb; ++i, ++it) {
-      const uint32_t stage = it % STAGES;
-      if (!mbar_wait(p, B.full0 + 8u * stage, (it / STAGES) & 1u, SITE_FULL, true)) {
+      const uint32_t stage = it % PP::STAGES;
+      if (!mbar_wait(p, B.full0 + 8u * stage, (it / PP::STAGES) & 1u, SITE_FULL, true)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sa = sbase + SMEM_STAGES + stage * STAGE_BYTES;
+      const uint32_t sa = sbase + SMEM_STAGES + stage * PP::STAGE_BYTES;
       const uint64_t da = smem_desc_sw128(sa);
       const uint64_t db = smem_desc_sw128(sa + A_STAGE_BYTES);
       // four MMAs of K = 32 bytes each cover the 128-byte K block
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t accum = (i > 0 || kk > 0) ? 1u : 0u;
-        if (p.fp8)
-          mma_e4m3(d, da + 2u * kk, db + 2u * kk, idesc, accum);
-        else
-          mma_bf16(d, da + 2u * kk, db + 2u * kk, idesc, accum);
-      }
-      mma_commit(B.empty0 + 8u * stage);  // frees the stage once these MMAs have read it
+      for (int kk = 0; kk < 4; ++kk)
+        mma_cg<CG>(p.fp8 != 0, d, da + 2u * kk, db + 2u * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_cg<CG>(B.empty0 + 8u * stage);  // frees the stage (in both CTAs) once read
     }
     if (!ok) break;
-    mma_commit(B.tfull0 + 8u * acc);  // accumulator ready for the epilogue
+    mma_commit_cg<CG>(B.tfull0 + 8u * acc);  // accumulator ready for the epilogue(s)
   }
   if (!ok) {  // every MMA issued so far must complete before tensor memory is freed
-    mma_commit(B.drain);
+    mma_commit_local_cg<CG>(B.drain);
     mbar_wait(p, B.drain, 0u, SITE_DRAIN, false);
   }
 }
 
-__device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, const Bars& B, int g, int G,
-                              int total_tiles) {
+template <int CG>
+__device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, const Bars& B, uint32_t rank, int g,
+                              int G, int total_tiles) {
+  using PP = Pipe<CG>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;  // tensor-memory lanes this warp may read: [32*quad, 32*quad+32)
   const uint32_t ebase = smem_u32(smem + SMEM_EPI + (warp - 2) * 2 * EPI_BUF_BYTES);
   const float scale = p.fp8 ? (__ldg(p.scale_x) * __ldg(p.scale_w)) : 1.0f;
+  const int row_off = BM * static_cast<int>(rank);
   uint32_t lt = 0, nst = 0;
   for (int t = g; t < total_tiles; t += G, ++lt) {
-    const Tile T = tile_at(p, t);
+    const Tile T = tile_at<PP::TILE_M>(p, t);
     const uint32_t acc = lt & 1u;
     const uint32_t bar = B.tfull0 + 8u * acc, par = (lt >> 1) & 1u;
     int ok = (lane == 0) ? (mbar_wait(p, bar, par, SITE_TMEM_FULL, true) ? 1 : 0) : 0;
@@ -488,9 +609,15 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
       uint32_t r[32];
       tmem_ld32(taddr + c * EPI_COLS, r);
       tmem_wait_ld();
-      if (c == BN / EPI_COLS - 1) {  // accumulator fully read: hand it back to the MMA warp
+      if (c == BN / EPI_COLS - 1) {  // accumulator fully read: hand it back to the MMA issuer
         tc_fence_before();
-        mbar_arrive(B.tempty0 + 8u * acc);
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CG == 1)
+            mbar_arrive(B.tempty0 + 8u * acc);
+          else
+            mbar_arrive_cluster(map_to_rank(B.tempty0 + 8u * acc, 0));
+        }
       }
       uint32_t packed[16];
 #pragma unroll
@@ -512,7 +639,7 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_2d(&p.mapY[T.y_map], buf, T.col + c * EPI_COLS, T.y_row + quad * 32);
+        tma_store_2d(&p.mapY[T.y_map], buf, T.col + c * EPI_COLS, T.y_row + row_off + quad * 32);
         bulk_commit();
       }
     }
@@ -527,57 +654,64 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
   __syncwarp();
 }
 
+template <int CG>
 __device__ void gemm_role(const Params& p, uint8_t* smem) {
+  using PP = Pipe<CG>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
+  const uint32_t rank = (CG == 2) ? cluster_rank() : 0u;
   Bars B;
-  B.full0 = sbase + SMEM_BARS;
-  B.empty0 = B.full0 + 8u * STAGES;
-  B.tfull0 = B.empty0 + 8u * STAGES;
-  B.tempty0 = B.tfull0 + 16u;
-  B.drain = B.tempty0 + 16u;
+  B.full0 = sbase + SMEM_BARS + 8u * BAR_FULL;
+  B.empty0 = sbase + SMEM_BARS + 8u * BAR_EMPTY;
+  B.tfull0 = sbase + SMEM_BARS + 8u * BAR_TFULL;
+  B.tempty0 = sbase + SMEM_BARS + 8u * BAR_TEMPTY;
+  B.drain = sbase + SMEM_BARS + 8u * BAR_DRAIN;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_TMEM_SLOT);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < PP::STAGES; ++s) {
       mbar_init(B.full0 + 8u * s, 1);
       mbar_init(B.empty0 + 8u * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(B.tfull0 + 8u * a, 1);
-      mbar_init(B.tempty0 + 8u * a, EPI_WARPS * 32);
+      mbar_init(B.tempty0 + 8u * a, CG * EPI_WARPS);  // one arrival per epilogue warp of the group
     }
     mbar_init(B.drain, 1);
     fence_barrier_init();
   }
+  __syncwarp();
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before anyone signals them
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_cg<CG>(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_cg<CG>();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  const int g = blockIdx.x - p.num_producers, G = p.num_gemm;
+  const int g = (static_cast<int>(blockIdx.x) - p.num_producers) / CG, G = p.num_gemm / CG;
   const int total_tiles = p.num_groups * p.row_tiles * p.col_tiles;
   const int nkb = p.num_segs * p.kb_per_seg;
   if (warp == 0) {
-    if (lane == 0) tma_role(p, sbase, B, g, G, total_tiles, nkb);
+    if (lane == 0) tma_role<CG>(p, sbase, B, rank, g, G, total_tiles, nkb);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) mma_role(p, sbase, tmem, B, g, G, total_tiles, nkb);
+    if (lane == 0 && rank == 0) mma_role<CG>(p, sbase, tmem, B, g, G, total_tiles, nkb);
     __syncwarp();
   } else {
-    epilogue_role(p, smem, tmem, B, g, G, total_tiles);
+    epilogue_role<CG>(p, smem, tmem, B, rank, g, G, total_tiles);
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // neither CTA leaves while its peer may still use it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc_cg<CG>(tmem, TMEM_COLS);
   }
 }
 
+template <int CG>
 __global__ void __launch_bounds__(NUM_THREADS, 1) fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -586,7 +720,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_kernel(const __grid_cons
   if (static_cast<int>(blockIdx.x) < p.num_producers) {
     producer_role(p, smem);
   } else if (static_cast<int>(blockIdx.x) < p.num_producers + p.num_gemm) {
-    gemm_role(p, smem);
+    gemm_role<CG>(p, smem);
   }
   if (p.trace_on && threadIdx.x == 0) atomicMax(&p.words->trace[TPO_TRACE_END], gtime());
 }
@@ -594,11 +728,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_kernel(const __grid_cons
 // ------------------------------------------------------------------ host side launch
 
 cudaError_t configure_kernel() {
-  return cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  cudaError_t e = cudaFuncSetAttribute(fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  return e;
 }
 
 cudaError_t max_blocks_per_sm(int* n) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fused_kernel, NUM_THREADS, SMEM_ALLOC);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fused_kernel<1>, NUM_THREADS, SMEM_ALLOC);
+}
+
+cudaError_t max_active_pairs(int* n) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_ALLOC;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(n, fused_kernel<2>, &cfg);
 }
 
 cudaError_t launch_fused(const Params& p, int grid, bool cooperative, cudaStream_t stream) {
@@ -607,12 +759,24 @@ cudaError_t launch_fused(const Params& p, int grid, bool cooperative, cudaStream
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_ALLOC;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (cooperative) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  }
+  if (p.cta_group == 2) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = cooperative ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, fused_kernel, p);
+  cfg.numAttrs = na;
+  if (p.cta_group == 2) return cudaLaunchKernelEx(&cfg, fused_kernel<2>, p);
+  return cudaLaunchKernelEx(&cfg, fused_kernel<1>, p);
 }
 
 }  // namespace tpo

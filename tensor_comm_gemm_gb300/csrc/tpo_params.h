@@ -9,16 +9,26 @@
 
 namespace tpo {
 
-// Tile shape: one CTA computes a BM x BN output tile; every pipeline stage holds
-// a BM x 128-byte slice of A and a BN x 128-byte slice of B (64 bf16 or 128 e4m3
-// contraction elements), the width of one 128-byte swizzle row.
+// Tile shape.  A CTA owns BM rows of a BN-column output tile.  With the
+// single-SM MMA (CG = 1) one CTA computes a BM x BN tile; with the 2-SM MMA
+// (tcgen05 cta_group::2, CG = 2) a CTA pair computes a 2*BM x BN tile, each CTA
+// loading its own BM rows of A and half (BN/2 rows) of the B tile.  Every
+// pipeline stage holds 128-byte K slices (64 bf16 or 128 e4m3 contraction
+// elements), the width of one 128-byte swizzle row.
 constexpr int BM = TPO_BLOCK_M;
 constexpr int BN = TPO_BLOCK_N;
 constexpr int BK_BYTES = 128;
-constexpr int STAGES = 4;
 constexpr int A_STAGE_BYTES = BM * BK_BYTES;  // 16 KiB
-constexpr int B_STAGE_BYTES = BN * BK_BYTES;  // 32 KiB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int STAGE_AREA = 196608;            // 192 KiB of pipeline stages
+template <int CG>
+struct Pipe {
+  static constexpr int B_ROWS = BN / CG;                  // B rows one CTA loads per stage
+  static constexpr int B_STAGE_BYTES = B_ROWS * BK_BYTES;  // 32 or 16 KiB
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr int STAGES = STAGE_AREA / STAGE_BYTES;  // 4 or 6
+  static constexpr int TILE_M = BM * CG;                  // output rows of one tile
+};
+constexpr int MAX_STAGES = 6;
 constexpr int NUM_THREADS = 192;              // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int EPI_WARPS = 4;
 constexpr int EPI_COLS = 32;                  // columns per epilogue store box
@@ -32,13 +42,18 @@ constexpr int COPY_LAG = 6;
 
 // Shared memory map (offsets from a 1024-byte aligned base).
 constexpr int SMEM_STAGES = 0;
-constexpr int SMEM_EPI = SMEM_STAGES + STAGES * STAGE_BYTES;            // 196608
+constexpr int SMEM_EPI = SMEM_STAGES + STAGE_AREA;                      // 196608
 constexpr int SMEM_BARS = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;     // 212992
-constexpr int NUM_BARS = 2 * STAGES + 4 + 1 + COPY_BUFS;
+// barriers: full[MAX_STAGES], empty[MAX_STAGES], tmem_full[2], tmem_empty[2],
+// drain, copy[COPY_BUFS]
+constexpr int BAR_FULL = 0, BAR_EMPTY = MAX_STAGES, BAR_TFULL = 2 * MAX_STAGES, BAR_TEMPTY = BAR_TFULL + 2,
+              BAR_DRAIN = BAR_TEMPTY + 2, BAR_COPY = BAR_DRAIN + 1;
+constexpr int NUM_BARS = BAR_COPY + COPY_BUFS;
 constexpr int SMEM_TMEM_SLOT = SMEM_BARS + NUM_BARS * 8;
 constexpr int SMEM_USED = SMEM_TMEM_SLOT + 16;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for aligning the base
-static_assert(COPY_BUFS * COPY_PIECE <= STAGES * STAGE_BYTES, "copy ring must fit the stage area");
+static_assert(COPY_BUFS * COPY_PIECE <= STAGE_AREA, "copy ring must fit the stage area");
+static_assert(Pipe<1>::STAGES * Pipe<1>::STAGE_BYTES <= STAGE_AREA && Pipe<2>::STAGES <= MAX_STAGES, "stages");
 static_assert(SMEM_ALLOC <= 232448, "exceeds the per-CTA shared memory limit");
 
 enum Op : int { OP_AG = 0, OP_RS = 1, OP_AR = 2 };
@@ -95,11 +110,15 @@ struct Params {
   int skip_slot;          // debug: never publish this slot (-1 off)
   int last_step;          // debug: producer stops after this ring step (-1 all)
   int trace_on;
+  int cta_group;          // 1: single-SM MMA, 2: CTA pairs (cluster of 2) with the 2-SM MMA
 };
 
 // Host-side launch helpers defined next to the kernel (kernels.cu).
 cudaError_t configure_kernel();
 cudaError_t max_blocks_per_sm(int* n);
+// Largest number of co-resident CTA pairs of the 2-SM variant (0 if pairs cannot be placed).
+cudaError_t max_active_pairs(int* n);
+// Launches the variant p.cta_group selects; pair launches use clusters of 2.
 cudaError_t launch_fused(const Params& p, int grid, bool cooperative, cudaStream_t stream);
 
 // Sets the thread-local message returned by tpo_last_error (ctx.cu).

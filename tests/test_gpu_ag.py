@@ -228,3 +228,41 @@ def test_workload_ag_tp4_4096_sampled_parity():
         assert np.array_equal(host_bits(run.y), bits)
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("tp,n,k,m", [(4, 2048, 512, 768), (3, 768, 192, 768), (2, 1024, 4096, 512)])
+def test_pair_and_single_sm_variants_agree(tp, n, k, m):
+    """The 2-SM (CTA pair) MMA and the single-SM MMA compute every output
+    element with the same K order; both meet the oracle bar and agree bitwise."""
+    wl = synth.make_ag(tp, n, k, m, seed=70 + tp, dist="normal", sigma=k ** -0.25)
+    ref = ref_ag(wl)
+    run = AgRun(wl)
+    try:
+        bits = {}
+        for cg in (1, 2):
+            t.tpo_set_opt(run.ctx, "cta_group", cg)
+            for mode in (0, 1):
+                t.tpo_set_opt(run.ctx, "mode", mode)
+                run.y.fill_(float("nan"))
+                run.run()
+                assert_close(host_f64(run.y), ref)
+                bits[(cg, mode)] = host_bits(run.y)
+        assert np.array_equal(bits[(1, 0)], bits[(1, 1)]) and np.array_equal(bits[(2, 0)], bits[(2, 1)])
+        assert np.array_equal(bits[(1, 0)], bits[(2, 0)])
+    finally:
+        run.close()
+
+
+def test_pair_variant_rejected_for_128_row_slots():
+    wl = synth.make_ag(2, 256, 256, 256, seed=1, dist="uniform")
+    run = AgRun(wl)
+    try:
+        t.tpo_set_opt(run.ctx, "cta_group", 2)
+        with pytest.raises(t.TpoError) as e:
+            t.tpo_ag_gemm(run.ctx, run.xs, run.w, run.y)
+        assert e.value.status == 2
+        t.tpo_set_opt(run.ctx, "cta_group", 0)          # auto picks the single-SM variant
+        run.run()
+        assert_close(host_f64(run.y), ref_ag(wl))
+    finally:
+        run.close()

@@ -41,7 +41,7 @@ def test_rs_full_parity(tp, n, k, m):
 
 
 @pytest.mark.parametrize("tp,n,k,m,chunks", [(2, 1024, 256, 256, 4), (3, 2304, 384, 512, 2), (1, 512, 128, 512, 4),
-                                             (2, 512, 1024, 256, 1)])
+                                             (2, 512, 1024, 256, 1), (2, 2048, 512, 512, 2)])
 def test_ar_full_parity_and_done_counters(tp, n, k, m, chunks):
     wl = synth.make_ksplit("ar", tp, n, k, m, seed=30 + tp, dist="uniform", n_row_chunks=chunks)
     ref = oracle.ksplit(wl.x, wl.w)
@@ -130,5 +130,27 @@ def test_workload_rs_tp8_sampled_parity():
         tiles = synth.sample_tiles(wl.n, wl.m, 16, SAMPLE_TILES, seed=1000 + wl.seed)
         ref = oracle.ksplit(wl.x, wl.w, tiles=tiles)
         assert_close(gather_tiles(host_f64(full), tiles), ref)
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("op,tp,n,k,m,chunks", [("rs", 4, 1024, 1280, 768, 1), ("ar", 2, 2048, 512, 512, 2)])
+def test_ksplit_pair_and_single_sm_variants_agree(op, tp, n, k, m, chunks):
+    wl = synth.make_ksplit(op, tp, n, k, m, seed=80 + tp, dist="normal", sigma=k ** -0.25, n_row_chunks=chunks)
+    ref = oracle.ksplit(wl.x, wl.w)
+    run = KsplitRun(wl)
+    try:
+        outs = {}
+        for cg in (1, 2):
+            t.tpo_set_opt(run.ctx, "cta_group", cg)
+            if op == "rs":
+                run.rs()
+                y = torch.cat(run.yb, 0)
+            else:
+                run.ar(chunks)
+                y = run.y
+            assert_close(host_f64(y), ref)
+            outs[cg] = host_bits(y)
+        assert np.array_equal(outs[1], outs[2])
     finally:
         run.close()
