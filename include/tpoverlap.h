@@ -147,7 +147,9 @@ tpo_status tpo_gemm_ar(tpo_ctx* ctx, const void* const* x, const void* const* w,
 
 /*
  * Options (integers).  Keys:
- *   "producer_sms"     CTAs given to the chunk producer in overlapped AG (>=1)
+ *   "producer_sms"     CTAs given to the chunk producer in overlapped AG; 0 (the
+ *                      default) picks the largest count in [8, 32] that does not
+ *                      add a round of GEMM tiles (rounded up to even for pairs)
  *   "gemm_ctas"        CTAs given to the GEMM (0 = all SMs not producing)
  *   "mode"             AG schedule: 0 overlapped (one launch, producer and GEMM
  *                      co-resident), 1 sequential (copy to completion, then the
@@ -162,6 +164,11 @@ tpo_status tpo_gemm_ar(tpo_ctx* ctx, const void* const* x, const void* const* w,
  *   "debug_delay_ns"   producer spin before each publish
  *   "debug_last_step"  mode 3 only: the producer stops after this ring step
  *                      (-1 = all steps)
+ *   "cta_group"        MMA variant: 0 automatic, 1 single-SM 128x256 tiles,
+ *                      2 CTA pairs (2-SM MMA, 256x256 tiles; needs every tile
+ *                      group a multiple of 256 rows).  Results are identical.
+ * Read-only keys for tpo_get_opt: "last_producer_ctas", "last_gemm_ctas",
+ * "last_cta_group" (launch shape of the latest overlapped AG call).
  * Environment variables TPO_<KEY in upper case> override the defaults at
  * create time.  Unknown keys or out-of-range values: TPO_ERR_INVALID_ARG.
  */
@@ -197,6 +204,13 @@ const uint32_t* tpo_ar_done_counters(tpo_ctx* ctx, uint32_t* target);
 #define TPO_TRACE_ACQUIRE 18   /* + slot: earliest GEMM acquire of the slot */
 #define TPO_TRACE_WAIT_NS 34   /* total ns GEMM CTAs spent waiting on counters */
 #define TPO_TRACE_CHUNK_DONE 35 /* + chunk: AR chunk completion time */
+/* Pipeline diagnosis (SM clock cycles summed over GEMM CTAs): */
+#define TPO_TRACE_CYC_TMA_EMPTY 100  /* TMA issuer blocked on a free stage */
+#define TPO_TRACE_CYC_MMA_FULL 101   /* MMA issuer blocked on a loaded stage */
+#define TPO_TRACE_CYC_MMA_TEMPTY 102 /* MMA issuer blocked on a drained accumulator */
+#define TPO_TRACE_CYC_EPI_TFULL 103  /* epilogue warps blocked on a finished accumulator */
+#define TPO_TRACE_CYC_GEMM 104       /* GEMM CTAs' total cycles (set-up to tear-down) */
+#define TPO_TRACE_KBLOCKS 105        /* 128-byte K blocks issued to the tensor cores */
 #define TPO_TRACE_WORDS 128
 tpo_status tpo_read_trace(tpo_ctx* ctx, uint64_t* out, int cap);
 

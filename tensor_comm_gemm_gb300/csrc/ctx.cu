@@ -78,7 +78,7 @@ struct tpo_ctx {
   int max_pairs = 0;             // co-resident CTA pairs of the 2-SM variant
   bool coop_clusters = true;     // cooperative launches accept cluster dimensions
   // options
-  int64_t producer_sms = 8, gemm_ctas = 0, mode = 0, seq_copy_ctas = 0, self_rank = 0, wait_timeout_ms = 2000,
+  int64_t producer_sms = 0, gemm_ctas = 0, mode = 0, seq_copy_ctas = 0, self_rank = 0, wait_timeout_ms = 2000,
           trace = 0, debug_skip_chunk = -1, debug_delay_ns = 0, debug_last_step = -1, cta_group = 0;
   // device memory
   uint8_t* staging = nullptr;
@@ -91,6 +91,7 @@ struct tpo_ctx {
   cudaEvent_t last = nullptr;
   bool has_last = false;
   uint32_t last_dev_err[4] = {0, 0, 0, 0};
+  int64_t last_producers = 0, last_gemm_ctas = 0, last_cta_group = 0;  // launch shape of the latest call
   // tensor-map cache: the Params of the latest call of each op, keyed by pointers
   Params cache[3];
   const void* cache_key[3][3 * TPO_MAX_TP + 2];
@@ -106,7 +107,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
     int64_t lo, hi;
   };
   const E table[] = {
-      {"producer_sms", &tpo_ctx::producer_sms, 1, 1024},
+      {"producer_sms", &tpo_ctx::producer_sms, 0, 1024},
       {"gemm_ctas", &tpo_ctx::gemm_ctas, 0, 1 << 20},
       {"mode", &tpo_ctx::mode, 0, 3},
       {"seq_copy_ctas", &tpo_ctx::seq_copy_ctas, 0, 1 << 20},
@@ -240,6 +241,23 @@ int gemm_grid(const tpo_ctx* c, int cg, int64_t want, int producers, int tiles) 
   if (pairs > tiles) pairs = tiles;
   if (pairs < 1) pairs = 1;
   return static_cast<int>(2 * pairs);
+}
+
+// Producer CTAs of an overlapped AG call.  An explicit option wins; otherwise
+// the largest count in [8, 32] that leaves the GEMM as many rounds of tiles as
+// 8 producers would: with whole rounds, SMs beyond the last full round are
+// free for copying, and more producers publish every ring chunk sooner.
+int producer_count(const tpo_ctx* c, int cg, int tiles) {
+  if (c->producer_sms > 0) return static_cast<int>(c->producer_sms) + ((cg == 2) ? static_cast<int>(c->producer_sms & 1) : 0);
+  auto rounds = [&](int P) {
+    const int units = gemm_grid(c, cg, c->num_sms - P, P, tiles) / cg;
+    return (tiles + units - 1) / units;
+  };
+  const int r8 = rounds(8);
+  int best = 8;
+  for (int P = 8; P <= 32 && P < c->num_sms - 2 * cg; P += cg)
+    if (rounds(P) == r8) best = P;
+  return best;
 }
 
 // Validation shared by RS and AR.
@@ -396,6 +414,9 @@ tpo_status tpo_set_opt(tpo_ctx* c, const char* key, int64_t value) {
 
 tpo_status tpo_get_opt(tpo_ctx* c, const char* key, int64_t* value) {
   if (!c || !key || !value) return fail(TPO_ERR_INVALID_ARG, "NULL argument");
+  if (std::strcmp(key, "last_producer_ctas") == 0) return *value = c->last_producers, TPO_OK;
+  if (std::strcmp(key, "last_gemm_ctas") == 0) return *value = c->last_gemm_ctas, TPO_OK;
+  if (std::strcmp(key, "last_cta_group") == 0) return *value = c->last_cta_group, TPO_OK;
   int64_t lo, hi;
   int64_t* f = opt_slot(c, key, &lo, &hi);
   if (!f) return fail(TPO_ERR_INVALID_ARG, "unknown option '%s'", key);
@@ -461,8 +482,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   const int64_t gemm_want = c->gemm_ctas ? c->gemm_ctas : c->num_sms;
   switch (c->mode) {
     case 0: {  // overlapped: one cooperative launch, producer and GEMM co-resident
-      int P = static_cast<int>(c->producer_sms);
-      if (cg == 2) P += P & 1;  // clusters of two: producers come in pairs too
+      const int P = producer_count(c, cg, tiles);  // even for CTA pairs: clusters of two
       const int G = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, P, tiles);
       if (P < 1 || c->num_sms - P < cg || P + G > c->max_coop_grid)
         return fail(TPO_ERR_INVALID_ARG, "producer_sms=%d + gemm CTAs=%d exceed the %d co-resident CTAs", P, G,
@@ -470,6 +490,9 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       advance_targets(c, p, P);
       p.num_producers = P;
       p.num_gemm = G;
+      c->last_producers = P;
+      c->last_gemm_ctas = G;
+      c->last_cta_group = cg;
       return launch(c, p, P + G, true, s);
     }
     case 1: {  // sequential: the copy to completion, then the same GEMM
@@ -492,7 +515,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       return launch(c, p, p.num_gemm, false, s);
     }
     default: {  // producer only
-      const int P = static_cast<int>(c->producer_sms);
+      const int P = producer_count(c, cg, tiles);
       if (P > c->max_coop_grid) return fail(TPO_ERR_INVALID_ARG, "producer_sms too large");
       advance_targets(c, p, P);
       p.num_producers = P;

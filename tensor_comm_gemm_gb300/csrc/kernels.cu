@@ -98,6 +98,16 @@ __device__ bool mbar_wait(const Params& p, uint32_t bar, uint32_t parity, uint32
     }
   }
 }
+// mbar_wait that adds the SM cycles spent blocked to *cycles (trace runs only).
+__device__ __forceinline__ bool mbar_wait_timed(const Params& p, uint32_t bar, uint32_t parity, uint32_t site,
+                                                bool honor_abort, unsigned long long* cycles) {
+  if (!p.trace_on) return mbar_wait(p, bar, parity, site, honor_abort);
+  if (mbar_test(bar, parity)) return true;
+  const long long c0 = clock64();
+  const bool ok = mbar_wait(p, bar, parity, site, honor_abort);
+  *cycles += static_cast<unsigned long long>(clock64() - c0);
+  return ok;
+}
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -202,16 +212,14 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uin
       "{\n\t.reg .pred P;\n\t"
       "setp.ne.b32 P, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, P;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 __device__ __forceinline__ void mma_e4m3(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred P;\n\t"
       "setp.ne.b32 P, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, P;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
+      "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
@@ -296,14 +304,12 @@ __device__ __forceinline__ void mma_cg(bool fp8, uint32_t d, uint64_t a, uint64_
       asm volatile(
           "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %4, 0;\n\t"
           "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, P;\n\t}" ::"r"(d),
-          "l"(a), "l"(b), "r"(idesc), "r"(acc)
-          : "memory");
+          "l"(a), "l"(b), "r"(idesc), "r"(acc));
     else
       asm volatile(
           "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %4, 0;\n\t"
           "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, P;\n\t}" ::"r"(d),
-          "l"(a), "l"(b), "r"(idesc), "r"(acc)
-          : "memory");
+          "l"(a), "l"(b), "r"(idesc), "r"(acc));
   }
 }
 // Arrive on `bar` (same offset in every CTA of the group) once all prior MMAs completed.
@@ -487,101 +493,161 @@ struct Bars {
   uint32_t full0, empty0, tfull0, tempty0, drain;
 };
 
-template <int CG>
-__device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, uint32_t rank, int g, int G,
-                         int total_tiles, int nkb) {
+// The TMA issuer: one thread keeps every stage of the pipeline in flight.  Like
+// the MMA issuer it runs from registers only (tensor-map addresses, ring
+// position, stage and phase), so that refills follow stage releases closely.
+template <int CG, bool AG>
+__device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_t rank, int g, int G,
+                         int total_tiles, int nkb, bool trace) {
   using PP = Pipe<CG>;
+  const uint64_t mapA0 = reinterpret_cast<uint64_t>(&p.mapA[0]);
+  const uint64_t mapB0 = reinterpret_cast<uint64_t>(&p.mapB[0]);
+  constexpr uint64_t kMap = sizeof(CUtensorMap);
+  const int tp = p.tp, kb_per_seg = p.kb_per_seg;
   const int kelems = p.fp8 ? BK_BYTES : BK_BYTES / 2;
-  uint32_t ready = 0;
-  uint32_t it = 0;
+  const uint32_t full0 = B.full0, empty0 = B.empty0;
+  const uint32_t full0_leader = (CG == 2) ? map_to_rank(full0, 0) : full0;
+  const int a_off = BM * static_cast<int>(rank), b_off = PP::B_ROWS * static_cast<int>(rank);
+  uint32_t ready = 0, stage = 0, phase = 0, issued = 0;
   bool ok = true;
+  unsigned long long cyc_empty = 0;
   for (int t = g; t < total_tiles && ok; t += G) {
     const Tile T = tile_at<PP::TILE_M>(p, t);
-    if (T.gate >= 0 && !((ready >> T.gate) & 1u)) {
+    if (AG && T.gate >= 0 && !((ready >> T.gate) & 1u)) {
       if (!wait_counter(p, T.gate)) {
         ok = false;
         break;
       }
       ready |= 1u << T.gate;
     }
+    int r = AG ? T.a_map : T.seg0;  // tensor map of the current K segment
+    int kk = 0;
+    const int a_row = T.a_row + a_off, b_row = T.col + b_off;
     for (int i = 0; i < nkb; ++i) {
-      const uint32_t stage = it % PP::STAGES;
-      if (!mbar_wait(p, B.empty0 + 8u * stage, ((it / PP::STAGES) & 1u) ^ 1u, SITE_EMPTY, true)) {
+      const uint32_t eb = empty0 + 8u * stage;
+      if (!mbar_test(eb, phase ^ 1u) && !mbar_wait_timed(p, eb, phase ^ 1u, SITE_EMPTY, true, &cyc_empty)) {
         ok = false;
         break;
       }
-      const int seg = i / p.kb_per_seg;
-      const int kk = i - seg * p.kb_per_seg;
-      const int amap = (p.op == OP_AG) ? T.a_map : (T.seg0 + seg) % p.tp;
-      const int bmap = (p.op == OP_AG) ? 0 : amap;
+      const CUtensorMap* ma = reinterpret_cast<const CUtensorMap*>(mapA0 + kMap * static_cast<uint64_t>(r));
+      const CUtensorMap* mb = reinterpret_cast<const CUtensorMap*>(mapB0 + kMap * static_cast<uint64_t>(AG ? 0 : r));
       const uint32_t sa = sbase + SMEM_STAGES + stage * PP::STAGE_BYTES;
-      const uint32_t full = B.full0 + 8u * stage;
+      const int kx = kk * kelems;
       if constexpr (CG == 1) {
-        mbar_expect_tx(full, PP::STAGE_BYTES);
-        tma_load_2d(sa, &p.mapA[amap], full, kk * kelems, T.a_row);
-        tma_load_2d(sa + A_STAGE_BYTES, &p.mapB[bmap], full, kk * kelems, T.col);
+        const uint32_t fb = full0 + 8u * stage;
+        mbar_expect_tx(fb, PP::STAGE_BYTES);
+        tma_load_2d(sa, ma, fb, kx, a_row);
+        tma_load_2d(sa + A_STAGE_BYTES, mb, fb, kx, b_row);
       } else {
         // both halves complete on the even CTA's barrier, which expects the pair's bytes
-        if (rank == 0) mbar_expect_tx(full, 2 * PP::STAGE_BYTES);
-        const uint32_t full_leader = map_to_rank(full, 0);
-        tma_load_2d_pair(sa, &p.mapA[amap], full_leader, kk * kelems, T.a_row + BM * static_cast<int>(rank));
-        tma_load_2d_pair(sa + A_STAGE_BYTES, &p.mapB[bmap], full_leader, kk * kelems,
-                         T.col + PP::B_ROWS * static_cast<int>(rank));
+        if (rank == 0) mbar_expect_tx(full0 + 8u * stage, 2 * PP::STAGE_BYTES);
+        const uint32_t fl = full0_leader + 8u * stage;
+        tma_load_2d_pair(sa, ma, fl, kx, a_row);
+        tma_load_2d_pair(sa + A_STAGE_BYTES, mb, fl, kx, b_row);
       }
-      ++it;
+      ++issued;
+      if (++kk == kb_per_seg) {  // next K segment: the next rank in ring order
+        kk = 0;
+        if (!AG && ++r == tp) r = 0;
+      }
+      if (++stage == static_cast<uint32_t>(PP::STAGES)) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
   }
   if (!ok) {  // loads already issued must land before the CTA releases its shared memory
     if (CG == 1 || rank == 0) {
-      const uint32_t first = it > static_cast<uint32_t>(PP::STAGES) ? it - PP::STAGES : 0u;
-      for (uint32_t j = first; j < it; ++j)
-        mbar_wait(p, B.full0 + 8u * (j % PP::STAGES), (j / PP::STAGES) & 1u, SITE_DRAIN, false);
-    } else if (it > 0) {
+      const uint32_t first = issued > static_cast<uint32_t>(PP::STAGES) ? issued - PP::STAGES : 0u;
+      for (uint32_t j = first; j < issued; ++j)
+        mbar_wait(p, full0 + 8u * (j % PP::STAGES), (j / PP::STAGES) & 1u, SITE_DRAIN, false);
+    } else if (issued > 0) {
       // the odd CTA's loads signal the even CTA's barrier: give them time to land
       const unsigned long long t0 = gtime();
       while (gtime() - t0 < 200000ull) __nanosleep(1000);
     }
+  }
+  if (trace) atomicAdd(&p.words->trace[TPO_TRACE_CYC_TMA_EMPTY], cyc_empty);
+}
+
+template <int CG>
+__device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, uint32_t rank, int g, int G,
+                         int total_tiles, int nkb) {
+  const bool trace = p.trace_on != 0;
+  if (p.op == OP_AG)
+    tma_loop<CG, true>(p, sbase, B, rank, g, G, total_tiles, nkb, trace);
+  else
+    tma_loop<CG, false>(p, sbase, B, rank, g, G, total_tiles, nkb, trace);
+}
+
+// The MMA issuer.  tcgen05.mma issue returns only once the tensor core can take
+// the instruction, so about one MMA is ever queued: every cycle the issuing
+// thread spends between two MMAs is tensor-pipe idle time.  The loop therefore
+// keeps all state in registers (no parameter reloads), tests each stage's
+// barrier inline and only falls back to the bounded wait when it is not ready.
+template <int CG, bool FP8>
+__device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
+                         int total_tiles, int nkb, bool trace) {
+  using PP = Pipe<CG>;
+  constexpr uint32_t idesc = make_idesc(FP8, PP::TILE_M);
+  constexpr uint64_t kStageDesc = static_cast<uint64_t>(PP::STAGE_BYTES >> 4);  // stage step in the address field
+  const uint64_t da0 = smem_desc_sw128(sbase + SMEM_STAGES);
+  const uint64_t db0 = smem_desc_sw128(sbase + SMEM_STAGES + A_STAGE_BYTES);
+  const uint32_t full0 = B.full0, empty0 = B.empty0, tfull0 = B.tfull0, tempty0 = B.tempty0;
+  uint32_t stage = 0, phase = 0, lt = 0, issued = 0;
+  bool ok = true;
+  unsigned long long cyc_full = 0, cyc_tempty = 0;
+  for (int t = g; t < total_tiles; t += G, ++lt) {
+    const uint32_t acc = lt & 1u;
+    const uint32_t te = tempty0 + 8u * acc, tpar = ((lt >> 1) & 1u) ^ 1u;
+    if (!mbar_test(te, tpar) && !mbar_wait_timed(p, te, tpar, SITE_TMEM_EMPTY, true, &cyc_tempty)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d = tmem + acc * BN;
+    for (int i = 0; i < nkb; ++i) {
+      const uint32_t fb = full0 + 8u * stage;
+      if (!mbar_test(fb, phase) && !mbar_wait_timed(p, fb, phase, SITE_FULL, true, &cyc_full)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t da = da0 + kStageDesc * stage, db = db0 + kStageDesc * stage;
+      // four MMAs of K = 32 bytes each cover the 128-byte K block
+      mma_cg<CG>(FP8, d, da, db, idesc, i > 0 ? 1u : 0u);
+      mma_cg<CG>(FP8, d, da + 2u, db + 2u, idesc, 1u);
+      mma_cg<CG>(FP8, d, da + 4u, db + 4u, idesc, 1u);
+      mma_cg<CG>(FP8, d, da + 6u, db + 6u, idesc, 1u);
+      mma_commit_cg<CG>(empty0 + 8u * stage);  // frees the stage (in both CTAs) once read
+      ++issued;
+      if (++stage == static_cast<uint32_t>(PP::STAGES)) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) break;
+    mma_commit_cg<CG>(tfull0 + 8u * acc);  // accumulator ready for the epilogue(s)
+  }
+  if (!ok) {  // every MMA issued so far must complete before tensor memory is freed
+    mma_commit_local_cg<CG>(B.drain);
+    mbar_wait(p, B.drain, 0u, SITE_DRAIN, false);
+  }
+  if (trace) {
+    atomicAdd(&p.words->trace[TPO_TRACE_CYC_MMA_FULL], cyc_full);
+    atomicAdd(&p.words->trace[TPO_TRACE_CYC_MMA_TEMPTY], cyc_tempty);
+    atomicAdd(&p.words->trace[TPO_TRACE_KBLOCKS], static_cast<unsigned long long>(issued));
   }
 }
 
 template <int CG>
 __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
                          int total_tiles, int nkb) {
-  using PP = Pipe<CG>;
-  const uint32_t idesc = make_idesc(p.fp8 != 0, PP::TILE_M);
-  uint32_t it = 0, lt = 0;
-  bool ok = true;
-  for (int t = g; t < total_tiles; t += G, ++lt) {
-    const uint32_t acc = lt & 1u;
-    if (!mbar_wait(p, B.tempty0 + 8u * acc, ((lt >> 1) & 1u) ^ 1u, SITE_TMEM_EMPTY, true)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-    const uint32_t d = tmem + acc * BN;
-    for (int i = 0; i < nkb; ++i, ++it) {
-      const uint32_t stage = it % PP::STAGES;
-      if (!mbar_wait(p, B.full0 + 8u * stage, (it / PP::STAGES) & 1u, SITE_FULL, true)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t sa = sbase + SMEM_STAGES + stage * PP::STAGE_BYTES;
-      const uint64_t da = smem_desc_sw128(sa);
-      const uint64_t db = smem_desc_sw128(sa + A_STAGE_BYTES);
-      // four MMAs of K = 32 bytes each cover the 128-byte K block
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_cg<CG>(p.fp8 != 0, d, da + 2u * kk, db + 2u * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_cg<CG>(B.empty0 + 8u * stage);  // frees the stage (in both CTAs) once read
-    }
-    if (!ok) break;
-    mma_commit_cg<CG>(B.tfull0 + 8u * acc);  // accumulator ready for the epilogue(s)
-  }
-  if (!ok) {  // every MMA issued so far must complete before tensor memory is freed
-    mma_commit_local_cg<CG>(B.drain);
-    mbar_wait(p, B.drain, 0u, SITE_DRAIN, false);
-  }
+  const bool trace = p.trace_on != 0;
+  if (p.fp8)
+    mma_loop<CG, true>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
+  else
+    mma_loop<CG, false>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
 }
 
 template <int CG>
@@ -594,11 +660,12 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
   const float scale = p.fp8 ? (__ldg(p.scale_x) * __ldg(p.scale_w)) : 1.0f;
   const int row_off = BM * static_cast<int>(rank);
   uint32_t lt = 0, nst = 0;
+  unsigned long long cyc_tfull = 0;
   for (int t = g; t < total_tiles; t += G, ++lt) {
     const Tile T = tile_at<PP::TILE_M>(p, t);
     const uint32_t acc = lt & 1u;
     const uint32_t bar = B.tfull0 + 8u * acc, par = (lt >> 1) & 1u;
-    int ok = (lane == 0) ? (mbar_wait(p, bar, par, SITE_TMEM_FULL, true) ? 1 : 0) : 0;
+    int ok = (lane == 0) ? (mbar_wait_timed(p, bar, par, SITE_TMEM_FULL, true, &cyc_tfull) ? 1 : 0) : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
     mbar_wait(p, bar, par, SITE_TMEM_FULL, false);  // already complete: gives every lane its ordering
@@ -651,6 +718,7 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
     }
   }
   if (lane == 0) bulk_wait<0>();
+  if (p.trace_on && lane == 0) atomicAdd(&p.words->trace[TPO_TRACE_CYC_EPI_TFULL], cyc_tfull);
   __syncwarp();
 }
 
@@ -658,6 +726,7 @@ template <int CG>
 __device__ void gemm_role(const Params& p, uint8_t* smem) {
   using PP = Pipe<CG>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long cyc_start = clock64();
   const uint32_t sbase = smem_u32(smem);
   const uint32_t rank = (CG == 2) ? cluster_rank() : 0u;
   Bars B;
@@ -709,6 +778,8 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
     tc_fence_after();
     tmem_dealloc_cg<CG>(tmem, TMEM_COLS);
   }
+  if (p.trace_on && threadIdx.x == 0)
+    atomicAdd(&p.words->trace[TPO_TRACE_CYC_GEMM], static_cast<unsigned long long>(clock64() - cyc_start));
 }
 
 template <int CG>

@@ -20,6 +20,8 @@ STATUS = {0: "TPO_OK", 1: "TPO_ERR_INVALID_ARG", 2: "TPO_ERR_UNSUPPORTED", 3: "T
           4: "TPO_ERR_TIMEOUT", 5: "TPO_ERR_OOM"}
 TPO_TRACE_START, TPO_TRACE_END, TPO_TRACE_PUBLISH, TPO_TRACE_ACQUIRE = 0, 1, 2, 18
 TPO_TRACE_WAIT_NS, TPO_TRACE_CHUNK_DONE, TPO_TRACE_WORDS = 34, 35, 128
+TPO_TRACE_CYC_TMA_EMPTY, TPO_TRACE_CYC_MMA_FULL, TPO_TRACE_CYC_MMA_TEMPTY = 100, 101, 102
+TPO_TRACE_CYC_EPI_TFULL, TPO_TRACE_CYC_GEMM, TPO_TRACE_KBLOCKS = 103, 104, 105
 TPO_MAX_TP, TPO_MAX_ROW_CHUNKS = 16, 64
 
 # Every symbol the public header declares.
