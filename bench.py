@@ -284,6 +284,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "data": "synthetic (seeded splitmix64 normal inputs, sigma = K^-1/4)",
         "config": {"workload": "ag_tp4_4096: " + describe(HEADLINE), "mode": "overlapped (one launch)",
                    "producer_ctas": t.tpo_get_opt(ctx, "last_producer_ctas"), "gemm_ctas": t.tpo_get_opt(ctx, "last_gemm_ctas"), "cta_group": t.tpo_get_opt(ctx, "last_cta_group"),
+                   "cooperative_launch": bool(t.tpo_get_opt(ctx, "cooperative") and t.tpo_get_opt(ctx, "coop_clusters")),
                    "l2": "flushed before every step by a 256 MiB write outside the events",
                    "parallelism": "replicas only (simulated ranks in one GPU's memory)"},
         "gpu_launches": args.steps,

@@ -167,8 +167,14 @@ tpo_status tpo_gemm_ar(tpo_ctx* ctx, const void* const* x, const void* const* w,
  *   "cta_group"        MMA variant: 0 automatic, 1 single-SM 128x256 tiles,
  *                      2 CTA pairs (2-SM MMA, 256x256 tiles; needs every tile
  *                      group a multiple of 256 rows).  Results are identical.
+ *   "cooperative"      1 (default): overlapped AG is a cooperative launch, so
+ *                      the driver guarantees producer and GEMM CTAs co-resident;
+ *                      0: plain launch (the grid never exceeds the co-resident
+ *                      CTA count either way), e.g. for profilers that reject
+ *                      cooperative launches of CTA clusters
  * Read-only keys for tpo_get_opt: "last_producer_ctas", "last_gemm_ctas",
- * "last_cta_group" (launch shape of the latest overlapped AG call).
+ * "last_cta_group" (launch shape of the latest overlapped AG call),
+ * "coop_clusters" (0 once the driver refused a cooperative cluster launch).
  * Environment variables TPO_<KEY in upper case> override the defaults at
  * create time.  Unknown keys or out-of-range values: TPO_ERR_INVALID_ARG.
  */

@@ -79,7 +79,8 @@ struct tpo_ctx {
   bool coop_clusters = true;     // cooperative launches accept cluster dimensions
   // options
   int64_t producer_sms = 0, gemm_ctas = 0, mode = 0, seq_copy_ctas = 0, self_rank = 0, wait_timeout_ms = 2000,
-          trace = 0, debug_skip_chunk = -1, debug_delay_ns = 0, debug_last_step = -1, cta_group = 0;
+          trace = 0, debug_skip_chunk = -1, debug_delay_ns = 0, debug_last_step = -1, cta_group = 0,
+          cooperative = 1;
   // device memory
   uint8_t* staging = nullptr;
   size_t staging_bytes = 0;
@@ -118,6 +119,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
       {"debug_delay_ns", &tpo_ctx::debug_delay_ns, 0, 1000000000},
       {"debug_last_step", &tpo_ctx::debug_last_step, -1, TPO_MAX_TP - 1},
       {"cta_group", &tpo_ctx::cta_group, 0, 2},
+      {"cooperative", &tpo_ctx::cooperative, 0, 1},
   };
   for (const E& e : table)
     if (std::strcmp(e.k, key) == 0) {
@@ -133,7 +135,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
 
 const char* kOptKeys[] = {"producer_sms",     "gemm_ctas",      "mode",           "seq_copy_ctas",
                           "self_rank",        "wait_timeout_ms", "trace",          "debug_skip_chunk",
-                          "debug_delay_ns",   "debug_last_step", "cta_group"};
+                          "debug_delay_ns",   "debug_last_step", "cta_group",      "cooperative"};
 
 void destroy_all(tpo_ctx* c) {
   if (!c) return;
@@ -170,7 +172,7 @@ tpo_status reset_trace(tpo_ctx* c, cudaStream_t s) {
 }
 
 tpo_status launch(tpo_ctx* c, const Params& p, int grid, bool coop, cudaStream_t s) {
-  if (coop && p.cta_group == 2 && !c->coop_clusters) coop = false;
+  if (coop && (!c->cooperative || (p.cta_group == 2 && !c->coop_clusters))) coop = false;
   cudaError_t e = tpo::launch_fused(p, grid, coop, s);
   if (e != cudaSuccess && coop && p.cta_group == 2) {
     // Cooperative launches of clusters are not accepted here: launch without the
@@ -417,6 +419,7 @@ tpo_status tpo_get_opt(tpo_ctx* c, const char* key, int64_t* value) {
   if (std::strcmp(key, "last_producer_ctas") == 0) return *value = c->last_producers, TPO_OK;
   if (std::strcmp(key, "last_gemm_ctas") == 0) return *value = c->last_gemm_ctas, TPO_OK;
   if (std::strcmp(key, "last_cta_group") == 0) return *value = c->last_cta_group, TPO_OK;
+  if (std::strcmp(key, "coop_clusters") == 0) return *value = c->coop_clusters ? 1 : 0, TPO_OK;
   int64_t lo, hi;
   int64_t* f = opt_slot(c, key, &lo, &hi);
   if (!f) return fail(TPO_ERR_INVALID_ARG, "unknown option '%s'", key);
