@@ -133,6 +133,23 @@ class Clocks:
                 "power_w_max": max(power) if power else None}
 
 
+# ---------------------------------------------------------------------------- aggregation
+
+def slowest_rank_ms(ms, dist, device=None):
+    """Per-step time of the slowest rank (every rank runs its own replica)."""
+    if dist is None:
+        return ms
+    import torch
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_tflops(flops_per_replica, world, ms):
+    """Work of all ranks divided by the slowest rank's time."""
+    return world * flops_per_replica / (ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------------------- GPU arm
 
 def gpu_arm(args, rank, world, local_rank, dist):
@@ -232,12 +249,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
     clk = clocks.stop(wall0, wall1)
     check(ctx)
     step_ms = [a.elapsed_time(b) for a, b in evs]
-    ms = mean(step_ms)
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = world * flops / (ms * 1e-3) / 1e12
+    ms = slowest_rank_ms(mean(step_ms), dist, dev)
+    value = whole_job_tflops(flops, world, ms)
 
     # ---- end to end through the C ABI with host buffers: H2D inputs, call, D2H Y
     hx = [torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).pin_memory() for x in wl.x]
@@ -401,8 +414,7 @@ def reference_arm(args):
     g = oracle.gather(wl.x)
     tile = 16
     per_tile = 2.0 * tile * tile * wl.k
-    total_budget = 120.0
-    per_step = max(0.5, total_budget / max(1, args.steps + args.warmup))
+    per_step = args.reference_seconds / max(1, args.steps + args.warmup)
     probe = synth.sample_tiles(wl.n, wl.m, tile, 16, seed=7)
     t0 = time.perf_counter()
     oracle.ag(g, wl.w[0], tiles=probe)
@@ -440,6 +452,8 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=90.0,
+                    help="oracle work for the whole reference-arm run (split over its steps)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
