@@ -65,7 +65,8 @@ def _lib():
             lib.oracle_staging_after_step.argtypes = [i32, i32, i32, i64, i64, p, ctypes.c_uint8, p]
             lib.oracle_ag_tiles.argtypes = [i32, i64, i64, p, p, ctypes.c_double, ctypes.c_double,
                                             i64, p, p, i64, i64, p, i32]
-            lib.oracle_ksplit_tiles.argtypes = [i32, i32, i64, i64, p, p, i64, p, p, i64, i64, p, i32]
+            lib.oracle_ksplit_tiles.argtypes = [i32, i32, i64, i64, p, p, ctypes.c_double, ctypes.c_double,
+                                                i64, p, p, i64, i64, p, i32]
             _handle = lib
     return _handle
 
@@ -147,8 +148,9 @@ def ag(g: np.ndarray, w: np.ndarray, sx: float = 1.0, sw: float = 1.0, tiles=Non
     return out[0] if th == n and tw == m and len(tiles) == 1 else out
 
 
-def ksplit(xs, ws, tiles=None, tile=16, nthreads=None) -> np.ndarray:
-    """Reference Y = sum_r X_r . W_r^T (double); tiles as in ``ag``."""
+def ksplit(xs, ws, tiles=None, tile=16, nthreads=None, sx: float = 1.0, sw: float = 1.0) -> np.ndarray:
+    """Reference Y = sum_r X_r . W_r^T (double), times sx * sw for e4m3 inputs;
+    tiles as in ``ag``."""
     xs = [np.ascontiguousarray(x) for x in xs]
     ws = [np.ascontiguousarray(x) for x in ws]
     n, kr = xs[0].shape
@@ -160,7 +162,7 @@ def ksplit(xs, ws, tiles=None, tile=16, nthreads=None) -> np.ndarray:
         th = tw = tile
     tiles, r0, c0 = _tiles(tiles, th, tw)
     out = np.empty((len(tiles), th, tw), dtype=np.float64)
-    rc = _lib().oracle_ksplit_tiles(_dt(xs[0]), len(xs), kr, m, _ptrs(xs), _ptrs(ws), len(tiles),
+    rc = _lib().oracle_ksplit_tiles(_dt(xs[0]), len(xs), kr, m, _ptrs(xs), _ptrs(ws), float(sx), float(sw), len(tiles),
                                     r0.ctypes.data, c0.ctypes.data, th, tw, out.ctypes.data,
                                     nthreads or threads())
     if rc:

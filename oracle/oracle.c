@@ -145,6 +145,7 @@ static void do_item(work_t* w, int64_t item) {
       for (int r = 0; r < w->tp; ++r)
         for (int64_t q = 0; q < w->k; ++q)
           acc += elem(w->dtype, w->xs[r], i * w->k + q) * elem(w->dtype, w->ws[r], c * w->k + q);
+      acc *= w->scale;
     }
     o[cc] = acc;
   }
@@ -196,14 +197,18 @@ int oracle_ag_tiles(int dtype, int64_t k, int64_t m, const void* g, const void* 
 }
 
 /* K-split sum reference on a list of tiles:
- * out[t][a][b] = sum_r sum_q X_r[r0[t]+a, q] * W_r[c0[t]+b, q], q < kr. */
+ * out[t][a][b] = scale * sum_r sum_q X_r[r0[t]+a, q] * W_r[c0[t]+b, q], q < kr,
+ * scale = sx * sw for e4m3 inputs (one scale_inv for all X_r, one for all
+ * W_r, the per-tensor scaling the gathered input carries in the AG listing,
+ * applied to the K-split case), 1 for bf16. */
 int oracle_ksplit_tiles(int dtype, int tp, int64_t kr, int64_t m, const void* const* xs, const void* const* ws,
-                        int64_t ntiles, const int64_t* r0, const int64_t* c0, int64_t th, int64_t tw,
-                        double* out, int nthreads) {
+                        double sx, double sw, int64_t ntiles, const int64_t* r0, const int64_t* c0, int64_t th,
+                        int64_t tw, double* out, int nthreads) {
   if ((dtype != 0 && dtype != 1) || tp < 1 || kr < 1 || m < 1) return 1;
   work_t wk;
   memset(&wk, 0, sizeof(wk));
   wk.kind = 1; wk.dtype = dtype; wk.tp = tp; wk.k = kr; wk.m = m; wk.xs = xs; wk.ws = ws;
+  wk.scale = (dtype == 1) ? sx * sw : 1.0;
   wk.ntiles = ntiles; wk.th = th; wk.tw = tw; wk.r0 = r0; wk.c0 = c0; wk.out = out;
   return run(&wk, nthreads);
 }

@@ -209,3 +209,19 @@ def test_ag_fp8_scales():
     y = oracle.ag(oracle.gather([enc(x) for x in xs_f]), enc(w_f), sx=0.5, sw=0.25)
     ref = np.concatenate(xs_f, 0).astype(np.float64) @ w_f.astype(np.float64).T * 0.125
     assert np.array_equal(y, ref)
+
+
+def test_ksplit_fp8_scales():
+    """e4m3 K-slices carry one scale_inv for all X_r and one for all W_r: the
+    sum over ranks is multiplied by sx * sw."""
+    rng = np.random.default_rng(11)
+    vals = np.array([0, 1, -1, 2, -2, 0.5, 3, -4, 0.25], dtype=np.float32)
+    xs_f = [rng.choice(vals, size=(4, 16)) for _ in range(3)]
+    ws_f = [rng.choice(vals, size=(5, 16)) for _ in range(3)]
+    enc = synth.f32_to_e4m3_bits
+    y = oracle.ksplit([enc(x) for x in xs_f], [enc(w) for w in ws_f], sx=0.5, sw=0.25)
+    ref = sum(x.astype(np.float64) @ w.astype(np.float64).T for x, w in zip(xs_f, ws_f)) * 0.125
+    assert np.array_equal(y, ref)
+    # bf16 inputs ignore the scale arguments
+    yb = oracle.ksplit([bf16(x) for x in xs_f], [bf16(w) for w in ws_f], sx=0.5, sw=0.25)
+    assert np.array_equal(yb, ref / 0.125)
