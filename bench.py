@@ -377,6 +377,23 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
         t.tpo_ctx_destroy(ctx)
         del fn
         torch.cuda.empty_cache()
+    # the GEMM+RS down-projection shape with e4m3 K-slices (one scale for all X_r, one for all W_r)
+    wl = synth.make_ksplit("rs", 8, 16384, 28672, 8192, seed=5, dtype="e4m3", name="rs_fp8_tp8_16384x8192x28672")
+    xs = [to_dev(x) for x in wl.x]
+    ws = [to_dev(x) for x in wl.w]
+    yb = [torch.empty((wl.n // wl.tp, wl.m), dtype=torch.bfloat16, device=dev) for _ in range(wl.tp)]
+    sx = torch.tensor([wl.scale_inv_x], dtype=torch.float32, device=dev)
+    sw = torch.tensor([wl.scale_inv_w], dtype=torch.float32, device=dev)
+    ctx = t.tpo_ctx_create(wl.tp, wl.n, wl.k, wl.m, t.TPO_FP8_E4M3)
+    t.tpo_set_fp8_scales(ctx, sx, sw)
+    ms = mean(time_steps(lambda: t.tpo_gemm_rs(ctx, xs, ws, yb), steps, 3))
+    check(ctx)
+    flops = 2.0 * wl.n * wl.k * wl.m
+    out[wl.name] = {"workload": "GEMM+RS e4m3 tp=8: X_r [16384,3584], W_r [8192,3584] -> 8 blocks [2048,8192]",
+                    "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+                    "frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / (peak * FP8_OVER_BF16), 4),
+                    "peak_tflops": peak * FP8_OVER_BF16}
+    t.tpo_ctx_destroy(ctx)
     return out
 
 

@@ -80,7 +80,7 @@ typedef enum {
  *   tp     number of simulated ranks, 1..16
  *   n      rows of Y, a multiple of tp*128
  *   k      global contraction length: a multiple of 64 (bf16) or 128 (e4m3);
- *          for RS/AR also k % tp == 0 and k/tp a multiple of 64
+ *          for RS/AR also k % tp == 0 and k/tp a multiple of 64 (128 for e4m3)
  *   m      columns of Y, a multiple of 256
  *   dtype  a tpo_dtype value
  * Allocates the staging buffer (n*k elements), counters, error word and trace
@@ -126,7 +126,8 @@ tpo_status tpo_ag_gemm(tpo_ctx* ctx, const void* const* x, const void* w, void* 
  * The partial products are summed in a fixed ring order inside one GEMM:
  * the output rows owned by rank b accumulate ranks b+1, b+2, ..., b (mod tp),
  * the order of a ring reduce-scatter that ends at the owner, in fp32, with a
- * single rounding to bf16 in the epilogue.  bf16 contexts only.
+ * single rounding to bf16 in the epilogue.  e4m3 contexts take their scales
+ * from tpo_set_fp8_scales and need (k/tp) a multiple of 128.
  */
 tpo_status tpo_gemm_rs(tpo_ctx* ctx, const void* const* x, const void* const* w, void* const* y,
                        void* stream);
@@ -140,10 +141,22 @@ tpo_status tpo_gemm_rs(tpo_ctx* ctx, const void* const* x, const void* const* w,
  * chunk c, the rows of the chunk's i-th of tp equal parts sum ranks i+1, ...,
  * i (mod tp), the per-part order of a ring all-reduce of that chunk.  After
  * every tile of chunk c is stored, the chunk's done counter (see
- * tpo_ar_done_counters) reaches its target with release semantics.  bf16 only.
+ * tpo_ar_done_counters) reaches its target with release semantics.  e4m3
+ * contexts as tpo_gemm_rs.
  */
 tpo_status tpo_gemm_ar(tpo_ctx* ctx, const void* const* x, const void* const* w, void* y,
                        int n_row_chunks, void* stream);
+
+/*
+ * Scales for GEMM+RS / GEMM+AR on an e4m3 context: device pointers to one fp32
+ * each, the scale_inv shared by all X_r and the one shared by all W_r (one
+ * per-tensor scale across the ranks' K-slices, as the gathered AG input
+ * carries one).  The accumulated sum is multiplied by both in fp32 before the
+ * bf16 rounding.  The pointers are read by every later RS/AR call (they must
+ * stay valid); required before the first RS/AR call of an e4m3 context;
+ * TPO_ERR_INVALID_ARG on a bf16 context or NULL pointers.
+ */
+tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const float* d_scale_inv_w);
 
 /*
  * Options (integers).  Keys:

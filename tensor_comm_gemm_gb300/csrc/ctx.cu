@@ -92,6 +92,8 @@ struct tpo_ctx {
   cudaEvent_t last = nullptr;
   bool has_last = false;
   uint32_t last_dev_err[4] = {0, 0, 0, 0};
+  const float* ks_scale_x = nullptr;  // e4m3 RS/AR scale_inv pointers (tpo_set_fp8_scales)
+  const float* ks_scale_w = nullptr;
   int64_t last_producers = 0, last_gemm_ctas = 0, last_cta_group = 0;  // launch shape of the latest call
   // tensor-map cache: the Params of the latest call of each op, keyed by pointers
   Params cache[3];
@@ -264,10 +266,12 @@ int producer_count(const tpo_ctx* c, int cg, int tiles) {
 
 // Validation shared by RS and AR.
 tpo_status check_ksplit(tpo_ctx* c, const void* const* x, const void* const* w) {
-  if (c->dtype != TPO_BF16) return fail(TPO_ERR_UNSUPPORTED, "GEMM+RS/AR supports bf16 contexts only");
-  if (c->k % c->tp != 0 || (c->k / c->tp) % 64 != 0)
-    return fail(TPO_ERR_UNSUPPORTED, "k/tp must be an integer multiple of 64 (k=%lld, tp=%d)", (long long)c->k,
+  const int kq = c->dtype == TPO_BF16 ? 64 : 128;
+  if (c->k % c->tp != 0 || (c->k / c->tp) % kq != 0)
+    return fail(TPO_ERR_UNSUPPORTED, "k/tp must be an integer multiple of %d (k=%lld, tp=%d)", kq, (long long)c->k,
                 c->tp);
+  if (c->dtype == TPO_FP8_E4M3 && (!c->ks_scale_x || !c->ks_scale_w))
+    return fail(TPO_ERR_INVALID_ARG, "e4m3 GEMM+RS/AR needs tpo_set_fp8_scales first");
   if (!x || !w) return fail(TPO_ERR_INVALID_ARG, "x and w must be arrays of tp device pointers");
   for (int r = 0; r < c->tp; ++r)
     if (!aligned16(x[r]) || !aligned16(w[r]))
@@ -550,13 +554,15 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   }
   key[nkey++] = y;
   key[nkey++] = reinterpret_cast<const void*>(static_cast<intptr_t>(cg));
+  const bool fp8 = c->dtype == TPO_FP8_E4M3;
+  const int elem = fp8 ? 1 : 2;
+  const int kel = tpo::BK_BYTES / elem;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!cache_lookup(c, op, key, nkey, p)) {
     bool ok = true;
     for (int r = 0; r < c->tp && ok; ++r) {
-      ok = encode2d(&p.mapA[r], x[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, c->n, 64, tpo::BM,
-                    CU_TENSOR_MAP_SWIZZLE_128B) &&
-           encode2d(&p.mapB[r], w[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kr, c->m, 64, tpo::BN / cg,
-                    CU_TENSOR_MAP_SWIZZLE_128B);
+      ok = encode2d(&p.mapA[r], x[r], dt, elem, kr, c->n, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           encode2d(&p.mapB[r], w[r], dt, elem, kr, c->m, kel, tpo::BN / cg, CU_TENSOR_MAP_SWIZZLE_128B);
       if (ok && op == tpo::OP_RS)
         ok = encode2d(&p.mapY[r], yb[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->m, c->n / c->tp, tpo::EPI_COLS,
                       32, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -571,9 +577,11 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   p.row_tiles = p.rows_per_group / (tpo::BM * cg);
   p.col_tiles = static_cast<int>(c->m / tpo::BN);
   p.num_groups = groups;
-  p.kb_per_seg = static_cast<int>(kr * 2 / tpo::BK_BYTES);
+  p.kb_per_seg = static_cast<int>(kr * elem / tpo::BK_BYTES);
   p.num_segs = c->tp;
   p.gate = 0;
+  p.scale_x = c->ks_scale_x;
+  p.scale_w = c->ks_scale_w;
   const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
   tpo_status st = reset_trace(c, s);
   if (st != TPO_OK) return st;
@@ -614,6 +622,15 @@ tpo_status tpo_gemm_ar(tpo_ctx* c, const void* const* x, const void* const* w, v
   if (c->n % (static_cast<int64_t>(n_row_chunks) * c->tp * tpo::BM) != 0)
     return fail(TPO_ERR_UNSUPPORTED, "n=%lld must be a multiple of n_row_chunks*tp*%d", (long long)c->n, tpo::BM);
   return ksplit_common(c, tpo::OP_AR, x, w, nullptr, y, n_row_chunks, static_cast<cudaStream_t>(stream));
+}
+
+tpo_status tpo_set_fp8_scales(tpo_ctx* c, const float* d_scale_inv_x, const float* d_scale_inv_w) {
+  if (!c) return fail(TPO_ERR_INVALID_ARG, "NULL context");
+  if (c->dtype != TPO_FP8_E4M3) return fail(TPO_ERR_INVALID_ARG, "scales apply to e4m3 contexts only");
+  if (!d_scale_inv_x || !d_scale_inv_w) return fail(TPO_ERR_INVALID_ARG, "scale pointers must be non-NULL");
+  c->ks_scale_x = d_scale_inv_x;
+  c->ks_scale_w = d_scale_inv_w;
+  return TPO_OK;
 }
 
 tpo_status tpo_sync_status(tpo_ctx* c) {

@@ -277,11 +277,21 @@ def make_ag(tp, n, k, m, seed, dist="uniform", sigma=1.0, dtype="bf16", name="ag
     return Workload(name, "ag", "e4m3", tp, n, k, m, xq, wq, sx, sw, seed=seed)
 
 
-def make_ksplit(op, tp, n, k, m, seed, dist="normal", sigma=1.0, n_row_chunks=1, name=None) -> Workload:
+def make_ksplit(op, tp, n, k, m, seed, dist="normal", sigma=1.0, n_row_chunks=1, name=None,
+                dtype="bf16") -> Workload:
     kr = k // tp
-    x = [_bf16_tensor(seed, r, (n, kr), dist, sigma) for r in range(tp)]
-    w = [_bf16_tensor(seed, 100 + r, (m, kr), dist, sigma) for r in range(tp)]
-    return Workload(name or op, op, "bf16", tp, n, k, m, x, w, n_row_chunks=n_row_chunks, seed=seed)
+    if dtype == "bf16":
+        x = [_bf16_tensor(seed, r, (n, kr), dist, sigma) for r in range(tp)]
+        w = [_bf16_tensor(seed, 100 + r, (m, kr), dist, sigma) for r in range(tp)]
+        return Workload(name or op, op, "bf16", tp, n, k, m, x, w, n_row_chunks=n_row_chunks, seed=seed)
+    # e4m3: N(0,1) values, one amax-derived scale for all X_r and one for all W_r
+    xs = [fast_normal_f32(stream_key(seed, r), n * kr, 1.0).reshape(n, kr) for r in range(tp)]
+    xq, sx = _quantize_e4m3(xs)
+    del xs
+    ws = [fast_normal_f32(stream_key(seed, 100 + r), m * kr, 1.0).reshape(m, kr) for r in range(tp)]
+    wq, sw = _quantize_e4m3(ws)
+    del ws
+    return Workload(name or op, op, "e4m3", tp, n, k, m, xq, wq, sx, sw, n_row_chunks=n_row_chunks, seed=seed)
 
 
 def workload(idx: int) -> Workload:

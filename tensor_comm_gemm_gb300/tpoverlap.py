@@ -27,7 +27,7 @@ TPO_MAX_TP, TPO_MAX_ROW_CHUNKS = 16, 64
 # Every symbol the public header declares.
 EXPORTS = ["tpo_ctx_create", "tpo_ctx_destroy", "tpo_ag_gemm", "tpo_gemm_rs", "tpo_gemm_ar", "tpo_set_opt",
            "tpo_get_opt", "tpo_sync_status", "tpo_last_device_error", "tpo_last_error", "tpo_staging_ptr",
-           "tpo_ar_done_counters", "tpo_read_trace", "tpo_version", "tpo_ag_gemm_noalloc"]
+           "tpo_ar_done_counters", "tpo_read_trace", "tpo_version", "tpo_ag_gemm_noalloc", "tpo_set_fp8_scales"]
 TPO_NOALLOC_MAX_STAGING_BYTES = 32 << 20
 
 
@@ -68,6 +68,8 @@ def lib(path: Optional[str] = None):
     L.tpo_read_trace.argtypes = [p, ctypes.POINTER(ctypes.c_uint64), i32]
     L.tpo_version.restype = ctypes.c_char_p
     L.tpo_ag_gemm_noalloc.argtypes = [i32, i64, i64, i64, i32, p, p, p, p, p, p]
+    L.tpo_set_fp8_scales.argtypes = [p, p, p]
+    L.tpo_set_fp8_scales.restype = ctypes.c_int
     L.tpo_ag_gemm_noalloc.restype = ctypes.c_int
     for name in ("tpo_ctx_destroy", "tpo_ag_gemm", "tpo_gemm_rs", "tpo_gemm_ar", "tpo_set_opt", "tpo_get_opt",
                  "tpo_sync_status", "tpo_last_device_error", "tpo_read_trace"):
@@ -132,6 +134,10 @@ def tpo_gemm_rs(ctx: int, x: Sequence, w: Sequence, y: Sequence, stream=None) ->
 
 def tpo_gemm_ar(ctx: int, x: Sequence, w: Sequence, y, n_row_chunks: int, stream=None) -> None:
     _check(lib().tpo_gemm_ar(ctx, _ptr_array(x), _ptr_array(w), _ptr(y), n_row_chunks, _stream(stream)))
+
+
+def tpo_set_fp8_scales(ctx: int, scale_inv_x, scale_inv_w) -> None:
+    _check(lib().tpo_set_fp8_scales(ctx, _ptr(scale_inv_x), _ptr(scale_inv_w)))
 
 
 def tpo_set_opt(ctx: int, key: str, value: int) -> None:

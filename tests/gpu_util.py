@@ -86,7 +86,12 @@ class KsplitRun:
         tp, n, m = wl.tp, wl.n, wl.m
         self.y = torch.empty((n, m), dtype=torch.bfloat16, device="cuda")
         self.yb = [torch.empty((n // tp, m), dtype=torch.bfloat16, device="cuda") for _ in range(tp)]
-        self.ctx = t.tpo_ctx_create(tp, n, wl.k, m, t.TPO_BF16)
+        self.fp8 = wl.dtype == "e4m3"
+        self.ctx = t.tpo_ctx_create(tp, n, wl.k, m, t.TPO_FP8_E4M3 if self.fp8 else t.TPO_BF16)
+        if self.fp8:
+            self.sx = torch.tensor([wl.scale_inv_x], dtype=torch.float32, device="cuda")
+            self.sw = torch.tensor([wl.scale_inv_w], dtype=torch.float32, device="cuda")
+            t.tpo_set_fp8_scales(self.ctx, self.sx, self.sw)
 
     def rs(self, sync=True):
         t.tpo_gemm_rs(self.ctx, self.xs, self.ws, self.yb)

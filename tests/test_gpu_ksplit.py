@@ -100,8 +100,21 @@ def test_ksplit_rejects_fp8_and_bad_shapes():
     ctx = t.tpo_ctx_create(2, 256, 256, 256, t.TPO_FP8_E4M3)
     try:
         x = torch.zeros((256, 128), dtype=torch.uint8, device="cuda")
-        with pytest.raises(t.TpoError) as e:
+        with pytest.raises(t.TpoError) as e:       # e4m3 RS/AR needs its scales first
             t.tpo_gemm_rs(ctx, [x, x], [x, x], [x, x])
+        assert e.value.status == 1
+        with pytest.raises(t.TpoError) as e:
+            t.tpo_set_fp8_scales(ctx, 0, x)
+        assert e.value.status == 1
+    finally:
+        t.tpo_ctx_destroy(ctx)
+    ctx = t.tpo_ctx_create(4, 512, 256, 256, t.TPO_FP8_E4M3)    # k/tp = 64: not a whole e4m3 K block
+    try:
+        sc = torch.ones(1, device="cuda")
+        t.tpo_set_fp8_scales(ctx, sc, sc)
+        x = torch.zeros((512, 64), dtype=torch.uint8, device="cuda")
+        with pytest.raises(t.TpoError) as e:
+            t.tpo_gemm_rs(ctx, [x] * 4, [x] * 4, [x] * 4)
         assert e.value.status == 2
     finally:
         t.tpo_ctx_destroy(ctx)
@@ -152,5 +165,38 @@ def test_ksplit_pair_and_single_sm_variants_agree(op, tp, n, k, m, chunks):
             assert_close(host_f64(y), ref)
             outs[cg] = host_bits(y)
         assert np.array_equal(outs[1], outs[2])
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("op,tp,n,k,m,chunks", [("rs", 2, 256, 256, 256, 1), ("rs", 4, 1024, 1024, 768, 1),
+                                                ("ar", 2, 2048, 512, 512, 2), ("ar", 3, 2304, 384, 256, 2)])
+def test_fp8_ksplit_full_parity(op, tp, n, k, m, chunks):
+    wl = synth.make_ksplit(op, tp, n, k, m, seed=90 + tp, n_row_chunks=chunks, dtype="e4m3")
+    ref = oracle.ksplit(wl.x, wl.w, sx=wl.scale_inv_x, sw=wl.scale_inv_w)
+    run = KsplitRun(wl)
+    try:
+        if op == "rs":
+            run.rs()
+            got = np.concatenate([host_f64(y) for y in run.yb], 0)
+        else:
+            run.ar(chunks)
+            got = host_f64(run.y)
+        assert_close(got, ref, "e4m3")
+    finally:
+        run.close()
+
+
+@pytest.mark.slow
+def test_fp8_rs_tp8_down_projection_sampled_parity():
+    """The GEMM+RS workload shape (tp=8, 16384 x 8192, K = 28672) in e4m3."""
+    wl = synth.make_ksplit("rs", 8, 16384, 28672, 8192, seed=5, dtype="e4m3")
+    run = KsplitRun(wl)
+    try:
+        run.rs()
+        full = torch.cat(run.yb, 0)
+        tiles = synth.sample_tiles(wl.n, wl.m, 16, SAMPLE_TILES, seed=1000 + wl.seed)
+        ref = oracle.ksplit(wl.x, wl.w, tiles=tiles, sx=wl.scale_inv_x, sw=wl.scale_inv_w)
+        assert_close(gather_tiles(host_f64(full), tiles), ref, "e4m3")
     finally:
         run.close()
