@@ -168,7 +168,14 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      co-resident), 1 sequential (copy to completion, then the
  *                      same GEMM), 2 GEMM only (staging and counters must hold a
  *                      previous call's chunks), 3 producer only (no GEMM; y is
- *                      not written)
+ *                      not written), 4 split: per ring step one chunk copy on a
+ *                      side stream and one GEMM launch over that slot after it
+ *                      (no counters; the multi-launch design of the split
+ *                      all-gather overlap in TransformerEngine PR "Comm+GEMM
+ *                      overlap API updated to support cuBlasMp backend" and the
+ *                      ring decomposition of nvFuser PR "Ring-based
+ *                      decomposition for Allgather+GEMM overlap ATen
+ *                      implementation"), for comparison
  *   "seq_copy_ctas"    CTAs of the copy in sequential mode (0 = all SMs)
  *   "self_rank"        observer rank for the ring order, 0..tp-1
  *   "wait_timeout_ms"  bound of every device-side wait (default 2000)

@@ -89,6 +89,8 @@ struct tpo_ctx {
   uint32_t ar_target = 0;  // AR done-counter value after the latest call
   int ar_chunks = 0;       // row-chunk count of the latest AR call
   cudaStream_t aux = nullptr;
+  cudaStream_t copy = nullptr;             // split mode: chunk copies run here
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_copy[TPO_MAX_TP] = {};
   cudaEvent_t last = nullptr;
   bool has_last = false;
   uint32_t last_dev_err[4] = {0, 0, 0, 0};
@@ -112,7 +114,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
   const E table[] = {
       {"producer_sms", &tpo_ctx::producer_sms, 0, 1024},
       {"gemm_ctas", &tpo_ctx::gemm_ctas, 0, 1 << 20},
-      {"mode", &tpo_ctx::mode, 0, 3},
+      {"mode", &tpo_ctx::mode, 0, 4},
       {"seq_copy_ctas", &tpo_ctx::seq_copy_ctas, 0, 1 << 20},
       {"self_rank", &tpo_ctx::self_rank, 0, TPO_MAX_TP - 1},
       {"wait_timeout_ms", &tpo_ctx::wait_timeout_ms, 1, 600000},
@@ -145,7 +147,13 @@ void destroy_all(tpo_ctx* c) {
   if (c->aux) cudaStreamSynchronize(c->aux);
   if (c->staging) cudaFree(c->staging);
   if (c->words) cudaFree(c->words);
+  if (c->copy) cudaStreamSynchronize(c->copy);
   if (c->last) cudaEventDestroy(c->last);
+  if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+  if (c->ev_join) cudaEventDestroy(c->ev_join);
+  for (cudaEvent_t e : c->ev_copy)
+    if (e) cudaEventDestroy(e);
+  if (c->copy) cudaStreamDestroy(c->copy);
   if (c->aux) cudaStreamDestroy(c->aux);
   delete c;
 }
@@ -158,6 +166,7 @@ void base_params(const tpo_ctx* c, Params& p) {
   p.delay_ns = static_cast<unsigned long long>(c->debug_delay_ns);
   p.skip_slot = static_cast<int>(c->debug_skip_chunk);
   p.last_step = static_cast<int>(c->debug_last_step);
+  p.only_step = -1;
   p.trace_on = static_cast<int>(c->trace);
   p.self_rank = static_cast<int>(c->self_rank);
   p.tp = c->tp;
@@ -378,6 +387,15 @@ tpo_ctx* tpo_ctx_create(int tp, int64_t n, int64_t k, int64_t m, int dtype) {
   e = cudaMalloc(&c->words, sizeof(tpo::DevWords));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->last, cudaEventDisableTiming);
+  if (e == cudaSuccess) {
+    int lo = 0, hi = 0;
+    cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    e = cudaStreamCreateWithPriority(&c->copy, cudaStreamNonBlocking, hi);  // copies first when SMs free up
+  }
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming);
+  for (int r = 0; r < TPO_MAX_TP && e == cudaSuccess; ++r)
+    e = cudaEventCreateWithFlags(&c->ev_copy[r], cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->words, 0, sizeof(tpo::DevWords), c->aux);
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->aux);
   if (e != cudaSuccess) {
@@ -520,6 +538,52 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       p.num_producers = 0;
       p.num_gemm = gemm_grid(c, cg, gemm_want, 0, tiles);
       return launch(c, p, p.num_gemm, false, s);
+    }
+    case 4: {  // split: per ring step a chunk copy, then a GEMM launch over that slot
+      const int P = producer_count(c, cg, tiles);
+      const int G = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, P, tiles / c->tp);
+      cudaError_t e = cudaEventRecord(c->ev_fork, s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(c->copy, c->ev_fork, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "split fork");
+      Params cp = p;  // copies: one producer launch per ring step, arrival order, own chunk last
+      cp.cta_group = 1;
+      cp.num_producers = P;
+      cp.num_gemm = 0;
+      for (int si = 0; si < c->tp; ++si) {
+        const int step = (si + 1) % c->tp;
+        const int slot = static_cast<int>(((c->self_rank - step) % c->tp + c->tp) % c->tp);
+        cp.only_step = step;
+        c->target[slot] += static_cast<uint32_t>(P);  // counters stay consistent for later modes
+        std::memcpy(cp.target, c->target, sizeof(cp.target));
+        st = launch(c, cp, P, false, c->copy);
+        if (st != TPO_OK) return st;
+        e = cudaEventRecord(c->ev_copy[slot], c->copy);
+        if (e != cudaSuccess) return cuda_fail(e, "split copy event");
+      }
+      // GEMMs: the observer's own chunk first (in place), then each slot once copied
+      Params gp = p;
+      gp.gate = 0;
+      gp.num_groups = 1;
+      gp.num_producers = 0;
+      gp.num_gemm = G;
+      const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      for (int step = 0; step < c->tp; ++step) {
+        const int slot = static_cast<int>(((c->self_rank - step) % c->tp + c->tp) % c->tp);
+        gp.self_rank = slot;  // group 0 of a one-group launch is this slot
+        if (step > 0) {
+          if (!encode2d(&gp.mapA[1], c->staging + static_cast<size_t>(slot) * p.chunk_bytes, dt, elem, c->k, rows,
+                        kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B))
+            return fail(TPO_ERR_INVALID_ARG, "tensor map encoding failed");
+          e = cudaStreamWaitEvent(s, c->ev_copy[slot], 0);
+          if (e != cudaSuccess) return cuda_fail(e, "split wait");
+        }
+        st = launch(c, gp, G, false, s);
+        if (st != TPO_OK) return st;
+      }
+      e = cudaEventRecord(c->ev_join, c->copy);  // the staging buffer is complete when the call ends
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, c->ev_join, 0);
+      if (e == cudaSuccess) e = cudaEventRecord(c->last, s);
+      return e == cudaSuccess ? TPO_OK : cuda_fail(e, "split join");
     }
     default: {  // producer only
       const int P = producer_count(c, cg, tiles);

@@ -449,6 +449,7 @@ __device__ void producer_role(const Params& p, uint8_t* smem) {
   for (int si = 0; si < p.tp; ++si) {
     const int step = (si + 1) % p.tp;
     if (p.last_step >= 0 && step > p.last_step) continue;
+    if (p.only_step >= 0 && step != p.only_step) continue;
     const int slot = ((p.self_rank - step) % p.tp + p.tp) % p.tp;
     const uint8_t* src = p.src[slot];
     uint8_t* dst = p.staging + static_cast<long long>(slot) * p.chunk_bytes;

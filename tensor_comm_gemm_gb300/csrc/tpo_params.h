@@ -109,6 +109,7 @@ struct Params {
   int gate;               // 1: wait on chunk counters before loading a slot
   int skip_slot;          // debug: never publish this slot (-1 off)
   int last_step;          // debug: producer stops after this ring step (-1 all)
+  int only_step;          // producer copies this ring step only (-1: every step)
   int trace_on;
   int cta_group;          // 1: single-SM MMA, 2: CTA pairs (cluster of 2) with the 2-SM MMA
 };

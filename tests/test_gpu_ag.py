@@ -92,12 +92,15 @@ def test_overlapped_bit_identical_to_sequential(tp, n, k, m):
     run = AgRun(wl)
     try:
         outs = {}
-        for mode, psms in [(0, 8), (1, 8), (2, 8), (0, 1), (0, 20)]:
+        for mode, psms in [(0, 8), (1, 8), (2, 8), (0, 1), (0, 20), (4, 8), (4, 0), (0, 0)]:
             t.tpo_set_opt(run.ctx, "mode", mode)
             t.tpo_set_opt(run.ctx, "producer_sms", psms)
             run.y.fill_(float("nan"))
             run.run()
             outs[(mode, psms)] = host_bits(run.y)
+            if mode == 4:   # split mode leaves the full gather in the staging buffer too
+                got = staging_view(run.ctx, wl.n * wl.k * 2).cpu().numpy().view(np.uint16).reshape(wl.n, wl.k)
+                assert np.array_equal(got, oracle.gather(wl.x))
         base = outs[(1, 8)]
         for key, v in outs.items():
             assert np.array_equal(v, base), key
