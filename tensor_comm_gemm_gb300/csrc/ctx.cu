@@ -166,7 +166,6 @@ void base_params(const tpo_ctx* c, Params& p) {
   p.delay_ns = static_cast<unsigned long long>(c->debug_delay_ns);
   p.skip_slot = static_cast<int>(c->debug_skip_chunk);
   p.last_step = static_cast<int>(c->debug_last_step);
-  p.only_step = -1;
   p.trace_on = static_cast<int>(c->trace);
   p.self_rank = static_cast<int>(c->self_rank);
   p.tp = c->tp;
@@ -473,7 +472,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   if (cg < 0) return fail(TPO_ERR_UNSUPPORTED, "cta_group=2 needs n/tp a multiple of 256 and placeable CTA pairs");
 
   Params p;
-  std::memset(&p, 0, sizeof(p));
+  tpo::init_params(p);
   base_params(c, p);
   p.op = tpo::OP_AG;
   p.cta_group = cg;
@@ -605,7 +604,7 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   const int cg = choose_cg(c, rows_per_group, op == tpo::OP_AR ? rows_per_group / c->tp : rows_per_group);
   if (cg < 0) return fail(TPO_ERR_UNSUPPORTED, "cta_group=2 needs 256-row tile groups and placeable CTA pairs");
   Params p;
-  std::memset(&p, 0, sizeof(p));
+  tpo::init_params(p);
   base_params(c, p);
   p.op = op;
   p.cta_group = cg;

@@ -155,7 +155,7 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
 
   // ---- launch parameters: overlapped schedule, observer rank 0
   tpo::Params p;
-  std::memset(&p, 0, sizeof(p));
+  tpo::init_params(p);
   const int64_t rows = n / tp;
   const int kel = tpo::BK_BYTES / elem;
   const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -183,8 +183,6 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
   p.kb_per_seg = static_cast<int>(k * elem / tpo::BK_BYTES);
   p.num_segs = 1;
   p.gate = 1;
-  p.skip_slot = -1;
-  p.last_step = -1;
   const int P = kProducers < s->num_sms - 1 ? kProducers : s->num_sms - 1;
   const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
   int G = s->num_sms - P;

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "tpoverlap.h"
 
@@ -113,6 +114,15 @@ struct Params {
   int trace_on;
   int cta_group;          // 1: single-SM MMA, 2: CTA pairs (cluster of 2) with the 2-SM MMA
 };
+
+// Zeroes a launch description and sets every field whose "off" value is not 0.
+inline void init_params(Params& p) {
+  memset(&p, 0, sizeof(p));
+  p.skip_slot = -1;
+  p.last_step = -1;
+  p.only_step = -1;
+  p.cta_group = 1;
+}
 
 // Host-side launch helpers defined next to the kernel (kernels.cu).
 cudaError_t configure_kernel();
