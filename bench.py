@@ -404,6 +404,13 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
         check(ctx)
         rec = {"workload": describe(idx), "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
                "frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / pk, 4), "peak_tflops": pk}
+        if op == "rs":  # the same call with the ranks' partials added in the epilogue
+            for rmode, key in ((1, "epilogue_fp32"), (2, "epilogue_bf16_wire")):
+                t.tpo_set_opt(ctx, "reduce", rmode)
+                rms = mean(time_steps(fn, steps, 2))
+                check(ctx)
+                rec["reduce_" + key + "_ms"] = round(rms, 4)
+            t.tpo_set_opt(ctx, "reduce", 0)
         if op == "ag":
             t.tpo_set_opt(ctx, "mode", 1)
             sms = mean(time_steps(fn, steps, 2))

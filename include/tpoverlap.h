@@ -192,6 +192,17 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      0: plain launch (the grid never exceeds the co-resident
  *                      CTA count either way), e.g. for profilers that reject
  *                      cooperative launches of CTA clusters
+ *   "reduce"           GEMM+RS / GEMM+AR sum of the ranks' partial products:
+ *                      0 (default) chain every rank's K-slice, in ring order,
+ *                      into one fp32 accumulator; 1 compute each rank's partial
+ *                      on its own and add the partials in ring order in the
+ *                      epilogue (fp32); 2 as 1 but round every partial and
+ *                      every running sum to bf16, the arithmetic of a bf16
+ *                      ring reduce-scatter such as the bf16 ring all-reduce in
+ *                      nvFuser PR "Reference implementation for Linear+Allreduce
+ *                      with overlapping".  Modes 1 and 2 give up the
+ *                      double-buffered accumulator (tensor memory holds the
+ *                      partial and the running sum).
  * Read-only keys for tpo_get_opt: "last_producer_ctas", "last_gemm_ctas",
  * "last_cta_group" (launch shape of the latest overlapped AG call),
  * "coop_clusters" (0 once the driver refused a cooperative cluster launch).

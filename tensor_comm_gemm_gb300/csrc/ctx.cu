@@ -80,7 +80,7 @@ struct tpo_ctx {
   // options
   int64_t producer_sms = 0, gemm_ctas = 0, mode = 0, seq_copy_ctas = 0, self_rank = 0, wait_timeout_ms = 2000,
           trace = 0, debug_skip_chunk = -1, debug_delay_ns = 0, debug_last_step = -1, cta_group = 0,
-          cooperative = 1;
+          cooperative = 1, reduce = 0;
   // device memory
   uint8_t* staging = nullptr;
   size_t staging_bytes = 0;
@@ -124,6 +124,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
       {"debug_last_step", &tpo_ctx::debug_last_step, -1, TPO_MAX_TP - 1},
       {"cta_group", &tpo_ctx::cta_group, 0, 2},
       {"cooperative", &tpo_ctx::cooperative, 0, 1},
+      {"reduce", &tpo_ctx::reduce, 0, 2},
   };
   for (const E& e : table)
     if (std::strcmp(e.k, key) == 0) {
@@ -139,7 +140,8 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
 
 const char* kOptKeys[] = {"producer_sms",     "gemm_ctas",      "mode",           "seq_copy_ctas",
                           "self_rank",        "wait_timeout_ms", "trace",          "debug_skip_chunk",
-                          "debug_delay_ns",   "debug_last_step", "cta_group",      "cooperative"};
+                          "debug_delay_ns",   "debug_last_step", "cta_group",      "cooperative",
+                          "reduce"};
 
 void destroy_all(tpo_ctx* c) {
   if (!c) return;
@@ -645,6 +647,7 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   p.gate = 0;
   p.scale_x = c->ks_scale_x;
   p.scale_w = c->ks_scale_w;
+  p.reduce_mode = static_cast<int>(c->reduce);
   const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
   tpo_status st = reset_trace(c, s);
   if (st != TPO_OK) return st;

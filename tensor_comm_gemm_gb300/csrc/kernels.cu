@@ -238,6 +238,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
 
 // ------------------------------------------------------------------ clusters (CTA pairs)
 
@@ -595,19 +610,27 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   const uint64_t da0 = smem_desc_sw128(sbase + SMEM_STAGES);
   const uint64_t db0 = smem_desc_sw128(sbase + SMEM_STAGES + A_STAGE_BYTES);
   const uint32_t full0 = B.full0, empty0 = B.empty0, tfull0 = B.tfull0, tempty0 = B.tempty0;
-  uint32_t stage = 0, phase = 0, lt = 0, issued = 0;
+  // Accumulation units: a whole tile (K-slices chained in one accumulator,
+  // double-buffered across tiles), or in the epilogue-reduction modes one
+  // rank's K-slice at a time into buffer 0 while buffer 1 holds the running sum.
+  const bool per_rank = p.reduce_mode != 0;
+  const int units = per_rank ? p.num_segs : 1;
+  const int kpu = per_rank ? p.kb_per_seg : nkb;
+  uint32_t stage = 0, phase = 0, ul = 0, issued = 0;
   bool ok = true;
   unsigned long long cyc_full = 0, cyc_tempty = 0;
-  for (int t = g; t < total_tiles; t += G, ++lt) {
-    const uint32_t acc = lt & 1u;
-    const uint32_t te = tempty0 + 8u * acc, tpar = ((lt >> 1) & 1u) ^ 1u;
+  for (int t = g; t < total_tiles && ok; t += G)
+   for (int u = 0; u < units; ++u, ++ul) {
+    const uint32_t acc = per_rank ? 0u : (ul & 1u);
+    const uint32_t te = tempty0 + 8u * acc;
+    const uint32_t tpar = (per_rank ? (ul & 1u) : ((ul >> 1) & 1u)) ^ 1u;
     if (!mbar_test(te, tpar) && !mbar_wait_timed(p, te, tpar, SITE_TMEM_EMPTY, true, &cyc_tempty)) {
       ok = false;
       break;
     }
     tc_fence_after();
     const uint32_t d = tmem + acc * BN;
-    for (int i = 0; i < nkb; ++i) {
+    for (int i = 0; i < kpu; ++i) {
       const uint32_t fb = full0 + 8u * stage;
       if (!mbar_test(fb, phase) && !mbar_wait_timed(p, fb, phase, SITE_FULL, true, &cyc_full)) {
         ok = false;
@@ -629,7 +652,7 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
     }
     if (!ok) break;
     mma_commit_cg<CG>(tfull0 + 8u * acc);  // accumulator ready for the epilogue(s)
-  }
+   }
   if (!ok) {  // every MMA issued so far must complete before tensor memory is freed
     mma_commit_local_cg<CG>(B.drain);
     mbar_wait(p, B.drain, 0u, SITE_DRAIN, false);
@@ -660,58 +683,107 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
   const uint32_t ebase = smem_u32(smem + SMEM_EPI + (warp - 2) * 2 * EPI_BUF_BYTES);
   const float scale = p.fp8 ? (__ldg(p.scale_x) * __ldg(p.scale_w)) : 1.0f;
   const int row_off = BM * static_cast<int>(rank);
-  uint32_t lt = 0, nst = 0;
+  const int rmode = p.reduce_mode;
+  const int units = rmode ? p.num_segs : 1;
+  uint32_t ul = 0, nst = 0;
   unsigned long long cyc_tfull = 0;
-  for (int t = g; t < total_tiles; t += G, ++lt) {
+  bool ok_all = true;
+  for (int t = g; t < total_tiles && ok_all; t += G) {
     const Tile T = tile_at<PP::TILE_M>(p, t);
-    const uint32_t acc = lt & 1u;
-    const uint32_t bar = B.tfull0 + 8u * acc, par = (lt >> 1) & 1u;
-    int ok = (lane == 0) ? (mbar_wait_timed(p, bar, par, SITE_TMEM_FULL, true, &cyc_tfull) ? 1 : 0) : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) break;
-    mbar_wait(p, bar, par, SITE_TMEM_FULL, false);  // already complete: gives every lane its ordering
-    tc_fence_after();
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+    for (int u = 0; u < units; ++u, ++ul) {
+      const uint32_t acc = rmode ? 0u : (ul & 1u);
+      const uint32_t bar = B.tfull0 + 8u * acc, par = rmode ? (ul & 1u) : ((ul >> 1) & 1u);
+      int ok = (lane == 0) ? (mbar_wait_timed(p, bar, par, SITE_TMEM_FULL, true, &cyc_tfull) ? 1 : 0) : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        ok_all = false;
+        break;
+      }
+      mbar_wait(p, bar, par, SITE_TMEM_FULL, false);  // already complete: gives every lane its ordering
+      tc_fence_after();
+      const bool last = (u == units - 1);
+      const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
+      const uint32_t taddr = tmem + lanes + acc * BN;
+      const uint32_t raddr = tmem + lanes + BN;  // running sum (epilogue-reduction modes)
 #pragma unroll 1
-    for (int c = 0; c < BN / EPI_COLS; ++c, ++nst) {
-      uint32_t r[32];
-      tmem_ld32(taddr + c * EPI_COLS, r);
-      tmem_wait_ld();
-      if (c == BN / EPI_COLS - 1) {  // accumulator fully read: hand it back to the MMA issuer
-        tc_fence_before();
+      for (int c = 0; c < BN / EPI_COLS; ++c) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c * EPI_COLS, r);
+        tmem_wait_ld();
+        float out_scale = scale;
+        if (rmode) {
+          // this rank's partial, added to the running sum in ring order
+          uint32_t q[32];
+          if (u > 0) {
+            tmem_ld32(raddr + c * EPI_COLS, q);
+            tmem_wait_ld();
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float part = __uint_as_float(r[j]);
+            float v;
+            if (rmode == 2) {  // bf16 on the wire: the partial and every running sum are rounded
+              part = round_bf16(part * scale);
+              v = (u > 0) ? round_bf16(__uint_as_float(q[j]) + part) : part;
+            } else {
+              v = (u > 0) ? __uint_as_float(q[j]) + part : part;
+            }
+            r[j] = __float_as_uint(v);
+          }
+          if (rmode == 2) out_scale = 1.0f;
+          if (!last) {
+            tmem_st32(raddr + c * EPI_COLS, r);
+            if (c == BN / EPI_COLS - 1) {  // partial consumed, running sum written: release buffer 0
+              tmem_wait_st();
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) {
+                if constexpr (CG == 1)
+                  mbar_arrive(B.tempty0 + 8u * acc);
+                else
+                  mbar_arrive_cluster(map_to_rank(B.tempty0 + 8u * acc, 0));
+              }
+            }
+            continue;
+          }
+        }
+        if (c == BN / EPI_COLS - 1) {  // accumulator fully read: hand it back to the MMA issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if constexpr (CG == 1)
+              mbar_arrive(B.tempty0 + 8u * acc);
+            else
+              mbar_arrive_cluster(map_to_rank(B.tempty0 + 8u * acc, 0));
+          }
+        }
+        uint32_t packed[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * out_scale,
+                                                         __uint_as_float(r[2 * j + 1]) * out_scale);
+          packed[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        const uint32_t buf = ebase + (nst & 1u) * EPI_BUF_BYTES;
+        ++nst;
+        if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer two boxes ago has read it
+        __syncwarp();
+        // row `lane` of a 32 x 64-byte box in the 64-byte swizzle layout the
+        // output tensor map expects (16-byte chunk index XOR (row / 2) % 4)
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const uint32_t addr = buf + lane * 64 + (static_cast<uint32_t>(ch ^ ((lane >> 1) & 3)) << 4);
+          st_shared_v4(addr, packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
+        }
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (CG == 1)
-            mbar_arrive(B.tempty0 + 8u * acc);
-          else
-            mbar_arrive_cluster(map_to_rank(B.tempty0 + 8u * acc, 0));
+          tma_store_2d(&p.mapY[T.y_map], buf, T.col + c * EPI_COLS, T.y_row + row_off + quad * 32);
+          bulk_commit();
         }
       }
-      uint32_t packed[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const __nv_bfloat162 h =
-            __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * scale, __uint_as_float(r[2 * j + 1]) * scale);
-        packed[j] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      const uint32_t buf = ebase + (nst & 1u) * EPI_BUF_BYTES;
-      if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer two boxes ago has read it
-      __syncwarp();
-      // row `lane` of a 32 x 64-byte box in the 64-byte swizzle layout the
-      // output tensor map expects (16-byte chunk index XOR (row / 2) % 4)
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const uint32_t addr = buf + lane * 64 + (static_cast<uint32_t>(ch ^ ((lane >> 1) & 3)) << 4);
-        st_shared_v4(addr, packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(&p.mapY[T.y_map], buf, T.col + c * EPI_COLS, T.y_row + row_off + quad * 32);
-        bulk_commit();
-      }
     }
-    if (p.op == OP_AR && lane == 0) {  // this warp's rows of the tile are in memory: count them
+    if (ok_all && p.op == OP_AR && lane == 0) {  // this warp's rows of the tile are in memory: count them
       bulk_wait<0>();
       fence_proxy_async_global();
       const uint32_t old = atom_add_release(&p.words->ar_done[T.group], 1u);

@@ -111,6 +111,9 @@ struct Params {
   int skip_slot;          // debug: never publish this slot (-1 off)
   int last_step;          // debug: producer stops after this ring step (-1 all)
   int only_step;          // producer copies this ring step only (-1: every step)
+  int reduce_mode;        // RS/AR: 0 chain the ranks' K-slices in one accumulator, 1 add per-rank
+                          // partials in the epilogue (fp32), 2 as 1 with bf16 rounding of every
+                          // partial and running sum (a bf16 ring's wire format)
   int trace_on;
   int cta_group;          // 1: single-SM MMA, 2: CTA pairs (cluster of 2) with the 2-SM MMA
 };

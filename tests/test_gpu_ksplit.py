@@ -200,3 +200,44 @@ def test_fp8_rs_tp8_down_projection_sampled_parity():
         assert_close(gather_tiles(host_f64(full), tiles), ref, "e4m3")
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("op,tp,n,k,m,chunks,dtype", [("rs", 8, 2048, 2048, 512, 1, "bf16"),
+                                                      ("rs", 3, 768, 384, 512, 1, "bf16"),
+                                                      ("ar", 2, 2048, 1024, 512, 4, "bf16"),
+                                                      ("rs", 4, 1024, 1024, 512, 1, "e4m3")])
+def test_epilogue_reduction_modes(op, tp, n, k, m, chunks, dtype):
+    """Per-rank partials added in the epilogue: in fp32 (reduce=1) the result is
+    an fp32 ring-order sum like the chained accumulator; with bf16 on the wire
+    (reduce=2) every partial and running sum is rounded, so its error against
+    the exact sum is visibly larger, yet within the tolerance."""
+    wl = synth.make_ksplit(op, tp, n, k, m, seed=100 + tp, n_row_chunks=chunks, dtype=dtype,
+                           sigma=k ** -0.25)
+    ref = oracle.ksplit(wl.x, wl.w, sx=wl.scale_inv_x, sw=wl.scale_inv_w)
+    run = KsplitRun(wl)
+    errs = {}
+    try:
+        for mode in (0, 1, 2):
+            t.tpo_set_opt(run.ctx, "reduce", mode)
+            for cg in (1, 2):
+                t.tpo_set_opt(run.ctx, "cta_group", cg)
+                try:
+                    if op == "rs":
+                        for y in run.yb:
+                            y.fill_(float("nan"))
+                        run.rs()
+                        got = np.concatenate([host_f64(y) for y in run.yb], 0)
+                    else:
+                        run.y.fill_(float("nan"))
+                        run.ar(chunks)
+                        got = host_f64(run.y)
+                except t.TpoError as e:
+                    assert cg == 2 and e.status == 2      # shape served by single-SM tiles only
+                    continue
+                errs[(mode, cg)] = assert_close(got, ref, dtype)
+        if tp >= 4:
+            e0 = min(v for (md, _), v in errs.items() if md == 0)
+            e2 = min(v for (md, _), v in errs.items() if md == 2)
+            assert e2 > 1.3 * e0, (e0, e2)
+    finally:
+        run.close()
