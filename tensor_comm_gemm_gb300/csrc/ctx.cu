@@ -501,6 +501,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   p.kb_per_seg = static_cast<int>(c->k * elem / tpo::BK_BYTES);
   p.num_segs = 1;
   p.gate = 1;
+  p.kps = (cg == 2 && p.kb_per_seg % 2 == 0) ? 2 : 1;  // pairs: two K blocks per stage when they divide
   const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
 
   tpo_status st = reset_trace(c, s);
@@ -648,6 +649,8 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   p.scale_x = c->ks_scale_x;
   p.scale_w = c->ks_scale_w;
   p.reduce_mode = static_cast<int>(c->reduce);
+  // pairs: two K blocks per stage when every accumulation unit has an even count
+  p.kps = (cg == 2 && (p.reduce_mode ? p.kb_per_seg : p.num_segs * p.kb_per_seg) % 2 == 0) ? 2 : 1;
   const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
   tpo_status st = reset_trace(c, s);
   if (st != TPO_OK) return st;

@@ -524,7 +524,10 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
   const uint32_t full0 = B.full0, empty0 = B.empty0;
   const uint32_t full0_leader = (CG == 2) ? map_to_rank(full0, 0) : full0;
   const int a_off = BM * static_cast<int>(rank), b_off = PP::B_ROWS * static_cast<int>(rank);
-  uint32_t ready = 0, stage = 0, phase = 0, issued = 0;
+  const uint32_t kps = static_cast<uint32_t>(p.kps);
+  const uint32_t stage_bytes = kps * PP::STAGE_BYTES;
+  const uint32_t nstages = STAGE_AREA / stage_bytes;
+  uint32_t ready = 0, stage = 0, phase = 0, blk = 0, armed = 0;
   bool ok = true;
   unsigned long long cyc_empty = 0;
   for (int t = g; t < total_tiles && ok; t += G) {
@@ -540,44 +543,50 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
     int kk = 0;
     const int a_row = T.a_row + a_off, b_row = T.col + b_off;
     for (int i = 0; i < nkb; ++i) {
-      const uint32_t eb = empty0 + 8u * stage;
-      if (!mbar_test(eb, phase ^ 1u) && !mbar_wait_timed(p, eb, phase ^ 1u, SITE_EMPTY, true, &cyc_empty)) {
-        ok = false;
-        break;
+      const uint32_t sbase_stage = sbase + SMEM_STAGES + stage * stage_bytes;
+      if (blk == 0) {  // a new stage: wait until the MMAs released it, then arm its barrier
+        const uint32_t eb = empty0 + 8u * stage;
+        if (!mbar_test(eb, phase ^ 1u) && !mbar_wait_timed(p, eb, phase ^ 1u, SITE_EMPTY, true, &cyc_empty)) {
+          ok = false;
+          break;
+        }
+        if (CG == 1 || rank == 0) mbar_expect_tx(full0 + 8u * stage, CG * stage_bytes);
+        ++armed;
       }
       const CUtensorMap* ma = reinterpret_cast<const CUtensorMap*>(mapA0 + kMap * static_cast<uint64_t>(r));
       const CUtensorMap* mb = reinterpret_cast<const CUtensorMap*>(mapB0 + kMap * static_cast<uint64_t>(AG ? 0 : r));
-      const uint32_t sa = sbase + SMEM_STAGES + stage * PP::STAGE_BYTES;
+      const uint32_t sa = sbase_stage + blk * A_STAGE_BYTES;
+      const uint32_t sb = sbase_stage + kps * A_STAGE_BYTES + blk * PP::B_STAGE_BYTES;
       const int kx = kk * kelems;
       if constexpr (CG == 1) {
         const uint32_t fb = full0 + 8u * stage;
-        mbar_expect_tx(fb, PP::STAGE_BYTES);
         tma_load_2d(sa, ma, fb, kx, a_row);
-        tma_load_2d(sa + A_STAGE_BYTES, mb, fb, kx, b_row);
+        tma_load_2d(sb, mb, fb, kx, b_row);
       } else {
         // both halves complete on the even CTA's barrier, which expects the pair's bytes
-        if (rank == 0) mbar_expect_tx(full0 + 8u * stage, 2 * PP::STAGE_BYTES);
         const uint32_t fl = full0_leader + 8u * stage;
         tma_load_2d_pair(sa, ma, fl, kx, a_row);
-        tma_load_2d_pair(sa + A_STAGE_BYTES, mb, fl, kx, b_row);
+        tma_load_2d_pair(sb, mb, fl, kx, b_row);
       }
-      ++issued;
       if (++kk == kb_per_seg) {  // next K segment: the next rank in ring order
         kk = 0;
         if (!AG && ++r == tp) r = 0;
       }
-      if (++stage == static_cast<uint32_t>(PP::STAGES)) {
-        stage = 0;
-        phase ^= 1u;
+      if (++blk == kps) {
+        blk = 0;
+        if (++stage == nstages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
   }
   if (!ok) {  // loads already issued must land before the CTA releases its shared memory
     if (CG == 1 || rank == 0) {
-      const uint32_t first = issued > static_cast<uint32_t>(PP::STAGES) ? issued - PP::STAGES : 0u;
-      for (uint32_t j = first; j < issued; ++j)
-        mbar_wait(p, full0 + 8u * (j % PP::STAGES), (j / PP::STAGES) & 1u, SITE_DRAIN, false);
-    } else if (issued > 0) {
+      const uint32_t first = armed > nstages ? armed - nstages : 0u;
+      for (uint32_t j = first; j < armed; ++j)
+        mbar_wait(p, full0 + 8u * (j % nstages), (j / nstages) & 1u, SITE_DRAIN, false);
+    } else if (armed > 0) {
       // the odd CTA's loads signal the even CTA's barrier: give them time to land
       const unsigned long long t0 = gtime();
       while (gtime() - t0 < 200000ull) __nanosleep(1000);
@@ -606,9 +615,13 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
                          int total_tiles, int nkb, bool trace) {
   using PP = Pipe<CG>;
   constexpr uint32_t idesc = make_idesc(FP8, PP::TILE_M);
-  constexpr uint64_t kStageDesc = static_cast<uint64_t>(PP::STAGE_BYTES >> 4);  // stage step in the address field
+  const uint32_t kps = static_cast<uint32_t>(p.kps);
+  const uint32_t stage_bytes = kps * PP::STAGE_BYTES;
+  const uint32_t nstages = STAGE_AREA / stage_bytes;
+  const uint64_t kStageDesc = static_cast<uint64_t>(stage_bytes >> 4);  // stage step in the address field
+  constexpr uint64_t kBlkA = static_cast<uint64_t>(A_STAGE_BYTES >> 4), kBlkB = static_cast<uint64_t>(PP::B_STAGE_BYTES >> 4);
   const uint64_t da0 = smem_desc_sw128(sbase + SMEM_STAGES);
-  const uint64_t db0 = smem_desc_sw128(sbase + SMEM_STAGES + A_STAGE_BYTES);
+  const uint64_t db0 = smem_desc_sw128(sbase + SMEM_STAGES + kps * A_STAGE_BYTES);
   const uint32_t full0 = B.full0, empty0 = B.empty0, tfull0 = B.tfull0, tempty0 = B.tempty0;
   // Accumulation units: a whole tile (K-slices chained in one accumulator,
   // double-buffered across tiles), or in the epilogue-reduction modes one
@@ -616,7 +629,7 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   const bool per_rank = p.reduce_mode != 0;
   const int units = per_rank ? p.num_segs : 1;
   const int kpu = per_rank ? p.kb_per_seg : nkb;
-  uint32_t stage = 0, phase = 0, ul = 0, issued = 0;
+  uint32_t stage = 0, phase = 0, blk = 0, ul = 0, issued = 0;
   bool ok = true;
   unsigned long long cyc_full = 0, cyc_tempty = 0;
   for (int t = g; t < total_tiles && ok; t += G)
@@ -631,23 +644,28 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
     tc_fence_after();
     const uint32_t d = tmem + acc * BN;
     for (int i = 0; i < kpu; ++i) {
-      const uint32_t fb = full0 + 8u * stage;
-      if (!mbar_test(fb, phase) && !mbar_wait_timed(p, fb, phase, SITE_FULL, true, &cyc_full)) {
-        ok = false;
-        break;
+      if (blk == 0) {
+        const uint32_t fb = full0 + 8u * stage;
+        if (!mbar_test(fb, phase) && !mbar_wait_timed(p, fb, phase, SITE_FULL, true, &cyc_full)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
       }
-      tc_fence_after();
-      const uint64_t da = da0 + kStageDesc * stage, db = db0 + kStageDesc * stage;
+      const uint64_t da = da0 + kStageDesc * stage + kBlkA * blk, db = db0 + kStageDesc * stage + kBlkB * blk;
       // four MMAs of K = 32 bytes each cover the 128-byte K block
       mma_cg<CG>(FP8, d, da, db, idesc, i > 0 ? 1u : 0u);
       mma_cg<CG>(FP8, d, da + 2u, db + 2u, idesc, 1u);
       mma_cg<CG>(FP8, d, da + 4u, db + 4u, idesc, 1u);
       mma_cg<CG>(FP8, d, da + 6u, db + 6u, idesc, 1u);
-      mma_commit_cg<CG>(empty0 + 8u * stage);  // frees the stage (in both CTAs) once read
       ++issued;
-      if (++stage == static_cast<uint32_t>(PP::STAGES)) {
-        stage = 0;
-        phase ^= 1u;
+      if (++blk == kps) {
+        blk = 0;
+        mma_commit_cg<CG>(empty0 + 8u * stage);  // frees the stage (in both CTAs) once read
+        if (++stage == nstages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
     if (!ok) break;
@@ -810,7 +828,7 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
   B.drain = sbase + SMEM_BARS + 8u * BAR_DRAIN;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_TMEM_SLOT);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < PP::STAGES; ++s) {
+    for (int s = 0; s < MAX_STAGES; ++s) {
       mbar_init(B.full0 + 8u * s, 1);
       mbar_init(B.empty0 + 8u * s, 1);
     }

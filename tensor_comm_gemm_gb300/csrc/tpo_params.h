@@ -23,12 +23,14 @@ constexpr int A_STAGE_BYTES = BM * BK_BYTES;  // 16 KiB
 constexpr int STAGE_AREA = 196608;            // 192 KiB of pipeline stages
 template <int CG>
 struct Pipe {
-  static constexpr int B_ROWS = BN / CG;                  // B rows one CTA loads per stage
-  static constexpr int B_STAGE_BYTES = B_ROWS * BK_BYTES;  // 32 or 16 KiB
-  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-  static constexpr int STAGES = STAGE_AREA / STAGE_BYTES;  // 4 or 6
+  static constexpr int B_ROWS = BN / CG;                  // B rows one CTA loads per K block
+  static constexpr int B_STAGE_BYTES = B_ROWS * BK_BYTES;  // 32 or 16 KiB per K block
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;  // one K block of A and B
+  static constexpr int STAGES = STAGE_AREA / STAGE_BYTES;  // 4 or 6 stages of one K block
   static constexpr int TILE_M = BM * CG;                  // output rows of one tile
 };
+// A stage may hold kps K blocks (A blocks first, then B blocks); the stage
+// count follows: STAGE_AREA / (kps * Pipe<CG>::STAGE_BYTES).
 constexpr int MAX_STAGES = 6;
 constexpr int NUM_THREADS = 192;              // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int EPI_WARPS = 4;
@@ -111,6 +113,7 @@ struct Params {
   int skip_slot;          // debug: never publish this slot (-1 off)
   int last_step;          // debug: producer stops after this ring step (-1 all)
   int only_step;          // producer copies this ring step only (-1: every step)
+  int kps;                // 128-byte K blocks per pipeline stage (1, or 2 for CTA pairs)
   int reduce_mode;        // RS/AR: 0 chain the ranks' K-slices in one accumulator, 1 add per-rank
                           // partials in the epilogue (fp32), 2 as 1 with bf16 rounding of every
                           // partial and running sum (a bf16 ring's wire format)
@@ -125,6 +128,7 @@ inline void init_params(Params& p) {
   p.last_step = -1;
   p.only_step = -1;
   p.cta_group = 1;
+  p.kps = 1;
 }
 
 // Host-side launch helpers defined next to the kernel (kernels.cu).
