@@ -24,7 +24,7 @@ def ref_ag(wl):
 
 # (tp, n, k, m): several tiles per slot, ragged K (not a multiple of 256), tp=1 and tp=16
 SHAPES = [(2, 256, 256, 256), (3, 768, 192, 768), (1, 128, 64, 256), (5, 1280, 320, 512), (16, 2048, 64, 256),
-          (4, 1024, 1088, 1024)]
+          (4, 1024, 1088, 1024), (16, 4096, 128, 256), (2, 512, 64, 2048)]
 
 
 @pytest.mark.parametrize("tp,n,k,m", SHAPES)

@@ -19,7 +19,8 @@ def _built(cuda_ok):
 
 
 # (tp, n, k, m): ragged per-rank K (k/tp not a multiple of 128), tp = 1, asymmetric shapes
-RS_SHAPES = [(2, 256, 256, 256), (3, 768, 192, 512), (1, 256, 64, 256), (4, 1024, 1280, 768), (8, 2048, 512, 256)]
+RS_SHAPES = [(2, 256, 256, 256), (3, 768, 192, 512), (1, 256, 64, 256), (4, 1024, 1280, 768), (8, 2048, 512, 256),
+             (16, 4096, 1024, 256), (16, 2048, 2048, 512)]
 
 
 @pytest.mark.parametrize("tp,n,k,m", RS_SHAPES)
@@ -41,7 +42,8 @@ def test_rs_full_parity(tp, n, k, m):
 
 
 @pytest.mark.parametrize("tp,n,k,m,chunks", [(2, 1024, 256, 256, 4), (3, 2304, 384, 512, 2), (1, 512, 128, 512, 4),
-                                             (2, 512, 1024, 256, 1), (2, 2048, 512, 512, 2)])
+                                             (2, 512, 1024, 256, 1), (2, 2048, 512, 512, 2),
+                                             (2, 16384, 128, 256, 64), (4, 8192, 256, 256, 16)])
 def test_ar_full_parity_and_done_counters(tp, n, k, m, chunks):
     wl = synth.make_ksplit("ar", tp, n, k, m, seed=30 + tp, dist="uniform", n_row_chunks=chunks)
     ref = oracle.ksplit(wl.x, wl.w)
