@@ -41,11 +41,12 @@ _lib = None
 
 
 def lib(path: Optional[str] = None):
-    """Load libtpoverlap.so (raises if it is not built)."""
+    """Load libtpoverlap.so (raises if it is not built).  The environment
+    variable TPO_LIBRARY names another build of the library to load instead."""
     global _lib
     if _lib is not None:
         return _lib
-    path = path or _build.LIB
+    path = path or os.environ.get("TPO_LIBRARY") or _build.LIB
     if not os.path.exists(path):
         raise ImportError("libtpoverlap.so not built (run tensor_comm_gemm_gb300.build.build()): " + path)
     L = ctypes.CDLL(path)
