@@ -97,10 +97,15 @@ struct tpo_ctx {
   const float* ks_scale_x = nullptr;  // e4m3 RS/AR scale_inv pointers (tpo_set_fp8_scales)
   const float* ks_scale_w = nullptr;
   int64_t last_producers = 0, last_gemm_ctas = 0, last_cta_group = 0;  // launch shape of the latest call
-  // tensor-map cache: the Params of the latest call of each op, keyed by pointers
-  Params cache[3];
-  const void* cache_key[3][3 * TPO_MAX_TP + 2];
-  bool cache_valid[3] = {false, false, false};
+  // tensor-map cache: the maps of the latest kCacheWays pointer sets of each op
+  static constexpr int kCacheWays = 4;
+  struct MapSet {
+    CUtensorMap a[TPO_MAX_TP], b[TPO_MAX_TP], y[TPO_MAX_TP];
+  };
+  MapSet cache[3][kCacheWays];
+  const void* cache_key[3][kCacheWays][3 * TPO_MAX_TP + 2];
+  bool cache_valid[3][kCacheWays] = {};
+  int cache_next[3] = {0, 0, 0};
 };
 
 namespace {
@@ -202,21 +207,29 @@ tpo_status launch(tpo_ctx* c, const Params& p, int grid, bool coop, cudaStream_t
 }
 
 bool cache_lookup(tpo_ctx* c, int op, const void* const* key, int nkey, Params& p) {
-  if (!c->cache_valid[op]) return false;
-  for (int i = 0; i < nkey; ++i)
-    if (c->cache_key[op][i] != key[i]) return false;
-  std::memcpy(p.mapA, c->cache[op].mapA, sizeof(p.mapA));
-  std::memcpy(p.mapB, c->cache[op].mapB, sizeof(p.mapB));
-  std::memcpy(p.mapY, c->cache[op].mapY, sizeof(p.mapY));
-  return true;
+  for (int way = 0; way < tpo_ctx::kCacheWays; ++way) {
+    if (!c->cache_valid[op][way]) continue;
+    bool hit = true;
+    for (int i = 0; i < nkey && hit; ++i) hit = c->cache_key[op][way][i] == key[i];
+    if (!hit) continue;
+    const tpo_ctx::MapSet& m = c->cache[op][way];
+    std::memcpy(p.mapA, m.a, sizeof(p.mapA));
+    std::memcpy(p.mapB, m.b, sizeof(p.mapB));
+    std::memcpy(p.mapY, m.y, sizeof(p.mapY));
+    return true;
+  }
+  return false;
 }
 
 void cache_store(tpo_ctx* c, int op, const void* const* key, int nkey, const Params& p) {
-  for (int i = 0; i < nkey; ++i) c->cache_key[op][i] = key[i];
-  std::memcpy(c->cache[op].mapA, p.mapA, sizeof(p.mapA));
-  std::memcpy(c->cache[op].mapB, p.mapB, sizeof(p.mapB));
-  std::memcpy(c->cache[op].mapY, p.mapY, sizeof(p.mapY));
-  c->cache_valid[op] = true;
+  const int way = c->cache_next[op];
+  c->cache_next[op] = (way + 1) % tpo_ctx::kCacheWays;
+  for (int i = 0; i < nkey; ++i) c->cache_key[op][way][i] = key[i];
+  tpo_ctx::MapSet& m = c->cache[op][way];
+  std::memcpy(m.a, p.mapA, sizeof(p.mapA));
+  std::memcpy(m.b, p.mapB, sizeof(p.mapB));
+  std::memcpy(m.y, p.mapY, sizeof(p.mapY));
+  c->cache_valid[op][way] = true;
 }
 
 // Advance the expected counter value of every slot this call's producer is
