@@ -222,9 +222,14 @@ def gpu_arm(args, rank, world, local_rank, dist):
 
     detail_steps = min(200, max(5, args.steps // 2))
     seq = mode_times(1, detail_steps, 3)
-    gemm_only = mode_times(2, detail_steps, 3)
     prod_only = mode_times(3, detail_steps, 3)
     split = mode_times(4, detail_steps, 3)
+    # exposed producer time: overlapped and GEMM-only calls in interleaved blocks of
+    # equal length, so that both see the same clock and power state
+    ov_blocks, gemm_only = [], []
+    for _ in range(4):
+        ov_blocks += mode_times(0, detail_steps // 2 or 1, 2)
+        gemm_only += mode_times(2, detail_steps // 2 or 1, 2)
     t.tpo_set_opt(ctx, "mode", 0)
 
     # ---- the timed region: K overlapped steps, barrier + synchronize on both sides
@@ -371,7 +376,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
             "producer_only_ms": round(prod_ms, 5),
             "producer_only_gbs": round(producer_bytes / (prod_ms * 1e-3) / 1e9, 1),
             "producer_frac_of_hbm": round(producer_bytes / (prod_ms * 1e-3) / 1e9 / hbm, 4),
-            "exposed_producer_frac": round((mean(step_ms) - gemm_ms) / gemm_ms, 4),
+            "exposed_producer_frac": round((mean(ov_blocks) - gemm_ms) / gemm_ms, 4),
+            "exposed_note": "overlapped vs GEMM-only (staging prefilled) in interleaved blocks",
             "split_ms": round(mean(split), 5),
             "split_tflops": round(flops / (mean(split) * 1e-3) / 1e12, 2),
         },
