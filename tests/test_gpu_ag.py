@@ -36,13 +36,16 @@ def test_ag_full_parity_every_observer(tp, n, k, m):
         first = None
         for self_rank in sorted({0, tp - 1, tp // 2}):
             t.tpo_set_opt(run.ctx, "self_rank", self_rank)
-            run.y.fill_(float("nan"))
-            run.run()
-            assert_close(host_f64(run.y), ref)
-            bits = host_bits(run.y)
-            if first is None:
-                first = bits
-            assert np.array_equal(bits, first), "result depends on the observer rank"
+            for mode in (0, 1, 4):      # overlapped, sequential, split
+                t.tpo_set_opt(run.ctx, "mode", mode)
+                run.y.fill_(float("nan"))
+                run.run()
+                if mode == 0:
+                    assert_close(host_f64(run.y), ref)
+                bits = host_bits(run.y)
+                if first is None:
+                    first = bits
+                assert np.array_equal(bits, first), ("result depends on the observer rank or mode", self_rank, mode)
     finally:
         run.close()
 

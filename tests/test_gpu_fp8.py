@@ -17,7 +17,8 @@ def _built(cuda_ok):
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("tp,n,k,m", [(2, 256, 256, 512), (8, 2048, 384, 768), (3, 768, 128, 256)])
+@pytest.mark.parametrize("tp,n,k,m", [(2, 256, 256, 512), (8, 2048, 384, 768), (3, 768, 128, 256),
+                                     (4, 1024, 512, 512)])
 def test_fp8_ag_full_parity(tp, n, k, m):
     wl = synth.make_ag(tp, n, k, m, seed=50 + tp, dtype="e4m3")
     ref = oracle.ag(oracle.gather(wl.x), wl.w[0], wl.scale_inv_x, wl.scale_inv_w)
