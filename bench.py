@@ -398,6 +398,17 @@ def gpu_arm(args, rank, world, local_rank, dist):
 def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
     out = {}
     steps = min(40, max(5, args.steps // 2))
+    # the small AG workload: latency-bound (2 output tiles), reported in microseconds per call
+    wl = synth.workload(0)
+    xs = [to_dev(x) for x in wl.x]
+    w = to_dev(wl.w[0])
+    y = torch.empty((wl.n, wl.m), dtype=torch.bfloat16, device=dev)
+    ctx = t.tpo_ctx_create(wl.tp, wl.n, wl.k, wl.m, t.TPO_BF16)
+    ms = mean(time_steps(lambda i=0: t.tpo_ag_gemm(ctx, xs, w, y), 200, 10))
+    check(ctx)
+    out[wl.name] = {"workload": describe(0), "us_per_call": round(ms * 1e3, 2),
+                    "tflops": round(synth.flops(0) / (ms * 1e-3) / 1e12, 3)}
+    t.tpo_ctx_destroy(ctx)
     for idx in (2, 3, 4):
         op, dt, tp, n, k, m, ch = synth.WORKLOAD_SHAPES[idx]
         wl = synth.workload(idx)
