@@ -130,7 +130,18 @@ class Clocks:
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None}
+                "power_w_max": max(power) if power else None, "power_limits_w": self.power_limits()}
+
+    def power_limits(self):
+        """The board's enforced and maximum power limits (read only)."""
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", str(self.gpu),
+                                  "--query-gpu=enforced.power.limit,power.max_limit",
+                                  "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
+            enforced, mx = [float(v) for v in out.stdout.strip().split(",")[:2]]
+            return {"enforced": enforced, "max": mx}
+        except (OSError, ValueError, subprocess.TimeoutExpired):
+            return None
 
 
 # ---------------------------------------------------------------------------- aggregation
