@@ -205,7 +205,8 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      partial and the running sum).
  * Read-only keys for tpo_get_opt: "last_producer_ctas", "last_gemm_ctas",
  * "last_cta_group" (launch shape of the latest overlapped AG call),
- * "coop_clusters" (0 once the driver refused a cooperative cluster launch).
+ * "coop_clusters" (0 once the driver refused a cooperative cluster launch),
+ * "tp", "n", "k", "m", "dtype" (the sizes the context was created for).
  * Environment variables TPO_<KEY in upper case> override the defaults at
  * create time.  Unknown keys or out-of-range values: TPO_ERR_INVALID_ARG.
  */

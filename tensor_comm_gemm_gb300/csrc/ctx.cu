@@ -456,6 +456,11 @@ tpo_status tpo_get_opt(tpo_ctx* c, const char* key, int64_t* value) {
   if (std::strcmp(key, "last_gemm_ctas") == 0) return *value = c->last_gemm_ctas, TPO_OK;
   if (std::strcmp(key, "last_cta_group") == 0) return *value = c->last_cta_group, TPO_OK;
   if (std::strcmp(key, "coop_clusters") == 0) return *value = c->coop_clusters ? 1 : 0, TPO_OK;
+  if (std::strcmp(key, "tp") == 0) return *value = c->tp, TPO_OK;
+  if (std::strcmp(key, "n") == 0) return *value = c->n, TPO_OK;
+  if (std::strcmp(key, "k") == 0) return *value = c->k, TPO_OK;
+  if (std::strcmp(key, "m") == 0) return *value = c->m, TPO_OK;
+  if (std::strcmp(key, "dtype") == 0) return *value = c->dtype, TPO_OK;
   int64_t lo, hi;
   int64_t* f = opt_slot(c, key, &lo, &hi);
   if (!f) return fail(TPO_ERR_INVALID_ARG, "unknown option '%s'", key);

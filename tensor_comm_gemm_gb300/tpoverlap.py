@@ -16,6 +16,7 @@ from typing import Optional, Sequence
 from . import build as _build
 
 TPO_BF16, TPO_FP8_E4M3 = 0, 1
+TPO_ERR_INVALID_ARG, TPO_ERR_UNSUPPORTED = 1, 2
 STATUS = {0: "TPO_OK", 1: "TPO_ERR_INVALID_ARG", 2: "TPO_ERR_UNSUPPORTED", 3: "TPO_ERR_CUDA",
           4: "TPO_ERR_TIMEOUT", 5: "TPO_ERR_OOM"}
 TPO_TRACE_START, TPO_TRACE_END, TPO_TRACE_PUBLISH, TPO_TRACE_ACQUIRE = 0, 1, 2, 18
@@ -100,6 +101,36 @@ def _ptr_array(ts: Sequence):
     return (ctypes.c_void_p * len(ts))(*[_ptr(t) for t in ts])
 
 
+def _check_tensor(name, t, shape, elem_bytes):
+    """Torch tensors handed to the C ABI must be dense CUDA tensors of the shape
+    and element size the context expects: a strided view would be read as if it
+    were row-major.  Raw integer pointers pass unchecked to the library's own
+    argument checks.  A mismatch raises TpoError with TPO_ERR_INVALID_ARG."""
+    if t is None or isinstance(t, int):
+        return
+    why = None
+    if not t.is_cuda:
+        why = "must be a CUDA tensor"
+    elif not t.is_contiguous():
+        why = "must be contiguous (row-major)"
+    elif t.element_size() != elem_bytes:
+        why = "has %d-byte elements, expected %d" % (t.element_size(), elem_bytes)
+    elif t.numel() != shape[0] * shape[1]:
+        why = "has %d elements, expected %d x %d" % (t.numel(), shape[0], shape[1])
+    if why:
+        raise TpoError(TPO_ERR_INVALID_ARG, "%s %s" % (name, why))
+
+
+_SIZES = {}      # context handle -> (tp, n, k, m, dtype), filled on first use
+
+
+def _sizes(ctx):
+    sz = _SIZES.get(ctx)
+    if sz is None:
+        sz = _SIZES[ctx] = tuple(tpo_get_opt(ctx, k) for k in ("tp", "n", "k", "m", "dtype"))
+    return sz
+
+
 def _stream(stream) -> int:
     if stream is None:
         import torch
@@ -117,23 +148,51 @@ def tpo_ctx_create(tp: int, n: int, k: int, m: int, dtype: int) -> int:
     h = lib().tpo_ctx_create(tp, n, k, m, dtype)
     if not h:
         raise TpoError(-1, tpo_last_error())
+    _SIZES.pop(h, None)
     return h
 
 
 def tpo_ctx_destroy(ctx: int) -> None:
+    _SIZES.pop(ctx, None)
     _check(lib().tpo_ctx_destroy(ctx))
 
 
 def tpo_ag_gemm(ctx: int, x: Sequence, w, y, scale_inv_x=None, scale_inv_w=None, stream=None) -> None:
+    tp, n, k, m, dt = _sizes(ctx)
+    eb = 1 if dt == TPO_FP8_E4M3 else 2
+    if len(x) != tp:
+        raise TpoError(TPO_ERR_INVALID_ARG, "x must hold tp=%d chunks" % tp)
+    for r, xr in enumerate(x):
+        _check_tensor("x[%d]" % r, xr, (n // tp, k), eb)
+    _check_tensor("w", w, (m, k), eb)
+    _check_tensor("y", y, (n, m), 2)
     _check(lib().tpo_ag_gemm(ctx, _ptr_array(x), _ptr(w), _ptr(y), _ptr(scale_inv_x), _ptr(scale_inv_w),
                              _stream(stream)))
 
 
+def _check_ksplit(ctx, x, w):
+    tp, n, k, m, dt = _sizes(ctx)
+    eb = 1 if dt == TPO_FP8_E4M3 else 2
+    if len(x) != tp or len(w) != tp:
+        raise TpoError(TPO_ERR_INVALID_ARG, "x and w must hold tp=%d slices each" % tp)
+    for r in range(tp):
+        _check_tensor("x[%d]" % r, x[r], (n, k // tp), eb)
+        _check_tensor("w[%d]" % r, w[r], (m, k // tp), eb)
+    return tp, n, m
+
+
 def tpo_gemm_rs(ctx: int, x: Sequence, w: Sequence, y: Sequence, stream=None) -> None:
+    tp, n, m = _check_ksplit(ctx, x, w)
+    if len(y) != tp:
+        raise TpoError(TPO_ERR_INVALID_ARG, "y must hold tp=%d row blocks" % tp)
+    for b, yb in enumerate(y):
+        _check_tensor("y[%d]" % b, yb, (n // tp, m), 2)
     _check(lib().tpo_gemm_rs(ctx, _ptr_array(x), _ptr_array(w), _ptr_array(y), _stream(stream)))
 
 
 def tpo_gemm_ar(ctx: int, x: Sequence, w: Sequence, y, n_row_chunks: int, stream=None) -> None:
+    tp, n, m = _check_ksplit(ctx, x, w)
+    _check_tensor("y", y, (n, m), 2)
     _check(lib().tpo_gemm_ar(ctx, _ptr_array(x), _ptr_array(w), _ptr(y), n_row_chunks, _stream(stream)))
 
 

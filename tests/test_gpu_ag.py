@@ -211,7 +211,8 @@ def test_call_argument_errors():
         with pytest.raises(t.TpoError):
             t.tpo_set_opt(run.ctx, "no_such_option", 1)
         with pytest.raises(t.TpoError) as e:
-            t.tpo_gemm_ar(run.ctx, run.xs, [run.w, run.w], run.y, 3)   # n % (3*tp*128) != 0
+            t.tpo_gemm_ar(run.ctx, [x.data_ptr() for x in run.xs], [run.w.data_ptr()] * 2, run.y,
+                          3)   # n % (3*tp*128) != 0
         assert e.value.status == 2
     finally:
         run.close()
@@ -255,6 +256,29 @@ def test_pair_and_single_sm_variants_agree(tp, n, k, m):
                 bits[(cg, mode)] = host_bits(run.y)
         assert np.array_equal(bits[(1, 0)], bits[(1, 1)]) and np.array_equal(bits[(2, 0)], bits[(2, 1)])
         assert np.array_equal(bits[(1, 0)], bits[(2, 0)])
+    finally:
+        run.close()
+
+
+def test_binding_rejects_mismatched_tensors():
+    """The binding refuses tensors whose layout the library would misread."""
+    wl = synth.make_ag(2, 256, 256, 256, seed=1, dist="uniform")
+    run = AgRun(wl)
+    try:
+        cases = [
+            ([run.xs[0]], run.w, run.y),                                # too few chunks
+            ([run.xs[0].t(), run.xs[1]], run.w, run.y),                 # transposed (strided) chunk
+            (run.xs, run.w.float(), run.y),                             # 4-byte weight elements
+            (run.xs, run.w[:128], run.y),                               # short weight
+            (run.xs, run.w, run.y.cpu()),                               # host output
+        ]
+        for xs, w, y in cases:
+            with pytest.raises(t.TpoError) as e:
+                t.tpo_ag_gemm(run.ctx, xs, w, y)
+            assert e.value.status == t.TPO_ERR_INVALID_ARG
+        assert t.tpo_get_opt(run.ctx, "tp") == 2 and t.tpo_get_opt(run.ctx, "m") == 256
+        run.run()                                                       # the context is unharmed
+        assert_close(host_f64(run.y), ref_ag(wl))
     finally:
         run.close()
 

@@ -103,8 +103,10 @@ def test_ksplit_rejects_fp8_and_bad_shapes():
     ctx = t.tpo_ctx_create(2, 256, 256, 256, t.TPO_FP8_E4M3)
     try:
         x = torch.zeros((256, 128), dtype=torch.uint8, device="cuda")
+        y = torch.zeros((128, 256), dtype=torch.bfloat16, device="cuda")
         with pytest.raises(t.TpoError) as e:       # e4m3 RS/AR needs its scales first
-            t.tpo_gemm_rs(ctx, [x, x], [x, x], [x, x])
+            t.tpo_gemm_rs(ctx, [x, x], [x, x], [y, y])
+        assert "scale" in str(e.value)
         assert e.value.status == 1
         with pytest.raises(t.TpoError) as e:
             t.tpo_set_fp8_scales(ctx, 0, x)
@@ -116,8 +118,8 @@ def test_ksplit_rejects_fp8_and_bad_shapes():
         sc = torch.ones(1, device="cuda")
         t.tpo_set_fp8_scales(ctx, sc, sc)
         x = torch.zeros((512, 64), dtype=torch.uint8, device="cuda")
-        with pytest.raises(t.TpoError) as e:
-            t.tpo_gemm_rs(ctx, [x] * 4, [x] * 4, [x] * 4)
+        with pytest.raises(t.TpoError) as e:        # raw pointers: the library's own shape check
+            t.tpo_gemm_rs(ctx, [x.data_ptr()] * 4, [x.data_ptr()] * 4, [x.data_ptr()] * 4)
         assert e.value.status == 2
     finally:
         t.tpo_ctx_destroy(ctx)
