@@ -348,6 +348,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
         if tj.get("kernel_sha") == kernel_sha():
             traffic = tj.get("ag_tp4_4096", {}).get("bytes_per_launch")
     gemm_ms, seq_ms, prod_ms = mean(gemm_only), mean(seq), mean(prod_only)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     producer_bytes = 2 * (wl.n * wl.k * 2)  # every chunk read once and written once
     result = {
         "metric": METRIC,
@@ -377,7 +378,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_kind if peak_kind == "measured"
-                     else "fallback 1.9 PFLOP/s"},
+                     else "fallback 1.9 PFLOP/s",
+                     "nominal": nominal_peak(achieved, sms, clk.get("sm_max_mhz"), clk.get("sm_mhz_in_kernel"))},
         "clocks": clk,
         "detail": {
             "sequential_ms": round(seq_ms, 5),
@@ -406,6 +408,41 @@ def gpu_arm(args, rank, world, local_rank, dist):
     return result
 
 
+def nominal_peak(achieved, sms, max_mhz, kernel_mhz):
+    """The tensor rate from the hardware's unit count: SMs x 8192 bf16 FLOP per
+    clock per SM (an assumption, the figure ncu gives as peak_sustained), at the
+    maximum SM clock and at the clock measured inside the kernel."""
+    out = {"flop_per_clk_per_sm": 8192, "sms": sms}
+    for key, mhz in (("max_clock", max_mhz), ("kernel_clock", kernel_mhz)):
+        if mhz:
+            pk = sms * 8192 * mhz * 1e6 / 1e12
+            out["peak_at_" + key] = round(pk, 1)
+            out["frac_at_" + key] = round(achieved / pk, 4)
+    return out
+
+
+def cublas_fp8_tflops(torch, dev, size=8192):
+    """Dense e4m3 GEMM rate of the vendor library (torch._scaled_mm, size^3), the
+    measured FP8 counterpart of the bf16 peak; None where the call is missing."""
+    try:
+        a = torch.randn(size, size, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(size, size, device=dev).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=dev)
+        f = lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)  # noqa: E731
+        for _ in range(3):
+            f()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(10):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        return round(2.0 * size ** 3 / (e0.elapsed_time(e1) / 10 * 1e-3) / 1e12, 1)
+    except Exception:  # noqa: BLE001
+        return None
+
+
 def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
     out = {}
     steps = min(40, max(5, args.steps // 2))
@@ -429,6 +466,9 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
                     "us_per_call_python": round(ms_py * 1e3, 2),
                     "tflops": round(synth.flops(0) / (ms * 1e-3) / 1e12, 3)}
     t.tpo_ctx_destroy(ctx)
+    fp8_lib = cublas_fp8_tflops(torch, dev)
+    out["fp8_library_gemm_8192"] = {"tflops": fp8_lib, "note": "torch._scaled_mm e4m3 8192^3 burst on this "
+                                    "box; the FP8 rows' frac_of_peak uses 2 x the measured bf16 peak"}
     for idx in (2, 3, 4):
         op, dt, tp, n, k, m, ch = synth.WORKLOAD_SHAPES[idx]
         wl = synth.workload(idx)
@@ -458,6 +498,8 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
         check(ctx)
         rec = {"workload": describe(idx), "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
                "frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / pk, 4), "peak_tflops": pk}
+        if dt == "e4m3" and fp8_lib:
+            rec["frac_of_library_fp8"] = round(flops / (ms * 1e-3) / 1e12 / fp8_lib, 4)
         if op == "rs":  # the same call with the ranks' partials added in the epilogue
             for rmode, key in ((1, "epilogue_fp32"), (2, "epilogue_bf16_wire")):
                 t.tpo_set_opt(ctx, "reduce", rmode)
@@ -493,6 +535,8 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
                     "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
                     "frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / (peak * FP8_OVER_BF16), 4),
                     "peak_tflops": peak * FP8_OVER_BF16}
+    if fp8_lib:
+        out[wl.name]["frac_of_library_fp8"] = round(flops / (ms * 1e-3) / 1e12 / fp8_lib, 4)
     t.tpo_ctx_destroy(ctx)
     return out
 

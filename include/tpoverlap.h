@@ -204,7 +204,8 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      double-buffered accumulator (tensor memory holds the
  *                      partial and the running sum).
  * Read-only keys for tpo_get_opt: "last_producer_ctas", "last_gemm_ctas",
- * "last_cta_group" (launch shape of the latest overlapped AG call),
+ * "last_cta_group" (shape of the context's latest kernel launch: producer
+ * CTAs, GEMM CTAs, 1 or 2 CTAs per MMA),
  * "coop_clusters" (0 once the driver refused a cooperative cluster launch),
  * "tp", "n", "k", "m", "dtype" (the sizes the context was created for).
  * Environment variables TPO_<KEY in upper case> override the defaults at

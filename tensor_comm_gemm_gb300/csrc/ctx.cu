@@ -96,7 +96,7 @@ struct tpo_ctx {
   uint32_t last_dev_err[4] = {0, 0, 0, 0};
   const float* ks_scale_x = nullptr;  // e4m3 RS/AR scale_inv pointers (tpo_set_fp8_scales)
   const float* ks_scale_w = nullptr;
-  int64_t last_producers = 0, last_gemm_ctas = 0, last_cta_group = 0;  // launch shape of the latest call
+  int64_t last_producers = 0, last_gemm_ctas = 0, last_cta_group = 0;  // shape of the latest kernel launch
   // tensor-map cache: the maps of the latest kCacheWays pointer sets of each op
   static constexpr int kCacheWays = 4;
   struct MapSet {
@@ -189,6 +189,9 @@ tpo_status reset_trace(tpo_ctx* c, cudaStream_t s) {
 }
 
 tpo_status launch(tpo_ctx* c, const Params& p, int grid, bool coop, cudaStream_t s) {
+  c->last_producers = p.num_producers;
+  c->last_gemm_ctas = p.num_gemm;
+  c->last_cta_group = p.cta_group;
   if (coop && (!c->cooperative || (p.cta_group == 2 && !c->coop_clusters))) coop = false;
   cudaError_t e = tpo::launch_fused(p, grid, coop, s);
   if (e != cudaSuccess && coop && p.cta_group == 2) {
@@ -535,9 +538,6 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       advance_targets(c, p, P);
       p.num_producers = P;
       p.num_gemm = G;
-      c->last_producers = P;
-      c->last_gemm_ctas = G;
-      c->last_cta_group = cg;
       return launch(c, p, P + G, true, s);
     }
     case 1: {  // sequential: the copy to completion, then the same GEMM
