@@ -81,9 +81,11 @@ def main(argv=None):
             times.append(a.elapsed_time(b))
         flops = 2.0 * args.n * args.k * args.m
         best = min(times)
-        print("%s tp=%d n=%d k=%d m=%d %s: best of %d calls %.4f ms, %.1f TFLOP/s (cta_group %d)" % (
-            args.op, args.tp, args.n, args.k, args.m, args.dtype, args.calls, best,
-            flops / (best * 1e-3) / 1e12, t.tpo_get_opt(ctx, "last_cta_group")))
+        print("%s tp=%d n=%d k=%d m=%d %s: best of %d calls %.4f ms, %.1f TFLOP/s "
+              "(%d producer CTAs, %d GEMM CTAs, cta_group %d)" % (
+                  args.op, args.tp, args.n, args.k, args.m, args.dtype, args.calls, best,
+                  flops / (best * 1e-3) / 1e12, t.tpo_get_opt(ctx, "last_producer_ctas"),
+                  t.tpo_get_opt(ctx, "last_gemm_ctas"), t.tpo_get_opt(ctx, "last_cta_group")))
     finally:
         t.tpo_ctx_destroy(ctx)
 
