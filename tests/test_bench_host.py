@@ -49,3 +49,11 @@ def test_reference_arm_line(tmp_path):
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_nominal_peak_fractions():
+    import bench
+    nom = bench.nominal_peak(1000.0, 152, 2070.0, 1850.0)
+    assert nom["peak_at_max_clock"] == round(152 * 8192 * 2070e6 / 1e12, 1)
+    assert abs(nom["frac_at_kernel_clock"] - 1000.0 / (152 * 8192 * 1850e6 / 1e12)) < 1e-4
+    assert "peak_at_kernel_clock" not in bench.nominal_peak(1000.0, 152, 2070.0, None)
