@@ -74,14 +74,17 @@ typedef enum {
 #define TPO_MAX_ROW_CHUNKS 64
 #define TPO_BLOCK_M 128 /* rows of one output tile */
 #define TPO_BLOCK_N 256 /* columns of one output tile */
+/* Sizes need not be multiples of the tile: the last tile of a slot, block or
+ * part loads zeros past its edge and stores only the rows and columns that
+ * exist.  Row pitches must be multiples of 16 bytes. */
 
 /*
  * Create a context for one problem size on the current CUDA device.
  *   tp     number of simulated ranks, 1..16
- *   n      rows of Y, a multiple of tp*128
- *   k      global contraction length: a multiple of 64 (bf16) or 128 (e4m3);
- *          for RS/AR also k % tp == 0 and k/tp a multiple of 64 (128 for e4m3)
- *   m      columns of Y, a multiple of 256
+ *   n      rows of Y, a multiple of tp (every rank holds n/tp rows)
+ *   k      global contraction length: a multiple of 8 (bf16) or 16 (e4m3);
+ *          for RS/AR also k % tp == 0 and k/tp a multiple of 8 (16 for e4m3)
+ *   m      columns of Y, a multiple of 8
  *   dtype  a tpo_dtype value
  * Allocates the staging buffer (n*k elements), counters, error word and trace
  * buffer on the current device.  Returns NULL on any error (no half-built
@@ -127,7 +130,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* ctx, const void* const* x, const void* w, void* 
  * the output rows owned by rank b accumulate ranks b+1, b+2, ..., b (mod tp),
  * the order of a ring reduce-scatter that ends at the owner, in fp32, with a
  * single rounding to bf16 in the epilogue.  e4m3 contexts take their scales
- * from tpo_set_fp8_scales and need (k/tp) a multiple of 128.
+ * from tpo_set_fp8_scales.
  */
 tpo_status tpo_gemm_rs(tpo_ctx* ctx, const void* const* x, const void* const* w, void* const* y,
                        void* stream);
@@ -136,7 +139,7 @@ tpo_status tpo_gemm_rs(tpo_ctx* ctx, const void* const* x, const void* const* w,
  * GEMM+AR (row-parallel linear): Y[n, m] = sum_r X_r . W_r^T.
  *   x, w          as tpo_gemm_rs
  *   y             device pointer [n, m] bf16
- *   n_row_chunks  1..64; n must be a multiple of n_row_chunks*tp*128
+ *   n_row_chunks  1..64; n must be a multiple of n_row_chunks*tp
  * Output tiles are produced chunk by chunk (row chunk 0 first).  Inside row
  * chunk c, the rows of the chunk's i-th of tp equal parts sum ranks i+1, ...,
  * i (mod tp), the per-part order of a ring all-reduce of that chunk.  After

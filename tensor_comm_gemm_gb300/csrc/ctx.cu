@@ -64,7 +64,22 @@ bool encode2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A [inner, rows, slots] view of `slots` consecutive row-major [rows, inner]
+// blocks; a box never crosses from one block into the next (rows past a
+// block's end load as zeros and are clipped on stores).
+bool encode3d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem, uint64_t inner, uint64_t rows,
+              uint64_t slots, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  cuuint64_t dims[3] = {inner, rows, slots};
+  cuuint64_t strides[2] = {inner * static_cast<uint64_t>(elem), inner * static_cast<uint64_t>(elem) * rows};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
@@ -292,10 +307,10 @@ int producer_count(const tpo_ctx* c, int cg, int tiles) {
 
 // Validation shared by RS and AR.
 tpo_status check_ksplit(tpo_ctx* c, const void* const* x, const void* const* w) {
-  const int kq = c->dtype == TPO_BF16 ? 64 : 128;
+  const int kq = c->dtype == TPO_BF16 ? 8 : 16;
   if (c->k % c->tp != 0 || (c->k / c->tp) % kq != 0)
-    return fail(TPO_ERR_UNSUPPORTED, "k/tp must be an integer multiple of %d (k=%lld, tp=%d)", kq, (long long)c->k,
-                c->tp);
+    return fail(TPO_ERR_UNSUPPORTED, "k/tp must be an integer multiple of %d (16-byte rows; k=%lld, tp=%d)", kq,
+                (long long)c->k, c->tp);
   if (c->dtype == TPO_FP8_E4M3 && (!c->ks_scale_x || !c->ks_scale_w))
     return fail(TPO_ERR_INVALID_ARG, "e4m3 GEMM+RS/AR needs tpo_set_fp8_scales first");
   if (!x || !w) return fail(TPO_ERR_INVALID_ARG, "x and w must be arrays of tp device pointers");
@@ -336,18 +351,19 @@ tpo_ctx* tpo_ctx_create(int tp, int64_t n, int64_t k, int64_t m, int dtype) {
          (long long)m);
     return nullptr;
   }
-  if (n % (static_cast<int64_t>(tp) * tpo::BM) != 0) {
-    fail(TPO_ERR_UNSUPPORTED, "n=%lld must be a multiple of tp*%d=%lld", (long long)n, tpo::BM,
-         (long long)tp * tpo::BM);
+  // Any size works with the tiling (partial tiles load zeros and clip their
+  // stores); what remains are equal chunks per rank and 16-byte row pitches.
+  if (n % tp != 0) {
+    fail(TPO_ERR_UNSUPPORTED, "n=%lld must be a multiple of tp=%d (equal row chunks per rank)", (long long)n, tp);
     return nullptr;
   }
-  if (m % tpo::BN != 0) {
-    fail(TPO_ERR_UNSUPPORTED, "m=%lld must be a multiple of %d", (long long)m, tpo::BN);
+  if (m % 8 != 0) {
+    fail(TPO_ERR_UNSUPPORTED, "m=%lld must be a multiple of 8 (16-byte rows of the bf16 output)", (long long)m);
     return nullptr;
   }
-  const int kq = dtype == TPO_BF16 ? 64 : 128;
+  const int kq = dtype == TPO_BF16 ? 8 : 16;
   if (k % kq != 0) {
-    fail(TPO_ERR_UNSUPPORTED, "k=%lld must be a multiple of %d for this dtype", (long long)k, kq);
+    fail(TPO_ERR_UNSUPPORTED, "k=%lld must be a multiple of %d for this dtype (16-byte rows)", (long long)k, kq);
     return nullptr;
   }
   tpo_ctx* c = new tpo_ctx();
@@ -502,12 +518,12 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   const void* key[5] = {c->staging, x[c->self_rank], w, y, reinterpret_cast<const void*>(static_cast<intptr_t>(cg))};
   if (!cache_lookup(c, tpo::OP_AG, key, 5, p)) {
     const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    bool ok = encode2d(&p.mapA[0], c->staging, dt, elem, c->k, c->n, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode2d(&p.mapA[1], x[c->self_rank], dt, elem, c->k, rows, kel, tpo::BM,
-                       CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode2d(&p.mapB[0], w, dt, elem, c->k, c->m, kel, tpo::BN / cg, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode2d(&p.mapY[0], y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->m, c->n, tpo::EPI_COLS, 32,
-                       CU_TENSOR_MAP_SWIZZLE_64B);
+    bool ok =
+        encode3d(&p.mapA[0], c->staging, dt, elem, c->k, rows, c->tp, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        encode3d(&p.mapA[1], x[c->self_rank], dt, elem, c->k, rows, 1, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        encode2d(&p.mapB[0], w, dt, elem, c->k, c->m, kel, tpo::BN / cg, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        encode3d(&p.mapY[0], y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->m, rows, c->tp, tpo::EPI_COLS, 32,
+                 CU_TENSOR_MAP_SWIZZLE_64B);
     if (!ok) return fail(TPO_ERR_INVALID_ARG, "tensor map encoding failed (pointer or size not TMA-compatible)");
     cache_store(c, tpo::OP_AG, key, 5, p);
   }
@@ -516,10 +532,12 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   p.scale_w = d_scale_inv_w;
   p.chunk_bytes = rows * c->k * elem;
   p.rows_per_group = static_cast<int>(rows);
-  p.row_tiles = static_cast<int>(rows / (tpo::BM * cg));
-  p.col_tiles = static_cast<int>(c->m / tpo::BN);
+  p.row_tiles = static_cast<int>(ceil_div(rows, tpo::BM * cg));
+  p.col_tiles = static_cast<int>(ceil_div(c->m, tpo::BN));
+  p.m = static_cast<int>(c->m);
+  p.y_rows = static_cast<int>(rows);
   p.num_groups = c->tp;
-  p.kb_per_seg = static_cast<int>(c->k * elem / tpo::BK_BYTES);
+  p.kb_per_seg = static_cast<int>(ceil_div(c->k * elem, tpo::BK_BYTES));
   p.num_segs = 1;
   p.gate = 1;
   p.kps = (cg == 2 && p.kb_per_seg % 2 == 0) ? 2 : 1;  // pairs: two K blocks per stage when they divide
@@ -591,8 +609,8 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
         const int slot = static_cast<int>(((c->self_rank - step) % c->tp + c->tp) % c->tp);
         gp.self_rank = slot;  // group 0 of a one-group launch is this slot
         if (step > 0) {
-          if (!encode2d(&gp.mapA[1], c->staging + static_cast<size_t>(slot) * p.chunk_bytes, dt, elem, c->k, rows,
-                        kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B))
+          if (!encode3d(&gp.mapA[1], c->staging + static_cast<size_t>(slot) * p.chunk_bytes, dt, elem, c->k, rows,
+                        1, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B))
             return fail(TPO_ERR_INVALID_ARG, "tensor map encoding failed");
           e = cudaStreamWaitEvent(s, c->ev_copy[slot], 0);
           if (e != cudaSuccess) return cuda_fail(e, "split wait");
@@ -622,7 +640,8 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   const int64_t kr = c->k / c->tp;
   const int groups = (op == tpo::OP_RS) ? c->tp : n_chunks;
   const int64_t rows_per_group = c->n / groups;
-  const int cg = choose_cg(c, rows_per_group, op == tpo::OP_AR ? rows_per_group / c->tp : rows_per_group);
+  const int64_t part_rows = (op == tpo::OP_AR) ? rows_per_group / c->tp : rows_per_group;
+  const int cg = choose_cg(c, rows_per_group, part_rows);
   if (cg < 0) return fail(TPO_ERR_UNSUPPORTED, "cta_group=2 needs 256-row tile groups and placeable CTA pairs");
   Params p;
   tpo::init_params(p);
@@ -645,23 +664,27 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   if (!cache_lookup(c, op, key, nkey, p)) {
     bool ok = true;
     for (int r = 0; r < c->tp && ok; ++r) {
-      ok = encode2d(&p.mapA[r], x[r], dt, elem, kr, c->n, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+      ok = encode3d(&p.mapA[r], x[r], dt, elem, kr, c->n, 1, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
            encode2d(&p.mapB[r], w[r], dt, elem, kr, c->m, kel, tpo::BN / cg, CU_TENSOR_MAP_SWIZZLE_128B);
       if (ok && op == tpo::OP_RS)
-        ok = encode2d(&p.mapY[r], yb[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->m, c->n / c->tp, tpo::EPI_COLS,
-                      32, CU_TENSOR_MAP_SWIZZLE_64B);
+        ok = encode3d(&p.mapY[r], yb[r], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->m, c->n / c->tp, 1,
+                      tpo::EPI_COLS, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     }
-    if (ok && op == tpo::OP_AR)
-      ok = encode2d(&p.mapY[0], y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->m, c->n, tpo::EPI_COLS, 32,
-                    CU_TENSOR_MAP_SWIZZLE_64B);
+    if (ok && op == tpo::OP_AR)  // one map slot per ring-order part of every row chunk
+      ok = encode3d(&p.mapY[0], y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c->m, part_rows,
+                    static_cast<uint64_t>(groups) * c->tp, tpo::EPI_COLS, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!ok) return fail(TPO_ERR_INVALID_ARG, "tensor map encoding failed (pointer or size not TMA-compatible)");
     cache_store(c, op, key, nkey, p);
   }
   p.rows_per_group = static_cast<int>(rows_per_group);
-  p.row_tiles = p.rows_per_group / (tpo::BM * cg);
-  p.col_tiles = static_cast<int>(c->m / tpo::BN);
+  p.part_rows = static_cast<int>(part_rows);
+  p.tiles_per_part = static_cast<int>(ceil_div(part_rows, tpo::BM * cg));
+  p.row_tiles = (op == tpo::OP_AR) ? c->tp * p.tiles_per_part : p.tiles_per_part;
+  p.col_tiles = static_cast<int>(ceil_div(c->m, tpo::BN));
+  p.m = static_cast<int>(c->m);
+  p.y_rows = static_cast<int>(part_rows);
   p.num_groups = groups;
-  p.kb_per_seg = static_cast<int>(kr * elem / tpo::BK_BYTES);
+  p.kb_per_seg = static_cast<int>(ceil_div(kr * elem, tpo::BK_BYTES));
   p.num_segs = c->tp;
   p.gate = 0;
   p.scale_x = c->ks_scale_x;
@@ -679,8 +702,8 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
       c->ar_target = 0;
       c->ar_chunks = n_chunks;
     }
-    // one release per epilogue warp and 128-row share of every tile of the chunk
-    c->ar_target += static_cast<uint32_t>((rows_per_group / tpo::BM) * p.col_tiles * tpo::EPI_WARPS);
+    // one release per epilogue warp of every CTA of every tile of the chunk
+    c->ar_target += static_cast<uint32_t>(p.row_tiles * cg * p.col_tiles * tpo::EPI_WARPS);
     p.ar_target = c->ar_target;
   }
   p.num_producers = 0;
@@ -706,8 +729,9 @@ tpo_status tpo_gemm_ar(tpo_ctx* c, const void* const* x, const void* const* w, v
   if (!aligned16(y)) return fail(TPO_ERR_INVALID_ARG, "y must be non-NULL and 16-byte aligned");
   if (n_row_chunks < 1 || n_row_chunks > TPO_MAX_ROW_CHUNKS)
     return fail(TPO_ERR_INVALID_ARG, "n_row_chunks=%d outside [1, %d]", n_row_chunks, TPO_MAX_ROW_CHUNKS);
-  if (c->n % (static_cast<int64_t>(n_row_chunks) * c->tp * tpo::BM) != 0)
-    return fail(TPO_ERR_UNSUPPORTED, "n=%lld must be a multiple of n_row_chunks*tp*%d", (long long)c->n, tpo::BM);
+  if (c->n % (static_cast<int64_t>(n_row_chunks) * c->tp) != 0)
+    return fail(TPO_ERR_UNSUPPORTED, "n=%lld must be a multiple of n_row_chunks*tp (equal ring-order parts)",
+                (long long)c->n);
   return ksplit_common(c, tpo::OP_AR, x, w, nullptr, y, n_row_chunks, static_cast<cudaStream_t>(stream));
 }
 

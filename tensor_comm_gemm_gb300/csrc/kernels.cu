@@ -121,10 +121,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
       : "memory");
 }
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+// A operands: [inner K, rows, slot] maps, so a tile's rows never run into the
+// next slot (rows past a slot's end read as zeros).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+// Outputs: [m, rows, slot] maps; the store writes only the part of the box
+// inside the slot and inside m.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
-               "r"(src), "r"(x), "r"(y)
+               "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -282,6 +293,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, "
+      "%4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 
 template <int CG>
 __device__ __forceinline__ void tmem_alloc_cg(uint32_t slot_smem, uint32_t ncols) {
@@ -355,9 +374,11 @@ __device__ __forceinline__ void mma_commit_local_cg(uint32_t bar) {
 struct Tile {
   int a_map;  // AG: 0 staging, 1 X_self
   int a_row;  // row coordinate of the A tile in its map
+  int a_z;    // slot coordinate of the A tile in its map
   int gate;   // slot whose counter gates the A loads, or -1
   int y_map;  // output map index
   int y_row;  // row coordinate of the output tile in its map
+  int y_z;    // slot coordinate of the output tile in its map
   int col;    // first output column (= first W row)
   int seg0;   // RS/AR: rank of the first K segment
   int group;  // AR: row chunk
@@ -380,27 +401,35 @@ __device__ __forceinline__ Tile tile_at(const Params& p, int t) {
     const int slot = ((p.self_rank - grp) % p.tp + p.tp) % p.tp;
     // ring step 0 is the observer's own chunk: read in place, nothing to wait on
     T.a_map = (grp == 0) ? 1 : 0;
-    T.a_row = (grp == 0) ? r * TILE_M : slot * p.rows_per_group + r * TILE_M;
+    T.a_row = r * TILE_M;
+    T.a_z = (grp == 0) ? 0 : slot;
     T.gate = (grp == 0 || !p.gate) ? -1 : slot;
     T.y_map = 0;
-    T.y_row = slot * p.rows_per_group + r * TILE_M;
+    T.y_row = r * TILE_M;
+    T.y_z = slot;
     T.seg0 = 0;
   } else if (p.op == OP_RS) {
+    // rows past the block's end (a ragged last tile) are computed but never stored
     T.a_map = -1;
     T.a_row = grp * p.rows_per_group + r * TILE_M;
+    T.a_z = 0;
     T.gate = -1;
     T.y_map = grp;
     T.y_row = r * TILE_M;
+    T.y_z = 0;
     T.seg0 = (grp + 1) % p.tp;  // ring reduce-scatter: the owner's own slice comes last
   } else {
-    const int local = r * TILE_M;
-    const int owner = (local * p.tp) / p.rows_per_group;  // part of the chunk owned in a ring all-reduce
+    // a row chunk is tp ring-order parts (part i sums ranks i+1, ..., i), each
+    // tiled on its own so that no tile mixes two summation orders
+    const int part = r / p.tiles_per_part, rr = r - part * p.tiles_per_part;
     T.a_map = -1;
-    T.a_row = grp * p.rows_per_group + local;
+    T.a_row = grp * p.rows_per_group + part * p.part_rows + rr * TILE_M;
+    T.a_z = 0;
     T.gate = -1;
     T.y_map = 0;
-    T.y_row = T.a_row;
-    T.seg0 = (owner + 1) % p.tp;
+    T.y_row = rr * TILE_M;
+    T.y_z = grp * p.tp + part;
+    T.seg0 = (part + 1) % p.tp;
   }
   return T;
 }
@@ -541,7 +570,7 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
     }
     int r = AG ? T.a_map : T.seg0;  // tensor map of the current K segment
     int kk = 0;
-    const int a_row = T.a_row + a_off, b_row = T.col + b_off;
+    const int a_row = T.a_row + a_off, a_z = T.a_z, b_row = T.col + b_off;
     for (int i = 0; i < nkb; ++i) {
       const uint32_t sbase_stage = sbase + SMEM_STAGES + stage * stage_bytes;
       if (blk == 0) {  // a new stage: wait until the MMAs released it, then arm its barrier
@@ -560,12 +589,12 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
       const int kx = kk * kelems;
       if constexpr (CG == 1) {
         const uint32_t fb = full0 + 8u * stage;
-        tma_load_2d(sa, ma, fb, kx, a_row);
+        tma_load_3d(sa, ma, fb, kx, a_row, a_z);
         tma_load_2d(sb, mb, fb, kx, b_row);
       } else {
         // both halves complete on the even CTA's barrier, which expects the pair's bytes
         const uint32_t fl = full0_leader + 8u * stage;
-        tma_load_2d_pair(sa, ma, fl, kx, a_row);
+        tma_load_3d_pair(sa, ma, fl, kx, a_row, a_z);
         tma_load_2d_pair(sb, mb, fl, kx, b_row);
       }
       if (++kk == kb_per_seg) {  // next K segment: the next rank in ring order
@@ -795,8 +824,9 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&p.mapY[T.y_map], buf, T.col + c * EPI_COLS, T.y_row + row_off + quad * 32);
+        const int ox = T.col + c * EPI_COLS, oy = T.y_row + row_off + quad * 32;
+        if (lane == 0 && ox < p.m && oy < p.y_rows) {  // boxes wholly past the output's edge are skipped
+          tma_store_3d(&p.mapY[T.y_map], buf, ox, oy, T.y_z);
           bulk_commit();
         }
       }

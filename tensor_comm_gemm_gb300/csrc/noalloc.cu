@@ -106,6 +106,17 @@ bool encode(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem
                      sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [inner, rows, slots] view of `slots` consecutive [rows, inner] blocks.
+bool encode3(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem, uint64_t inner, uint64_t rows,
+             uint64_t slots, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  cuuint64_t dims[3] = {inner, rows, slots};
+  cuuint64_t strides[2] = {inner * static_cast<uint64_t>(elem), inner * static_cast<uint64_t>(elem) * rows};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode_fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -118,13 +129,12 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
   if (dtype != TPO_BF16 && dtype != TPO_FP8_E4M3) return fail(TPO_ERR_INVALID_ARG, "dtype=%d unknown", dtype);
   if (n <= 0 || k <= 0 || m <= 0 || n > (1ll << 30) || k > (1ll << 30) || m > (1ll << 30))
     return fail(TPO_ERR_INVALID_ARG, "sizes must be in [1, 2^30]");
-  if (n % (static_cast<int64_t>(tp) * tpo::BM) != 0)
-    return fail(TPO_ERR_UNSUPPORTED, "n=%lld must be a multiple of tp*%d", (long long)n, tpo::BM);
-  if (m % tpo::BN != 0) return fail(TPO_ERR_UNSUPPORTED, "m=%lld must be a multiple of %d", (long long)m, tpo::BN);
+  if (n % tp != 0) return fail(TPO_ERR_UNSUPPORTED, "n=%lld must be a multiple of tp=%d", (long long)n, tp);
+  if (m % 8 != 0) return fail(TPO_ERR_UNSUPPORTED, "m=%lld must be a multiple of 8", (long long)m);
   const bool fp8 = dtype == TPO_FP8_E4M3;
   const int elem = fp8 ? 1 : 2;
-  if (k % (fp8 ? 128 : 64) != 0) return fail(TPO_ERR_UNSUPPORTED, "k=%lld not a multiple of %d", (long long)k,
-                                              fp8 ? 128 : 64);
+  if (k % (fp8 ? 16 : 8) != 0) return fail(TPO_ERR_UNSUPPORTED, "k=%lld not a multiple of %d", (long long)k,
+                                            fp8 ? 16 : 8);
   const uint64_t staging_bytes = static_cast<uint64_t>(n) * static_cast<uint64_t>(k) * elem;
   if (staging_bytes > TPO_NOALLOC_MAX_STAGING_BYTES)
     return fail(TPO_ERR_INVALID_ARG,
@@ -159,11 +169,11 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
   const int64_t rows = n / tp;
   const int kel = tpo::BK_BYTES / elem;
   const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!(encode(&p.mapA[0], staging, dt, elem, k, n, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
-        encode(&p.mapA[1], x[0], dt, elem, k, rows, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+  if (!(encode3(&p.mapA[0], staging, dt, elem, k, rows, tp, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        encode3(&p.mapA[1], x[0], dt, elem, k, rows, 1, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
         encode(&p.mapB[0], w, dt, elem, k, m, kel, tpo::BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
-        encode(&p.mapY[0], y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, m, n, tpo::EPI_COLS, 32,
-               CU_TENSOR_MAP_SWIZZLE_64B)))
+        encode3(&p.mapY[0], y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, m, rows, tp, tpo::EPI_COLS, 32,
+                CU_TENSOR_MAP_SWIZZLE_64B)))
     return fail(TPO_ERR_INVALID_ARG, "tensor map encoding failed (pointer or size not TMA-compatible)");
   for (int r = 0; r < tp; ++r) p.src[r] = static_cast<const uint8_t*>(x[r]);
   p.staging = staging;
@@ -177,10 +187,12 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
   p.tp = tp;
   p.self_rank = 0;
   p.rows_per_group = static_cast<int>(rows);
-  p.row_tiles = static_cast<int>(rows / tpo::BM);
-  p.col_tiles = static_cast<int>(m / tpo::BN);
+  p.row_tiles = static_cast<int>((rows + tpo::BM - 1) / tpo::BM);
+  p.col_tiles = static_cast<int>((m + tpo::BN - 1) / tpo::BN);
+  p.m = static_cast<int>(m);
+  p.y_rows = static_cast<int>(rows);
   p.num_groups = tp;
-  p.kb_per_seg = static_cast<int>(k * elem / tpo::BK_BYTES);
+  p.kb_per_seg = static_cast<int>((k * elem + tpo::BK_BYTES - 1) / tpo::BK_BYTES);
   p.num_segs = 1;
   p.gate = 1;
   const int P = kProducers < s->num_sms - 1 ? kProducers : s->num_sms - 1;

@@ -83,9 +83,11 @@ struct DevWords {
 };
 
 struct Params {
-  CUtensorMap mapA[TPO_MAX_TP];  // AG: [0] staging [n,k], [1] X_self; RS/AR: X_r
+  // Tensor maps.  A and Y maps are 3-D [inner, rows, slot] so that tiles clip at
+  // slot edges; B maps are 2-D [k, m].
+  CUtensorMap mapA[TPO_MAX_TP];  // AG: [0] staging [k, n/tp, tp], [1] X_self [k, n/tp, 1]; RS/AR: X_r [k/tp, n, 1]
   CUtensorMap mapB[TPO_MAX_TP];  // AG: [0] W; RS/AR: W_r
-  CUtensorMap mapY[TPO_MAX_TP];  // AG/AR: [0] Y; RS: y[b]
+  CUtensorMap mapY[TPO_MAX_TP];  // AG: [0] Y [m, n/tp, tp]; RS: y[b] [m, n/tp, 1]; AR: [0] Y [m, part rows, parts]
   const uint8_t* src[TPO_MAX_TP];  // producer sources X_r
   uint8_t* staging;
   DevWords* words;
@@ -104,8 +106,12 @@ struct Params {
   int num_producers;      // CTAs [0, num_producers) run the producer role
   int num_gemm;           // CTAs [num_producers, +num_gemm) run the GEMM role
   int rows_per_group;     // AG: rows per slot; RS: rows per block; AR: rows per chunk
-  int row_tiles;          // BM tiles per group
-  int col_tiles;          // BN tiles across m
+  int row_tiles;          // row tiles per group (the last one may be partial)
+  int col_tiles;          // BN tiles across m (the last one may be partial)
+  int part_rows;          // AR: rows of one ring-order part of a chunk (rows_per_group / tp)
+  int tiles_per_part;     // AR: row tiles per part
+  int m;                  // output columns
+  int y_rows;             // rows of one slot of the output map (store boxes starting past it are skipped)
   int num_groups;         // AG: tp slots; RS: tp blocks; AR: row chunks
   int kb_per_seg;         // 128-byte K blocks per segment
   int num_segs;           // AG: 1; RS/AR: tp

@@ -42,10 +42,10 @@ def test_version_names_target(lib):
     ((17, 256, 256, 256, 0), "tp"),
     ((2, 256, 256, 256, 7), "dtype"),
     ((2, 0, 256, 256, 0), "sizes"),
-    ((2, 192, 256, 256, 0), "n="),        # not a multiple of tp*128
-    ((2, 256, 256, 200, 0), "m="),        # not a multiple of 256
-    ((2, 256, 96, 256, 0), "k="),         # bf16 needs k % 64
-    ((2, 256, 192, 256, 1), "k="),        # e4m3 needs k % 128
+    ((3, 256, 256, 256, 0), "n="),        # unequal row chunks (n % tp)
+    ((2, 256, 256, 100, 0), "m="),        # bf16 output rows not a multiple of 16 bytes
+    ((2, 256, 100, 256, 0), "k="),        # bf16 rows of 200 bytes
+    ((2, 256, 200, 256, 1), "k="),        # e4m3 rows of 200 bytes
 ])
 def test_create_rejects_bad_arguments(lib, args, word):
     assert not lib.tpo_ctx_create(*args)

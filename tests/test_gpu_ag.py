@@ -212,7 +212,7 @@ def test_call_argument_errors():
             t.tpo_set_opt(run.ctx, "no_such_option", 1)
         with pytest.raises(t.TpoError) as e:
             t.tpo_gemm_ar(run.ctx, [x.data_ptr() for x in run.xs], [run.w.data_ptr()] * 2, run.y,
-                          3)   # n % (3*tp*128) != 0
+                          3)   # n % (3*tp) != 0: unequal ring-order parts
         assert e.value.status == 2
     finally:
         run.close()

@@ -113,11 +113,11 @@ def test_ksplit_rejects_fp8_and_bad_shapes():
         assert e.value.status == 1
     finally:
         t.tpo_ctx_destroy(ctx)
-    ctx = t.tpo_ctx_create(4, 512, 256, 256, t.TPO_FP8_E4M3)    # k/tp = 64: not a whole e4m3 K block
+    ctx = t.tpo_ctx_create(4, 512, 160, 256, t.TPO_FP8_E4M3)    # k/tp = 40: e4m3 rows of 40 bytes
     try:
         sc = torch.ones(1, device="cuda")
         t.tpo_set_fp8_scales(ctx, sc, sc)
-        x = torch.zeros((512, 64), dtype=torch.uint8, device="cuda")
+        x = torch.zeros((512, 48), dtype=torch.uint8, device="cuda")
         with pytest.raises(t.TpoError) as e:        # raw pointers: the library's own shape check
             t.tpo_gemm_rs(ctx, [x.data_ptr()] * 4, [x.data_ptr()] * 4, [x.data_ptr()] * 4)
         assert e.value.status == 2

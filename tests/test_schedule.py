@@ -1,9 +1,11 @@
 """CPU mirror of the fused kernel's tile schedule and producer split.
 
 The kernel's index arithmetic (tile order, TMA coordinates, producer pieces)
-is restated here and checked, for every workload shape and some edge shapes,
-to cover each output element exactly once, to keep every tensor-map access in
-bounds and 16-byte aligned, and to follow the ring orders of the pages.
+is restated here and checked, for every workload shape and for ragged shapes
+(partial row, column and K tiles), to cover each output element exactly once
+with stores that start inside the output, to load the rows each tile stores,
+to keep every TMA inner coordinate 16-byte aligned, and to follow the ring
+orders of the pages.
 """
 
 import pytest
@@ -13,25 +15,28 @@ from tensor_comm_gemm_gb300 import synth
 BM, BN, BK_BYTES, COPY_PIECE, EPI_COLS = 128, 256, 128, 16384, 32
 
 
-def tile_at(op, tp, self_rank, rows_per_group, row_tiles, col_tiles, t, tile_m=BM):
+def cdiv(a, b):
+    return -(-a // b)
+
+
+def tile_at(op, tp, self_rank, pl, t):
+    """The kernel's tile_at: A and output coordinates are (row, slot) pairs of
+    the 3-D [inner, rows, slot] tensor maps."""
+    row_tiles, col_tiles, tile_m, rpg = pl["row_tiles"], pl["col_tiles"], pl["tile_m"], pl["rows_per_group"]
     per = row_tiles * col_tiles
     grp, rem = divmod(t, per)
     c, r = divmod(rem, row_tiles)
     col = c * BN
     if op == "ag":
         slot = (self_rank - grp) % tp
-        a_map = 1 if grp == 0 else 0
-        a_row = r * tile_m if grp == 0 else slot * rows_per_group + r * tile_m
-        gate = -1 if grp == 0 else slot
-        return dict(a_map=a_map, a_row=a_row, gate=gate, y_map=0, y_row=slot * rows_per_group + r * tile_m,
-                    col=col, seg0=0, group=grp)
+        return dict(a_map=1 if grp == 0 else 0, a_row=r * tile_m, a_z=0 if grp == 0 else slot,
+                    gate=-1 if grp == 0 else slot, y_map=0, y_row=r * tile_m, y_z=slot, col=col, seg0=0, group=grp)
     if op == "rs":
-        return dict(a_map=-1, a_row=grp * rows_per_group + r * tile_m, gate=-1, y_map=grp, y_row=r * tile_m,
+        return dict(a_map=-1, a_row=grp * rpg + r * tile_m, a_z=0, gate=-1, y_map=grp, y_row=r * tile_m, y_z=0,
                     col=col, seg0=(grp + 1) % tp, group=grp)
-    local = r * tile_m
-    owner = (local * tp) // rows_per_group
-    return dict(a_map=-1, a_row=grp * rows_per_group + local, gate=-1, y_map=0,
-                y_row=grp * rows_per_group + local, col=col, seg0=(owner + 1) % tp, group=grp)
+    part, rr = divmod(r, pl["tiles_per_part"])
+    return dict(a_map=-1, a_row=grp * rpg + part * pl["part_rows"] + rr * tile_m, a_z=0, gate=-1, y_map=0,
+                y_row=rr * tile_m, y_z=grp * tp + part, col=col, seg0=(part + 1) % tp, group=grp)
 
 
 def choose_cg(op, tp, n, chunks):
@@ -45,20 +50,24 @@ def choose_cg(op, tp, n, chunks):
 
 def plan(op, tp, n, k, m, elem=2, chunks=1, cg=1):
     tile_m = BM * cg
-    if op == "ag":
-        rows = n // tp
-        return dict(rows_per_group=rows, row_tiles=rows // tile_m, col_tiles=m // BN, groups=tp,
-                    kb=k * elem // BK_BYTES, segs=1, tile_m=tile_m)
-    groups = tp if op == "rs" else chunks
+    groups = tp if op in ("ag", "rs") else chunks
     rows = n // groups
-    return dict(rows_per_group=rows, row_tiles=rows // tile_m, col_tiles=m // BN, groups=groups,
-                kb=(k // tp) * elem // BK_BYTES, segs=tp, tile_m=tile_m)
+    part_rows = rows // tp if op == "ar" else rows
+    tpp = cdiv(part_rows, tile_m)
+    kseg = k if op == "ag" else k // tp
+    return dict(rows_per_group=rows, part_rows=part_rows, tiles_per_part=tpp,
+                row_tiles=tp * tpp if op == "ar" else tpp, col_tiles=cdiv(m, BN), groups=groups,
+                kb=cdiv(kseg * elem, BK_BYTES), tile_m=tile_m, y_rows=part_rows)
 
 
 SHAPES = [("ag", 2, 256, 256, 256, 2, 1), ("ag", 4, 4096, 4096, 4096, 2, 1), ("ag", 8, 16384, 8192, 28672, 1, 1),
           ("ag", 3, 768, 192, 768, 2, 1), ("ag", 1, 128, 64, 256, 2, 1),
           ("ar", 2, 8192, 8192, 8192, 2, 4), ("ar", 3, 2304, 384, 512, 2, 2),
-          ("rs", 8, 16384, 28672, 8192, 2, 1), ("rs", 3, 768, 192, 512, 2, 1), ("rs", 1, 256, 64, 256, 2, 1)]
+          ("rs", 8, 16384, 28672, 8192, 2, 1), ("rs", 3, 768, 192, 512, 2, 1), ("rs", 1, 256, 64, 256, 2, 1),
+          # ragged: partial row tiles, partial column tiles, partial K blocks
+          ("ag", 3, 600, 200, 264, 2, 1), ("ag", 2, 1000, 48, 520, 1, 1), ("ag", 5, 5, 8, 8, 2, 1),
+          ("rs", 3, 390, 48, 24, 2, 1), ("rs", 2, 1030, 96, 776, 1, 1),
+          ("ar", 2, 600, 32, 40, 2, 3), ("ar", 4, 2056, 64, 272, 2, 2)]
 
 
 @pytest.mark.parametrize("op,tp,n,k,m,elem,chunks", SHAPES)
@@ -67,40 +76,40 @@ def test_tiles_cover_output_once_in_bounds(op, tp, n, k, m, elem, chunks, cg):
     if cg == 2 and choose_cg(op, tp, n, chunks) != 2:
         pytest.skip("shape served by the single-SM variant")
     pl = plan(op, tp, n, k, m, elem, chunks, cg)
-    tile_m = pl["tile_m"]
     total = pl["groups"] * pl["row_tiles"] * pl["col_tiles"]
     kel = BK_BYTES // elem
     kcols = k if op == "ag" else k // tp
+    assert (kcols * elem) % 16 == 0 and (m * 2) % 16 == 0  # 16-byte row pitches
     b_rows = BN // cg
+    y_rows = pl["y_rows"]
     for self_rank in sorted({0, tp - 1, tp // 2}):
-        seen = set()
+        boxes = set()
+        covered = 0
         gated_order = []
         for t in range(total):
-            T = tile_at(op, tp, self_rank, pl["rows_per_group"], pl["row_tiles"], pl["col_tiles"], t, tile_m)
-            if op != "ag":
-                # the CTAs of a pair share one K-segment order: one owner for all tile rows
-                rows_part = pl["rows_per_group"] // tp
-                if op == "ar":
-                    assert (T["a_row"] % pl["rows_per_group"]) // rows_part == \
-                        (T["a_row"] % pl["rows_per_group"] + tile_m - 1) // rows_part
+            T = tile_at(op, tp, self_rank, pl, t)
             for rank in range(cg):
                 off = BM * rank
-                if op == "rs":
-                    assert 0 <= T["y_row"] + off and T["y_row"] + off + BM <= n // tp
-                    key = (T["y_map"] * (n // tp) + T["y_row"] + off, T["col"])
-                else:
-                    assert 0 <= T["y_row"] + off and T["y_row"] + off + BM <= n
-                    key = (T["y_row"] + off, T["col"])
-                assert key not in seen
-                seen.add(key)
-                a_rows = (n // tp) if (op == "ag" and T["a_map"] == 1) else n
-                assert 0 <= T["a_row"] + off and T["a_row"] + off + BM <= a_rows
-                # B rows this CTA loads: its share of the tile's columns
-                assert T["col"] + b_rows * rank + b_rows <= m
+                # the rows a CTA loads are the rows it stores (same slot, same offset)
                 if op == "ag":
-                    src_row = T["a_row"] if T["a_map"] == 0 else self_rank * (n // tp) + T["a_row"]
-                    assert src_row == T["y_row"]
-            assert T["col"] + BN <= m and (T["col"] * 2) % 16 == 0
+                    assert T["a_row"] == T["y_row"] and (T["a_map"] == 1 or T["a_z"] == T["y_z"])
+                    if T["a_map"] == 1:
+                        assert T["y_z"] == self_rank
+                elif op == "rs":
+                    assert T["a_row"] == T["y_map"] * pl["rows_per_group"] + T["y_row"]
+                else:
+                    assert T["a_row"] == T["y_z"] * pl["part_rows"] + T["y_row"]
+                assert T["a_row"] + off >= 0 and T["col"] + b_rows * rank >= 0
+                for q in range(4):
+                    for c in range(BN // EPI_COLS):
+                        ox, oy = T["col"] + c * EPI_COLS, T["y_row"] + off + 32 * q
+                        assert (ox * 2) % 16 == 0 and oy >= 0   # stores never start at a negative coordinate
+                        if ox >= m or oy >= y_rows:
+                            continue                            # skipped by the epilogue
+                        key = (T["y_map"], T["y_z"], oy, ox)
+                        assert key not in boxes
+                        boxes.add(key)
+                        covered += (min(oy + 32, y_rows) - oy) * (min(ox + EPI_COLS, m) - ox)
             if op == "ag":
                 if T["gate"] >= 0 and T["gate"] not in gated_order:
                     gated_order.append(T["gate"])
@@ -111,16 +120,15 @@ def test_tiles_cover_output_once_in_bounds(op, tp, n, k, m, elem, chunks, cg):
                     assert order[-1] == T["group"]
             for i in range(pl["kb"]):
                 x = i * kel
-                assert x + kel <= kcols and (x * elem) % 16 == 0
-            for c in range(BN // EPI_COLS):
-                assert ((T["col"] + c * EPI_COLS) * 2) % 16 == 0
-        assert len(seen) == (n // BM) * (m // BN)
+                assert x < kcols and (x * elem) % 16 == 0
+        assert covered == n * m
         if op == "ag":
             assert gated_order == [(self_rank - s) % tp for s in range(1, tp)]
 
 
 @pytest.mark.parametrize("chunk_bytes,P", [(128 * 256 * 2, 8), (1024 * 4096 * 2, 8), (2048 * 8192, 8),
-                                           (128 * 64 * 2, 8), (384 * 192 * 2, 3), (1024 * 4096 * 2, 152)])
+                                           (128 * 64 * 2, 8), (384 * 192 * 2, 3), (1024 * 4096 * 2, 152),
+                                           (200 * 200 * 2, 8), (1 * 8 * 2, 8), (500 * 48, 24)])
 def test_producer_pieces_partition_chunk(chunk_bytes, P):
     pieces = (chunk_bytes + COPY_PIECE - 1) // COPY_PIECE
     covered = 0
@@ -135,6 +143,7 @@ def test_producer_pieces_partition_chunk(chunk_bytes, P):
 
 
 def test_workload_shapes_fit_the_tiling():
+    """The benchmark workloads are whole tiles (no partial tile anywhere)."""
     for idx, (op, dt, tp, n, k, m, chunks) in synth.WORKLOAD_SHAPES.items():
         assert n % (tp * BM) == 0 and m % BN == 0
         if op == "ag":
