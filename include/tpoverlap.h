@@ -203,9 +203,11 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      every running sum to bf16, the arithmetic of a bf16
  *                      ring reduce-scatter such as the bf16 ring all-reduce in
  *                      nvFuser PR "Reference implementation for Linear+Allreduce
- *                      with overlapping".  Modes 1 and 2 give up the
- *                      double-buffered accumulator (tensor memory holds the
- *                      partial and the running sum).
+ *                      with overlapping".  In modes 1 and 2 each rank's
+ *                      partial takes one of the two tensor-memory accumulators
+ *                      and the running sum lives in a context-owned workspace
+ *                      (one 128 x 256 block per SM, fp32 in mode 1, bf16 in
+ *                      mode 2), so the MMAs never wait for the additions.
  * Read-only keys for tpo_get_opt: "last_producer_ctas", "last_gemm_ctas",
  * "last_cta_group" (shape of the context's latest kernel launch: producer
  * CTAs, GEMM CTAs, 1 or 2 CTAs per MMA),

@@ -99,6 +99,7 @@ struct tpo_ctx {
   // device memory
   uint8_t* staging = nullptr;
   size_t staging_bytes = 0;
+  float* ws = nullptr;  // epilogue-reduction running sums, one BM x BN fp32 block per SM
   tpo::DevWords* words = nullptr;
   uint32_t target[TPO_MAX_TP] = {};  // per slot: counter value once the latest call published it
   uint32_t ar_target = 0;  // AR done-counter value after the latest call
@@ -168,6 +169,7 @@ void destroy_all(tpo_ctx* c) {
   if (c->has_last) cudaEventSynchronize(c->last);
   if (c->aux) cudaStreamSynchronize(c->aux);
   if (c->staging) cudaFree(c->staging);
+  if (c->ws) cudaFree(c->ws);
   if (c->words) cudaFree(c->words);
   if (c->copy) cudaStreamSynchronize(c->copy);
   if (c->last) cudaEventDestroy(c->last);
@@ -418,6 +420,8 @@ tpo_ctx* tpo_ctx_create(int tp, int64_t n, int64_t k, int64_t m, int dtype) {
     return nullptr;
   }
   e = cudaMalloc(&c->words, sizeof(tpo::DevWords));
+  if (e == cudaSuccess)
+    e = cudaMalloc(&c->ws, static_cast<size_t>(c->num_sms) * tpo::BM * tpo::BN * sizeof(float));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->last, cudaEventDisableTiming);
   if (e == cudaSuccess) {
@@ -690,6 +694,7 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   p.scale_x = c->ks_scale_x;
   p.scale_w = c->ks_scale_w;
   p.reduce_mode = static_cast<int>(c->reduce);
+  p.ws = c->ws;
   // pairs: two K blocks per stage when every accumulation unit has an even count
   p.kps = (cg == 2 && (p.reduce_mode ? p.kb_per_seg : p.num_segs * p.kb_per_seg) % 2 == 0) ? 2 : 1;
   const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
@@ -708,6 +713,8 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   }
   p.num_producers = 0;
   p.num_gemm = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms, 0, tiles);
+  // the running-sum workspace has one block per SM: at most one GEMM CTA per SM
+  if (p.reduce_mode && p.num_gemm > c->num_sms) p.num_gemm = c->num_sms - c->num_sms % cg;
   return launch(c, p, p.num_gemm, false, s);
 }
 

@@ -166,6 +166,20 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// 16-byte global accesses under an L2 cache policy.
+__device__ __forceinline__ void st_global_v4_keep(uint4* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                  uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(a), "r"(b), "r"(c),
+               "r"(d), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void ld_global_v4_keep(const uint4* p, uint32_t (&h)[4], uint64_t pol) {
+  asm volatile("ld.global.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+               : "l"(p), "l"(pol)
+               : "memory");
+}
+
 // ------------------------------------------------------------------ release / acquire
 
 __device__ __forceinline__ void red_add_release(uint32_t* ptr, uint32_t v) {
@@ -249,18 +263,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
@@ -652,9 +654,10 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   const uint64_t da0 = smem_desc_sw128(sbase + SMEM_STAGES);
   const uint64_t db0 = smem_desc_sw128(sbase + SMEM_STAGES + kps * A_STAGE_BYTES);
   const uint32_t full0 = B.full0, empty0 = B.empty0, tfull0 = B.tfull0, tempty0 = B.tempty0;
-  // Accumulation units: a whole tile (K-slices chained in one accumulator,
-  // double-buffered across tiles), or in the epilogue-reduction modes one
-  // rank's K-slice at a time into buffer 0 while buffer 1 holds the running sum.
+  // Accumulation units: a whole tile (K-slices chained in one accumulator), or
+  // in the epilogue-reduction modes one rank's K-slice.  Units alternate
+  // between the two accumulators, so the epilogue drains one while the MMAs
+  // fill the other.
   const bool per_rank = p.reduce_mode != 0;
   const int units = per_rank ? p.num_segs : 1;
   const int kpu = per_rank ? p.kb_per_seg : nkb;
@@ -663,9 +666,9 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   unsigned long long cyc_full = 0, cyc_tempty = 0;
   for (int t = g; t < total_tiles && ok; t += G)
    for (int u = 0; u < units; ++u, ++ul) {
-    const uint32_t acc = per_rank ? 0u : (ul & 1u);
+    const uint32_t acc = ul & 1u;
     const uint32_t te = tempty0 + 8u * acc;
-    const uint32_t tpar = (per_rank ? (ul & 1u) : ((ul >> 1) & 1u)) ^ 1u;
+    const uint32_t tpar = ((ul >> 1) & 1u) ^ 1u;
     if (!mbar_test(te, tpar) && !mbar_wait_timed(p, te, tpar, SITE_TMEM_EMPTY, true, &cyc_tempty)) {
       ok = false;
       break;
@@ -732,14 +735,23 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
   const int row_off = BM * static_cast<int>(rank);
   const int rmode = p.reduce_mode;
   const int units = rmode ? p.num_segs : 1;
+  // Epilogue-reduction modes: the running sum of the CTA's 128 x 256 tile lives
+  // in its own workspace block, laid out [column chunk][16-byte group][row] so
+  // that a warp's access is one contiguous 512 bytes, and marked to stay in L2
+  // while the operand streams pass through.
+  uint4* const ws_row = rmode ? reinterpret_cast<uint4*>(p.ws) +
+                                    static_cast<size_t>(blockIdx.x - p.num_producers) * (BM * BN / 4) + quad * 32 + lane
+                              : nullptr;
+  uint64_t ws_pol = 0;
+  if (rmode) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(ws_pol));
   uint32_t ul = 0, nst = 0;
   unsigned long long cyc_tfull = 0;
   bool ok_all = true;
   for (int t = g; t < total_tiles && ok_all; t += G) {
     const Tile T = tile_at<PP::TILE_M>(p, t);
     for (int u = 0; u < units; ++u, ++ul) {
-      const uint32_t acc = rmode ? 0u : (ul & 1u);
-      const uint32_t bar = B.tfull0 + 8u * acc, par = rmode ? (ul & 1u) : ((ul >> 1) & 1u);
+      const uint32_t acc = ul & 1u;
+      const uint32_t bar = B.tfull0 + 8u * acc, par = (ul >> 1) & 1u;
       int ok = (lane == 0) ? (mbar_wait_timed(p, bar, par, SITE_TMEM_FULL, true, &cyc_tfull) ? 1 : 0) : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
@@ -751,49 +763,58 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
       const bool last = (u == units - 1);
       const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
       const uint32_t taddr = tmem + lanes + acc * BN;
-      const uint32_t raddr = tmem + lanes + BN;  // running sum (epilogue-reduction modes)
-#pragma unroll 1
-      for (int c = 0; c < BN / EPI_COLS; ++c) {
+      // The running sum of this thread's row, 32 columns per chunk: fp32 in
+      // mode 1; in mode 2 every running sum is a bf16 value, kept as bf16.
+      auto store_sum = [&](int c, const uint32_t(&r)[32]) {
+        if (rmode == 2) {
+          uint4* w4 = reinterpret_cast<uint4*>(ws_row) + c * 4 * BM;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t h[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) h[i] = (r[8 * v + 2 * i] >> 16) | (r[8 * v + 2 * i + 1] & 0xffff0000u);
+            st_global_v4_keep(w4 + v * BM, h[0], h[1], h[2], h[3], ws_pol);
+          }
+        } else {
+          uint4* w4 = reinterpret_cast<uint4*>(ws_row) + c * 8 * BM;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) st_global_v4_keep(w4 + v * BM, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3], ws_pol);
+        }
+      };
+      auto load_sum = [&](int c, uint32_t(&q)[32]) {
+        if (rmode == 2) {
+          const uint4* w4 = reinterpret_cast<const uint4*>(ws_row) + c * 4 * BM;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t h[4];
+            ld_global_v4_keep(w4 + v * BM, h, ws_pol);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              q[8 * v + 2 * i] = h[i] << 16;
+              q[8 * v + 2 * i + 1] = h[i] & 0xffff0000u;
+            }
+          }
+        } else {
+          const uint4* w4 = reinterpret_cast<const uint4*>(ws_row) + c * 8 * BM;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            uint32_t h[4];
+            ld_global_v4_keep(w4 + v * BM, h, ws_pol);
+            q[4 * v] = h[0];
+            q[4 * v + 1] = h[1];
+            q[4 * v + 2] = h[2];
+            q[4 * v + 3] = h[3];
+          }
+        }
+      };
+      // One 32-column chunk: read it from tensor memory (handing the accumulator
+      // back after the last chunk), add it to the running sum `q` in the
+      // epilogue-reduction modes, and either keep the sum in the workspace or
+      // round the result to bf16 and store it.
+      auto chunk = [&](int c, const uint32_t(&q)[32], bool have_q) {
         uint32_t r[32];
         tmem_ld32(taddr + c * EPI_COLS, r);
         tmem_wait_ld();
-        float out_scale = scale;
-        if (rmode) {
-          // this rank's partial, added to the running sum in ring order
-          uint32_t q[32];
-          if (u > 0) {
-            tmem_ld32(raddr + c * EPI_COLS, q);
-            tmem_wait_ld();
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float part = __uint_as_float(r[j]);
-            float v;
-            if (rmode == 2) {  // bf16 on the wire: the partial and every running sum are rounded
-              part = round_bf16(part * scale);
-              v = (u > 0) ? round_bf16(__uint_as_float(q[j]) + part) : part;
-            } else {
-              v = (u > 0) ? __uint_as_float(q[j]) + part : part;
-            }
-            r[j] = __float_as_uint(v);
-          }
-          if (rmode == 2) out_scale = 1.0f;
-          if (!last) {
-            tmem_st32(raddr + c * EPI_COLS, r);
-            if (c == BN / EPI_COLS - 1) {  // partial consumed, running sum written: release buffer 0
-              tmem_wait_st();
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) {
-                if constexpr (CG == 1)
-                  mbar_arrive(B.tempty0 + 8u * acc);
-                else
-                  mbar_arrive_cluster(map_to_rank(B.tempty0 + 8u * acc, 0));
-              }
-            }
-            continue;
-          }
-        }
         if (c == BN / EPI_COLS - 1) {  // accumulator fully read: hand it back to the MMA issuer
           tc_fence_before();
           __syncwarp();
@@ -802,6 +823,27 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
               mbar_arrive(B.tempty0 + 8u * acc);
             else
               mbar_arrive_cluster(map_to_rank(B.tempty0 + 8u * acc, 0));
+          }
+        }
+        float out_scale = scale;
+        if (rmode) {
+          // this rank's partial, added in ring order to the running sum
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float part = __uint_as_float(r[j]);
+            float v;
+            if (rmode == 2) {  // bf16 on the wire: the partial and every running sum are rounded
+              part = round_bf16(part * scale);
+              v = have_q ? round_bf16(__uint_as_float(q[j]) + part) : part;
+            } else {
+              v = have_q ? __uint_as_float(q[j]) + part : part;
+            }
+            r[j] = __float_as_uint(v);
+          }
+          if (rmode == 2) out_scale = 1.0f;
+          if (!last) {
+            store_sum(c, r);
+            return;
           }
         }
         uint32_t packed[16];
@@ -829,6 +871,22 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
           tma_store_3d(&p.mapY[T.y_map], buf, ox, oy, T.y_z);
           bulk_commit();
         }
+      };
+      if (rmode && u > 0) {
+        // the running sum of the next chunk is fetched while this chunk is processed
+        uint32_t qa[32], qb[32];
+        load_sum(0, qa);
+#pragma unroll 1
+        for (int c = 0; c < BN / EPI_COLS; c += 2) {
+          load_sum(c + 1, qb);
+          chunk(c, qa, true);
+          if (c + 2 < BN / EPI_COLS) load_sum(c + 2, qa);
+          chunk(c + 1, qb, true);
+        }
+      } else {
+        const uint32_t none[32] = {};
+#pragma unroll 1
+        for (int c = 0; c < BN / EPI_COLS; ++c) chunk(c, none, false);
       }
     }
     if (ok_all && p.op == OP_AR && lane == 0) {  // this warp's rows of the tile are in memory: count them

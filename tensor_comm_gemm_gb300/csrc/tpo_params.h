@@ -90,6 +90,7 @@ struct Params {
   CUtensorMap mapY[TPO_MAX_TP];  // AG: [0] Y [m, n/tp, tp]; RS: y[b] [m, n/tp, 1]; AR: [0] Y [m, part rows, parts]
   const uint8_t* src[TPO_MAX_TP];  // producer sources X_r
   uint8_t* staging;
+  float* ws;              // RS/AR epilogue-reduction modes: a BM x BN fp32 running sum per GEMM CTA
   DevWords* words;
   const float* scale_x;
   const float* scale_w;
