@@ -20,6 +20,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -53,12 +54,16 @@ def describe(idx):
 
 
 def kernel_sha() -> str:
-    """Hash of the kernel sources; DRAM traffic figures taken with ncu are only
-    reported while they still describe the kernel as built."""
+    """Hash of the kernel sources' code (comments and blank space removed);
+    DRAM traffic figures taken with ncu are only reported while they still
+    describe the kernel as built."""
     h = hashlib.sha256()
     for f in ("kernels.cu", "tpo_params.h"):
-        with open(os.path.join(ROOT, "tensor_comm_gemm_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "tensor_comm_gemm_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)    # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                  # line comments
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

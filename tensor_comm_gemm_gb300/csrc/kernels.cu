@@ -18,9 +18,14 @@
 //    bf16 and TMA-store the tile.  In the pair variant (CG = 2) two CTAs of a
 //    cluster share one 256 x 256 tile through the 2-SM MMA: each loads its own
 //    128 rows of A and half of the B tile, the even CTA issues the MMAs, and
-//    each CTA's tensor memory receives its own 128 rows of the result.  This replaces the counter-gated cuBLAS
-//    atomic GEMM of the same listing.  For GEMM+RS / GEMM+AR the K loop of a
-//    tile walks the ranks' K-slices in a fixed ring order into one accumulator.
+//    each CTA's tensor memory receives its own 128 rows of the result.  This
+//    replaces the counter-gated cuBLAS atomic GEMM of the same listing.  For
+//    GEMM+RS / GEMM+AR the K loop of a tile walks the ranks' K-slices in a
+//    fixed ring order into one accumulator, or (epilogue-reduction modes)
+//    accumulates each rank's slice on its own and the epilogue warps add the
+//    partials in that order.  Sizes need not be whole tiles: A and the output
+//    are addressed through [inner, rows, slot] tensor maps, so the last tile
+//    of a slot loads zeros past the slot's end and its stores are clipped.
 //
 // Every wait (mbarrier, chunk counter) is bounded by the device global timer.
 // On expiry the waiting thread records the failure in the context's error word
