@@ -18,14 +18,9 @@
 //    bf16 and TMA-store the tile.  In the pair variant (CG = 2) two CTAs of a
 //    cluster share one 256 x 256 tile through the 2-SM MMA: each loads its own
 //    128 rows of A and half of the B tile, the even CTA issues the MMAs, and
-//    each CTA's tensor memory receives its own 128 rows of the result.  This
-//    replaces the counter-gated cuBLAS atomic GEMM of the same listing.  For
-//    GEMM+RS / GEMM+AR the K loop of a tile walks the ranks' K-slices in a
-//    fixed ring order into one accumulator, or (epilogue-reduction modes)
-//    accumulates each rank's slice on its own and the epilogue warps add the
-//    partials in that order.  Sizes need not be whole tiles: A and the output
-//    are addressed through [inner, rows, slot] tensor maps, so the last tile
-//    of a slot loads zeros past the slot's end and its stores are clipped.
+//    each CTA's tensor memory receives its own 128 rows of the result.  This replaces the counter-gated cuBLAS
+//    atomic GEMM of the same listing.  For GEMM+RS / GEMM+AR the K loop of a
+//    tile walks the ranks' K-slices in a fixed ring order into one accumulator.
 //
 // Every wait (mbarrier, chunk counter) is bounded by the device global timer.
 // On expiry the waiting thread records the failure in the context's error word
@@ -255,18 +250,22 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+// Loads 32 columns of the warp's 32 tensor-memory lanes and waits for them in
+// one statement: the compiler never sees the registers before the data landed
+// (a separate wait would let it copy them while the load is still in flight).
+__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
+      : "r"(taddr)
+      : "memory");
 }
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 
 __device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
@@ -818,8 +817,7 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
       // round the result to bf16 and store it.
       auto chunk = [&](int c, const uint32_t(&q)[32], bool have_q) {
         uint32_t r[32];
-        tmem_ld32(taddr + c * EPI_COLS, r);
-        tmem_wait_ld();
+        tmem_ld32_sync(taddr + c * EPI_COLS, r);
         if (c == BN / EPI_COLS - 1) {  // accumulator fully read: hand it back to the MMA issuer
           tc_fence_before();
           __syncwarp();

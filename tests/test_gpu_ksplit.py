@@ -279,3 +279,30 @@ def test_epilogue_reduction_modes(op, tp, n, k, m, chunks, dtype):
             assert e2 > 1.3 * e0, (e0, e2)
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("op,tp,n,k,m,chunks", [("ar", 4, 2056, 64, 272, 2), ("rs", 3, 390, 48, 24, 1),
+                                                ("ar", 2, 1024, 256, 512, 2)])
+def test_repeated_calls_bit_identical(op, tp, n, k, m, chunks):
+    """Every reduction mode and MMA variant gives the same bits call after call
+    (a race between the epilogue, the workspace and tensor memory would not)."""
+    wl = synth.make_ksplit(op, tp, n, k, m, seed=11, n_row_chunks=chunks, sigma=k ** -0.25)
+    run = KsplitRun(wl)
+    try:
+        for mode in (0, 1, 2):
+            t.tpo_set_opt(run.ctx, "reduce", mode)
+            for cg in (1, 2):
+                t.tpo_set_opt(run.ctx, "cta_group", cg)
+                first = None
+                for _ in range(8):
+                    try:
+                        run.rs() if op == "rs" else run.ar(chunks)
+                    except t.TpoError as e:
+                        assert cg == 2 and e.status == 2      # shape served by single-SM tiles only
+                        break
+                    bits = np.concatenate([host_bits(y) for y in run.yb], 0) if op == "rs" else host_bits(run.y)
+                    if first is None:
+                        first = bits
+                    assert np.array_equal(bits, first), (mode, cg)
+    finally:
+        run.close()
