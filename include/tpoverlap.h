@@ -130,7 +130,9 @@ tpo_status tpo_ag_gemm(tpo_ctx* ctx, const void* const* x, const void* w, void* 
  * the output rows owned by rank b accumulate ranks b+1, b+2, ..., b (mod tp),
  * the order of a ring reduce-scatter that ends at the owner, in fp32, with a
  * single rounding to bf16 in the epilogue.  e4m3 contexts take their scales
- * from tpo_set_fp8_scales.
+ * from tpo_set_fp8_scales.  Blocks are produced in order (block 0 first);
+ * after every tile of block b is stored, block b's done counter (see
+ * tpo_done_counters) reaches its target with release semantics.
  */
 tpo_status tpo_gemm_rs(tpo_ctx* ctx, const void* const* x, const void* const* w, void* const* y,
                        void* stream);
@@ -144,7 +146,7 @@ tpo_status tpo_gemm_rs(tpo_ctx* ctx, const void* const* x, const void* const* w,
  * chunk c, the rows of the chunk's i-th of tp equal parts sum ranks i+1, ...,
  * i (mod tp), the per-part order of a ring all-reduce of that chunk.  After
  * every tile of chunk c is stored, the chunk's done counter (see
- * tpo_ar_done_counters) reaches its target with release semantics.  e4m3
+ * tpo_done_counters) reaches its target with release semantics.  e4m3
  * contexts as tpo_gemm_rs.
  */
 tpo_status tpo_gemm_ar(tpo_ctx* ctx, const void* const* x, const void* const* w, void* y,
@@ -235,10 +237,17 @@ const char* tpo_last_error(void);
  * order), for inspection after a synchronised AG call. */
 const void* tpo_staging_ptr(tpo_ctx* ctx);
 
-/* Device pointer to the AR done counters (TPO_MAX_ROW_CHUNKS uint32 words) and
- * the value chunk c's counter reaches when the last tpo_gemm_ar call has
- * stored all of chunk c. */
-const uint32_t* tpo_ar_done_counters(tpo_ctx* ctx, uint32_t* target);
+/* Device pointer to the done counters (TPO_MAX_ROW_CHUNKS uint32 words), one
+ * per output group of the latest tpo_gemm_rs (group b = owner block y[b]) or
+ * tpo_gemm_ar (group c = row chunk c) call, and the value every group's counter
+ * reaches once that call has stored all of the group's rows.  The GEMM raises
+ * them with release semantics as it finishes each tile, so a consumer that
+ * acquire-loads a counter equal to *target may read the group's rows while
+ * the rest of the output is still being computed: the signal the
+ * communication side of an atomic GEMM+RS (or of a chunked all-reduce) waits
+ * on.  The counters restart from zero when the operation or the group count
+ * changes between calls. */
+const uint32_t* tpo_done_counters(tpo_ctx* ctx, uint32_t* target);
 
 /* Trace words (uint64 nanoseconds of the device global timer), valid after
  * tpo_sync_status when option "trace" was 1; reset by each traced call. */
@@ -247,7 +256,7 @@ const uint32_t* tpo_ar_done_counters(tpo_ctx* ctx, uint32_t* target);
 #define TPO_TRACE_PUBLISH 2    /* + slot: latest producer publish of the slot */
 #define TPO_TRACE_ACQUIRE 18   /* + slot: earliest GEMM acquire of the slot */
 #define TPO_TRACE_WAIT_NS 34   /* total ns GEMM CTAs spent waiting on counters */
-#define TPO_TRACE_CHUNK_DONE 35 /* + chunk: AR chunk completion time */
+#define TPO_TRACE_CHUNK_DONE 35 /* + group: completion time of an RS block / AR row chunk */
 /* Pipeline diagnosis (SM clock cycles summed over GEMM CTAs): */
 #define TPO_TRACE_CYC_TMA_EMPTY 100  /* TMA issuer blocked on a free stage */
 #define TPO_TRACE_CYC_MMA_FULL 101   /* MMA issuer blocked on a loaded stage */

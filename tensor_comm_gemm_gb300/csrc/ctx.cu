@@ -102,8 +102,9 @@ struct tpo_ctx {
   float* ws = nullptr;  // epilogue-reduction running sums, one BM x BN fp32 block per SM
   tpo::DevWords* words = nullptr;
   uint32_t target[TPO_MAX_TP] = {};  // per slot: counter value once the latest call published it
-  uint32_t ar_target = 0;  // AR done-counter value after the latest call
-  int ar_chunks = 0;       // row-chunk count of the latest AR call
+  uint32_t done_target = 0;  // RS/AR done-counter value after the latest call
+  int done_op = -1;          // operation and output-group count the done counters follow
+  int done_groups = 0;
   cudaStream_t aux = nullptr;
   cudaStream_t copy = nullptr;             // split mode: chunk copies run here
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_copy[TPO_MAX_TP] = {};
@@ -700,16 +701,19 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
   tpo_status st = reset_trace(c, s);
   if (st != TPO_OK) return st;
-  if (op == tpo::OP_AR) {
-    if (n_chunks != c->ar_chunks) {  // keep every chunk's done counter on the same target
-      cudaError_t e = cudaMemsetAsync(c->words->ar_done, 0, sizeof(c->words->ar_done), s);
+  {
+    // one done counter per output group (RS owner block, AR row chunk), all on
+    // the same target: restart them when the operation or the group count changes
+    if (op != c->done_op || groups != c->done_groups) {
+      cudaError_t e = cudaMemsetAsync(c->words->done, 0, sizeof(c->words->done), s);
       if (e != cudaSuccess) return cuda_fail(e, "done-counter reset");
-      c->ar_target = 0;
-      c->ar_chunks = n_chunks;
+      c->done_target = 0;
+      c->done_op = op;
+      c->done_groups = groups;
     }
     // one release per epilogue warp of every CTA of every tile of the chunk
-    c->ar_target += static_cast<uint32_t>(p.row_tiles * cg * p.col_tiles * tpo::EPI_WARPS);
-    p.ar_target = c->ar_target;
+    c->done_target += static_cast<uint32_t>(p.row_tiles * cg * p.col_tiles * tpo::EPI_WARPS);
+    p.done_target = c->done_target;
   }
   p.num_producers = 0;
   p.num_gemm = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms, 0, tiles);
@@ -767,8 +771,9 @@ tpo_status tpo_sync_status(tpo_ctx* c) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->aux);
   if (e != cudaSuccess) return cuda_fail(e, "reset after device failure");
   std::memset(c->target, 0, sizeof(c->target));
-  c->ar_target = 0;
-  c->ar_chunks = 0;
+  c->done_target = 0;
+  c->done_op = -1;
+  c->done_groups = 0;
   return fail(TPO_ERR_TIMEOUT, "device wait timed out (site %u, block %u, extra %u)", err[1], err[2], err[3]);
 }
 
@@ -780,10 +785,10 @@ tpo_status tpo_last_device_error(tpo_ctx* c, uint32_t out[4]) {
 
 const void* tpo_staging_ptr(tpo_ctx* c) { return c ? c->staging : nullptr; }
 
-const uint32_t* tpo_ar_done_counters(tpo_ctx* c, uint32_t* target) {
+const uint32_t* tpo_done_counters(tpo_ctx* c, uint32_t* target) {
   if (!c) return nullptr;
-  if (target) *target = c->ar_target;
-  return c->words->ar_done;
+  if (target) *target = c->done_target;
+  return c->words->done;
 }
 
 tpo_status tpo_read_trace(tpo_ctx* c, uint64_t* out, int cap) {

@@ -892,11 +892,11 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
         for (int c = 0; c < BN / EPI_COLS; ++c) chunk(c, none, false);
       }
     }
-    if (ok_all && p.op == OP_AR && lane == 0) {  // this warp's rows of the tile are in memory: count them
+    if (ok_all && p.op != OP_AG && lane == 0) {  // this warp's rows of the tile are in memory: count them
       bulk_wait<0>();
       fence_proxy_async_global();
-      const uint32_t old = atom_add_release(&p.words->ar_done[T.group], 1u);
-      if (p.trace_on && old + 1u == p.ar_target) p.words->trace[TPO_TRACE_CHUNK_DONE + T.group] = gtime();
+      const uint32_t old = atom_add_release(&p.words->done[T.group], 1u);
+      if (p.trace_on && old + 1u == p.done_target) p.words->trace[TPO_TRACE_CHUNK_DONE + T.group] = gtime();
     }
   }
   if (lane == 0) bulk_wait<0>();

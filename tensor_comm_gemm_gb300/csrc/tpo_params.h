@@ -77,7 +77,7 @@ enum Site : uint32_t {
 struct DevWords {
   uint32_t counters[TPO_MAX_TP];        // per-slot chunk counters (monotonic)
   uint32_t err[4];
-  uint32_t ar_done[TPO_MAX_ROW_CHUNKS]; // per-row-chunk done counters (monotonic)
+  uint32_t done[TPO_MAX_ROW_CHUNKS];    // per output group done counters (RS owner block, AR row chunk; monotonic)
   uint32_t pad[12];
   unsigned long long trace[TPO_TRACE_WORDS];
 };
@@ -98,7 +98,7 @@ struct Params {
   unsigned long long timeout_ns;
   unsigned long long delay_ns;
   uint32_t target[TPO_MAX_TP];  // per slot: counter value once this call has published it
-  uint32_t ar_target;     // AR done-counter value once this call stored the chunk
+  uint32_t done_target;   // RS/AR done-counter value once this call stored the whole group
   uint32_t pad1;
   int op;
   int fp8;

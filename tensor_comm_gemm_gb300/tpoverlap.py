@@ -28,7 +28,7 @@ TPO_MAX_TP, TPO_MAX_ROW_CHUNKS = 16, 64
 # Every symbol the public header declares.
 EXPORTS = ["tpo_ctx_create", "tpo_ctx_destroy", "tpo_ag_gemm", "tpo_gemm_rs", "tpo_gemm_ar", "tpo_set_opt",
            "tpo_get_opt", "tpo_sync_status", "tpo_last_device_error", "tpo_last_error", "tpo_staging_ptr",
-           "tpo_ar_done_counters", "tpo_read_trace", "tpo_version", "tpo_ag_gemm_noalloc", "tpo_set_fp8_scales"]
+           "tpo_done_counters", "tpo_read_trace", "tpo_version", "tpo_ag_gemm_noalloc", "tpo_set_fp8_scales"]
 TPO_NOALLOC_MAX_STAGING_BYTES = 32 << 20
 
 
@@ -65,8 +65,8 @@ def lib(path: Optional[str] = None):
     L.tpo_last_error.restype = ctypes.c_char_p
     L.tpo_staging_ptr.argtypes = [p]
     L.tpo_staging_ptr.restype = p
-    L.tpo_ar_done_counters.argtypes = [p, u32p]
-    L.tpo_ar_done_counters.restype = p
+    L.tpo_done_counters.argtypes = [p, u32p]
+    L.tpo_done_counters.restype = p
     L.tpo_read_trace.argtypes = [p, ctypes.POINTER(ctypes.c_uint64), i32]
     L.tpo_version.restype = ctypes.c_char_p
     L.tpo_ag_gemm_noalloc.argtypes = [i32, i64, i64, i64, i32, p, p, p, p, p, p]
@@ -226,9 +226,9 @@ def tpo_staging_ptr(ctx: int) -> int:
     return lib().tpo_staging_ptr(ctx) or 0
 
 
-def tpo_ar_done_counters(ctx: int):
+def tpo_done_counters(ctx: int):
     t = ctypes.c_uint32()
-    p = lib().tpo_ar_done_counters(ctx, ctypes.byref(t))
+    p = lib().tpo_done_counters(ctx, ctypes.byref(t))
     return (p or 0), t.value
 
 

@@ -54,7 +54,7 @@ def test_ar_full_parity_and_done_counters(tp, n, k, m, chunks):
             t.tpo_set_opt(run.ctx, "trace", 1)
             run.ar(chunks)
             assert_close(host_f64(run.y), ref)
-            ptr, target = t.tpo_ar_done_counters(run.ctx)
+            ptr, target = t.tpo_done_counters(run.ctx)
             if rep == 0:
                 first_target = target
             assert target == (rep + 1) * first_target and target > 0   # the same increment per call
@@ -304,5 +304,36 @@ def test_repeated_calls_bit_identical(op, tp, n, k, m, chunks):
                     if first is None:
                         first = bits
                     assert np.array_equal(bits, first), (mode, cg)
+    finally:
+        run.close()
+
+
+def test_rs_done_counters_per_block_and_restart():
+    """GEMM+RS raises one done counter per owner block; switching between RS
+    and AR (a different group count) restarts the counters from zero."""
+    wl = synth.make_ksplit("rs", 4, 2048, 512, 512, seed=17, dist="uniform")
+    run = KsplitRun(wl)
+    try:
+        t.tpo_set_opt(run.ctx, "trace", 1)
+        targets = []
+        for rep in range(2):
+            run.rs()
+            ptr, target = t.tpo_done_counters(run.ctx)
+            targets.append(target)
+            cnt = np.frombuffer(_read_device_words(ptr, 4), dtype=np.uint32)
+            assert np.all(cnt == target) and target > 0
+            tr = t.tpo_read_trace(run.ctx)
+            done = [tr[t.TPO_TRACE_CHUNK_DONE + b] for b in range(4)]
+            assert all(d > 0 for d in done)
+        assert targets[1] == 2 * targets[0]
+        run.ar(2)                                   # 2 row chunks: counters restart
+        ptr, target = t.tpo_done_counters(run.ctx)
+        cnt = np.frombuffer(_read_device_words(ptr, 4), dtype=np.uint32)
+        assert np.all(cnt[:2] == target) and np.all(cnt[2:] == 0)
+        run.rs()                                    # back to 4 blocks: restart again
+        ptr, target = t.tpo_done_counters(run.ctx)
+        assert target == targets[0]
+        cnt = np.frombuffer(_read_device_words(ptr, 4), dtype=np.uint32)
+        assert np.all(cnt == target)
     finally:
         run.close()

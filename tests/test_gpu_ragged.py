@@ -143,7 +143,7 @@ def test_ksplit_ragged_parity(op, tp, n, k, m, chunks, dtype):
             assert t.tpo_sync_status(run.ctx) == 0, t.tpo_last_error()
             assert out.guards_intact()
             got = host_f64(out.y)
-            ptr, target = t.tpo_ar_done_counters(run.ctx)
+            ptr, target = t.tpo_done_counters(run.ctx)
             cnt = torch.as_tensor(_Words(ptr, chunks), device="cuda").cpu().numpy()
             assert target > 0 and np.all(cnt == target), (cnt, target)
         assert_close(got, ref, dtype)
