@@ -505,6 +505,18 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
                "frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / pk, 4), "peak_tflops": pk}
         if dt == "e4m3" and fp8_lib:
             rec["frac_of_library_fp8"] = round(flops / (ms * 1e-3) / 1e12 / fp8_lib, 4)
+        if op in ("rs", "ar"):
+            # when each output group (RS owner block, AR row chunk) was complete, as a
+            # fraction of the call: the point at which its communication could start
+            t.tpo_set_opt(ctx, "trace", 1)
+            fn()
+            check(ctx)
+            tr = t.tpo_read_trace(ctx)
+            t.tpo_set_opt(ctx, "trace", 0)
+            span = max(1, tr[t.TPO_TRACE_END] - tr[t.TPO_TRACE_START])
+            groups = tp if op == "rs" else ch
+            rec["group_done_frac"] = [round((tr[t.TPO_TRACE_CHUNK_DONE + gi] - tr[t.TPO_TRACE_START]) / span, 3)
+                                      for gi in range(groups)]
         if op == "rs":  # the same call with the ranks' partials added in the epilogue
             for rmode, key in ((1, "epilogue_fp32"), (2, "epilogue_bf16_wire")):
                 t.tpo_set_opt(ctx, "reduce", rmode)
