@@ -46,7 +46,9 @@ class Guarded:
 # 256 (nor of 32), k not a whole 128-byte block; the smallest legal sizes
 AG_RAGGED = [(3, 600, 200, 264, "bf16"), (2, 1000, 48, 520, "e4m3"), (5, 5, 8, 8, "bf16"),
              (4, 1200, 1000, 1000, "bf16"), (1, 130, 24, 40, "bf16"), (16, 16 * 70, 80, 136, "e4m3"),
-             (2, 2 * 640, 264, 776, "bf16")]
+             (2, 2 * 640, 264, 776, "bf16"),
+             # whole 256-row slots (CTA pairs) with partial column and K tiles
+             (2, 1024, 200, 520, "bf16"), (4, 2048, 144, 264, "e4m3")]
 
 
 @pytest.mark.parametrize("tp,n,k,m,dtype", AG_RAGGED)
@@ -105,7 +107,9 @@ def test_ag_noalloc_ragged_matches_context_path():
 KSPLIT_RAGGED = [("rs", 3, 390, 48, 24, 1, "bf16"), ("rs", 2, 1030, 96, 776, 1, "bf16"),
                  ("rs", 4, 4 * 300, 4 * 208, 520, 1, "e4m3"), ("ar", 2, 600, 32, 40, 3, "bf16"),
                  ("ar", 4, 2056, 64, 272, 2, "bf16"), ("ar", 3, 3 * 2 * 90, 3 * 48, 264, 2, "e4m3"),
-                 ("ar", 2, 2 * 700, 2 * 136, 1000, 1, "bf16")]
+                 ("ar", 2, 2 * 700, 2 * 136, 1000, 1, "bf16"),
+                 # CTA pairs with partial column and K tiles
+                 ("rs", 2, 1024, 2 * 104, 520, 1, "bf16"), ("ar", 2, 2048, 2 * 72, 264, 2, "bf16")]
 
 
 @pytest.mark.parametrize("op,tp,n,k,m,chunks,dtype", KSPLIT_RAGGED)
