@@ -661,7 +661,8 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
     key[nkey++] = (op == tpo::OP_RS) ? yb[r] : nullptr;
   }
   key[nkey++] = y;
-  key[nkey++] = reinterpret_cast<const void*>(static_cast<intptr_t>(cg));
+  // the MMA variant sets the W box; the AR output map's part rows follow the chunk count
+  key[nkey++] = reinterpret_cast<const void*>(static_cast<intptr_t>(cg * 1000 + groups));
   const bool fp8 = c->dtype == TPO_FP8_E4M3;
   const int elem = fp8 ? 1 : 2;
   const int kel = tpo::BK_BYTES / elem;

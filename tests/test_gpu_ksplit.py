@@ -337,3 +337,24 @@ def test_rs_done_counters_per_block_and_restart():
         assert np.all(cnt == target)
     finally:
         run.close()
+
+
+def test_ar_chunk_count_changes_on_one_context():
+    """The same context and buffers called with different row-chunk counts
+    (each count its own part layout of the output) gives the right result
+    every time, and the same bits whenever a count comes back."""
+    wl = synth.make_ksplit("ar", 2, 2048, 512, 512, seed=23, dist="uniform")
+    ref = oracle.ksplit(wl.x, wl.w)
+    run = KsplitRun(wl)
+    try:
+        seen = {}
+        for chunks in (1, 4, 2, 8, 1, 4):
+            run.y.fill_(float("nan"))
+            run.ar(chunks)
+            assert_close(host_f64(run.y), ref)
+            bits = host_bits(run.y)
+            if chunks in seen:
+                assert np.array_equal(bits, seen[chunks]), chunks
+            seen[chunks] = bits
+    finally:
+        run.close()
