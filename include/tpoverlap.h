@@ -279,9 +279,9 @@ const char* tpo_version(void);
  * only owns the buffers it is handed.  tpo_ctx_create allocates, so these
  * callers cannot hold a context.
  *
- * Computes exactly what tpo_ag_gemm computes with a context's default options
- * (overlapped schedule, observer rank 0, 8 producer CTAs, 2 s wait bound); the
- * result is bit-identical to it.  Arguments as tpo_ctx_create (tp, n, k, m,
+ * Computes what tpo_ag_gemm computes for observer rank 0 in one overlapped
+ * launch (8 producer CTAs, single-SM 128 x 256 tiles, 2 s wait bound); the
+ * result is bit-identical to tpo_ag_gemm's in every mode and MMA variant.  Arguments as tpo_ctx_create (tp, n, k, m,
  * dtype) plus tpo_ag_gemm (x, w, y, scale_inv pointers, stream).
  *
  * Scratch (the gathered staging buffer, the chunk counters and the error word)
