@@ -448,6 +448,29 @@ def cublas_fp8_tflops(torch, dev, size=8192):
         return None
 
 
+def library_gemm_4096(torch, dev, sets=3, calls=60):
+    """The vendor library's plain bf16 GEMM (torch.matmul) on the headline's
+    4096^3 shape, rotating over input sets as the headline does: the GEMM alone,
+    with no chunk movement, for context beside the overlapped call."""
+    try:
+        xs = [torch.randn(4096, 4096, device=dev, dtype=torch.bfloat16) for _ in range(sets)]
+        ws = [torch.randn(4096, 4096, device=dev, dtype=torch.bfloat16) for _ in range(sets)]
+        ys = [torch.empty(4096, 4096, device=dev, dtype=torch.bfloat16) for _ in range(sets)]
+        for i in range(6):
+            torch.matmul(xs[i % sets], ws[i % sets].t(), out=ys[i % sets])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for i in range(calls):
+            torch.matmul(xs[i % sets], ws[i % sets].t(), out=ys[i % sets])
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / calls
+        return {"ms": round(ms, 5), "tflops": round(2.0 * 4096 ** 3 / (ms * 1e-3) / 1e12, 1)}
+    except Exception:  # noqa: BLE001
+        return None
+
+
 def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
     out = {}
     steps = min(40, max(5, args.steps // 2))
@@ -471,6 +494,7 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
                     "us_per_call_python": round(ms_py * 1e3, 2),
                     "tflops": round(synth.flops(0) / (ms * 1e-3) / 1e12, 3)}
     t.tpo_ctx_destroy(ctx)
+    out["library_bf16_gemm_4096"] = library_gemm_4096(torch, dev)
     fp8_lib = cublas_fp8_tflops(torch, dev)
     out["fp8_library_gemm_8192"] = {"tflops": fp8_lib, "note": "torch._scaled_mm e4m3 8192^3 burst on this "
                                     "box; the FP8 rows' frac_of_peak uses 2 x the measured bf16 peak"}
