@@ -391,15 +391,28 @@ struct Tile {
 };
 
 // Tiles are ordered group by group (AG: ring step, RS: owner block, AR: row
-// chunk); inside a group column-tile-major so that consecutive CTAs share the
-// same W tile.  Every role of a CTA walks the same sequence t = g, g+G, ...
+// chunk).  Inside a group, blocks of up to 2048 rows are swept column tile by
+// column tile, rows fastest: consecutive CTAs share a W tile, and a block's
+// rows of X stay in L2 while its sweep passes over all of W (a group with
+// more rows would otherwise stream X from memory once per column tile).
+// Every role of a CTA walks the same sequence t = g, g+G, ...
 template <int TILE_M>
 __device__ __forceinline__ Tile tile_at(const Params& p, int t) {
+  constexpr int RB = 2048 / TILE_M;  // row tiles per swept block
   const int per_group = p.row_tiles * p.col_tiles;
   const int grp = t / per_group;
   const int rem = t - grp * per_group;
-  const int c = rem / p.row_tiles;
-  const int r = rem - c * p.row_tiles;
+  const int full = p.row_tiles / RB;      // whole blocks of RB row tiles
+  int c, r;
+  if (rem < full * RB * p.col_tiles) {
+    const int b = rem / (RB * p.col_tiles), w = rem - b * RB * p.col_tiles;
+    c = w / RB;
+    r = b * RB + (w - c * RB);
+  } else {                                // the last, shorter block
+    const int h = p.row_tiles - full * RB, w = rem - full * RB * p.col_tiles;
+    c = w / h;
+    r = full * RB + (w - c * h);
+  }
   Tile T;
   T.col = c * BN;
   T.group = grp;

@@ -25,7 +25,16 @@ def tile_at(op, tp, self_rank, pl, t):
     row_tiles, col_tiles, tile_m, rpg = pl["row_tiles"], pl["col_tiles"], pl["tile_m"], pl["rows_per_group"]
     per = row_tiles * col_tiles
     grp, rem = divmod(t, per)
-    c, r = divmod(rem, row_tiles)
+    rb = 2048 // tile_m                    # row tiles per block swept column by column
+    full = row_tiles // rb
+    if rem < full * rb * col_tiles:
+        b, w = divmod(rem, rb * col_tiles)
+        c, rr0 = divmod(w, rb)
+        r = b * rb + rr0
+    else:
+        h = row_tiles - full * rb
+        c, rr0 = divmod(rem - full * rb * col_tiles, h)
+        r = full * rb + rr0
     col = c * BN
     if op == "ag":
         slot = (self_rank - grp) % tp
@@ -67,7 +76,10 @@ SHAPES = [("ag", 2, 256, 256, 256, 2, 1), ("ag", 4, 4096, 4096, 4096, 2, 1), ("a
           # ragged: partial row tiles, partial column tiles, partial K blocks
           ("ag", 3, 600, 200, 264, 2, 1), ("ag", 2, 1000, 48, 520, 1, 1), ("ag", 5, 5, 8, 8, 2, 1),
           ("rs", 3, 390, 48, 24, 2, 1), ("rs", 2, 1030, 96, 776, 1, 1),
-          ("ar", 2, 600, 32, 40, 2, 3), ("ar", 4, 2056, 64, 272, 2, 2)]
+          ("ar", 2, 600, 32, 40, 2, 3), ("ar", 4, 2056, 64, 272, 2, 2),
+          # groups of more than 2048 rows: several swept blocks, the last one shorter
+          ("ag", 1, 8192, 128, 512, 2, 1), ("ag", 2, 2 * 5000, 64, 264, 2, 1), ("rs", 2, 2 * 2304, 64, 512, 2, 1),
+          ("ar", 1, 5000, 64, 264, 2, 1)]
 
 
 @pytest.mark.parametrize("op,tp,n,k,m,elem,chunks", SHAPES)
