@@ -166,9 +166,27 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
 /*
  * Options (integers).  Keys:
  *   "producer_sms"     CTAs given to the chunk producer in overlapped AG; 0 (the
- *                      default) picks the largest count in [8, 32] that does not
- *                      add a round of GEMM tiles (rounded up to even for pairs)
+ *                      default) picks the largest count in [8, 32] that does
+ *                      not add a round of GEMM tiles (rounded up to even for
+ *                      pairs); with tail_split 1, the smallest count from 4
+ *                      whose copy stays ahead of the GEMM by a model of both
+ *                      rates
  *   "gemm_ctas"        CTAs given to the GEMM (0 = all SMs not producing)
+ *   "tail_split"       AG, modes 0-2 (default 0: whole tiles only, and every
+ *                      grid, mode and producer count gives the same bits).
+ *                      1: the tiles left over after the GEMM CTAs' whole
+ *                      rounds go first and are divided along K among them;
+ *                      2: the producer CTAs join the GEMM once their copy is
+ *                      done, and the last tiles are divided along K between
+ *                      the GEMM CTAs (a short share each) and them (the rest),
+ *                      sized from a model of both rates.  Each later K part of
+ *                      a split tile is an fp32 partial in the context's
+ *                      workspace, added in K order to the first part before
+ *                      the bf16 rounding, so the result depends on the plan:
+ *                      modes 1 and 2 then run mode 0's launch shape and plan
+ *                      (same bits in all three); other producer counts,
+ *                      gemm_ctas values and mode 4 (never split) may round
+ *                      split tiles differently.
  *   "mode"             AG schedule: 0 overlapped (one launch, producer and GEMM
  *                      co-resident), 1 sequential (copy to completion, then the
  *                      same GEMM), 2 GEMM only (staging and counters must hold a
@@ -189,6 +207,9 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *   "debug_delay_ns"   producer spin before each publish
  *   "debug_last_step"  mode 3 only: the producer stops after this ring step
  *                      (-1 = all steps)
+ *   "debug_skip_partial" GEMM CTA (index among the GEMM CTAs) that never
+ *                      publishes its split-tile partial (-1 off): the tile's
+ *                      finisher times out
  *   "cta_group"        MMA variant: 0 automatic, 1 single-SM 128x256 tiles,
  *                      2 CTA pairs (2-SM MMA, 256x256 tiles; needs every tile
  *                      group a multiple of 256 rows).  Results are identical.
@@ -211,8 +232,8 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      (one 128 x 256 block per SM, fp32 in mode 1, bf16 in
  *                      mode 2), so the MMAs never wait for the additions.
  * Read-only keys for tpo_get_opt: "last_producer_ctas", "last_gemm_ctas",
- * "last_cta_group" (shape of the context's latest kernel launch: producer
- * CTAs, GEMM CTAs, 1 or 2 CTAs per MMA),
+ * "last_cta_group", "last_split_tiles" (shape of the context's latest kernel
+ * launch: producer CTAs, GEMM CTAs, 1 or 2 CTAs per MMA, tiles split along K),
  * "coop_clusters" (0 once the driver refused a cooperative cluster launch),
  * "tp", "n", "k", "m", "dtype" (the sizes the context was created for).
  * Environment variables TPO_<KEY in upper case> override the defaults at

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cctype>
 #include <cstdarg>
 #include <cstddef>
@@ -95,7 +96,7 @@ struct tpo_ctx {
   // options
   int64_t producer_sms = 0, gemm_ctas = 0, mode = 0, seq_copy_ctas = 0, self_rank = 0, wait_timeout_ms = 2000,
           trace = 0, debug_skip_chunk = -1, debug_delay_ns = 0, debug_last_step = -1, cta_group = 0,
-          cooperative = 1, reduce = 0;
+          cooperative = 1, reduce = 0, tail_split = 0, debug_skip_partial = -1;
   // device memory
   uint8_t* staging = nullptr;
   size_t staging_bytes = 0;
@@ -114,6 +115,9 @@ struct tpo_ctx {
   const float* ks_scale_x = nullptr;  // e4m3 RS/AR scale_inv pointers (tpo_set_fp8_scales)
   const float* ks_scale_w = nullptr;
   int64_t last_producers = 0, last_gemm_ctas = 0, last_cta_group = 0;  // shape of the latest kernel launch
+  int64_t last_split_tiles = 0;  // tail tiles of the latest kernel launch (AG tail split)
+  int64_t last_late_groups = 0;  // producer CTA groups that joined its GEMM
+  uint32_t part_epoch = 0;       // launches with the AG tail split so far (part_ready value of this launch)
   // tensor-map cache: the maps of the latest kCacheWays pointer sets of each op
   static constexpr int kCacheWays = 4;
   struct MapSet {
@@ -147,6 +151,8 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
       {"cta_group", &tpo_ctx::cta_group, 0, 2},
       {"cooperative", &tpo_ctx::cooperative, 0, 1},
       {"reduce", &tpo_ctx::reduce, 0, 2},
+      {"tail_split", &tpo_ctx::tail_split, 0, 2},
+      {"debug_skip_partial", &tpo_ctx::debug_skip_partial, -1, tpo::MAX_GEMM_CTAS - 1},
   };
   for (const E& e : table)
     if (std::strcmp(e.k, key) == 0) {
@@ -163,7 +169,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
 const char* kOptKeys[] = {"producer_sms",     "gemm_ctas",      "mode",           "seq_copy_ctas",
                           "self_rank",        "wait_timeout_ms", "trace",          "debug_skip_chunk",
                           "debug_delay_ns",   "debug_last_step", "cta_group",      "cooperative",
-                          "reduce"};
+                          "reduce",           "tail_split",     "debug_skip_partial"};
 
 void destroy_all(tpo_ctx* c) {
   if (!c) return;
@@ -210,6 +216,10 @@ tpo_status launch(tpo_ctx* c, const Params& p, int grid, bool coop, cudaStream_t
   c->last_producers = p.num_producers;
   c->last_gemm_ctas = p.num_gemm;
   c->last_cta_group = p.cta_group;
+  c->last_split_tiles = 0;
+  c->last_late_groups = p.late_groups;
+  if (p.tail_split && p.num_gemm > 0)
+    c->last_split_tiles = p.num_groups * p.row_tiles * p.col_tiles - p.split_full * (p.num_gemm / p.cta_group);
   if (coop && (!c->cooperative || (p.cta_group == 2 && !c->coop_clusters))) coop = false;
   cudaError_t e = tpo::launch_fused(p, grid, coop, s);
   if (e != cudaSuccess && coop && p.cta_group == 2) {
@@ -291,12 +301,43 @@ int gemm_grid(const tpo_ctx* c, int cg, int64_t want, int producers, int tiles) 
   return static_cast<int>(2 * pairs);
 }
 
-// Producer CTAs of an overlapped AG call.  An explicit option wins; otherwise
-// the largest count in [8, 32] that leaves the GEMM as many rounds of tiles as
-// 8 producers would: with whole rounds, SMs beyond the last full round are
-// free for copying, and more producers publish every ring chunk sooner.
-int producer_count(const tpo_ctx* c, int cg, int tiles) {
+// Producer CTAs of an overlapped AG call.  An explicit option wins.
+//
+// With the tail split every GEMM group shortens the GEMM, so the count is the
+// smallest (from 4) that keeps the copy ahead of it.  Each gathered chunk must
+// land before the GEMM reaches its first tile, with 15% to spare, and the
+// whole staging copy (own chunk last) within 90% of the GEMM.  The model: a
+// producer CTA moves about 47 GB/s of chunk data (94 GB/s of HBM reads and
+// writes, whatever its depth of copies in flight), and a CTA group spends
+// about 0.3 us per 128-byte K block of a tile.
+//
+// Without it (or when no count passes), whole rounds decide: the largest count
+// in [8, 32] that leaves the GEMM as many rounds of tiles as 8 producers would,
+// since SMs beyond the last full round are free for copying.
+int producer_count(const tpo_ctx* c, int cg, int tiles, int nkb, int64_t chunk_bytes, bool split) {
   if (c->producer_sms > 0) return static_cast<int>(c->producer_sms) + ((cg == 2) ? static_cast<int>(c->producer_sms & 1) : 0);
+  if (split) {
+    const double rate = 47e9, t_tile = nkb * 0.3e-6;
+    const int per_group = tiles / c->tp;
+    for (int P = 4; P <= 32 && P < c->num_sms - 2 * cg; P += cg) {
+      const int G = gemm_grid(c, cg, c->num_sms - P, P, tiles) / cg;
+      const int R = tiles % G, gt = R ? std::min(G, tpo::TAIL_SPLIT * R) : 0;
+      const double tau = static_cast<double>(chunk_bytes) / (P * rate);
+      bool ok = c->tp * tau <= 0.9 * (static_cast<double>(tiles) / G) * t_tile;
+      for (int j = 1; j < c->tp && ok; ++j) {  // ring step j's chunk: first tile j * per_group
+        const int f = j * per_group;
+        if (f < R) {
+          ok = false;  // a split tile, needed from the start
+          break;
+        }
+        // whole round r after the split tiles; groups with split work start it R / gt tiles late
+        const int r = (f - R) / G, sl = (f - R) % G;
+        const double start = r + ((gt > 0 && sl >= G - gt) ? static_cast<double>(R) / gt : 0.0);
+        ok = j * tau <= 0.85 * start * t_tile;
+      }
+      if (ok) return P;
+    }
+  }
   auto rounds = [&](int P) {
     const int units = gemm_grid(c, cg, c->num_sms - P, P, tiles) / cg;
     return (tiles + units - 1) / units;
@@ -306,6 +347,60 @@ int producer_count(const tpo_ctx* c, int cg, int tiles) {
   for (int P = 8; P <= 32 && P < c->num_sms - 2 * cg; P += cg)
     if (rounds(P) == r8) best = P;
   return best;
+}
+
+// Tail-split plan of an AG GEMM launch (see SegIter in the kernel) with G GEMM
+// groups and L producer groups that join once their copy is done.
+//
+// With L > 0 the plan expects the copy of all tp chunks to end after
+// tp * chunk_bytes / (P * 31 GB/s) plus 3 us (a producer CTA's copy rate next
+// to a running GEMM), plans for 1.2 times that, and counts 0.36 us per
+// 128-byte K block of a tile: from these, the work is cut so that GEMM and
+// late groups end together.  A late start planned too early would make the
+// late groups end last, hence the margin; planned too late, they idle at the
+// end instead.  The plan only moves time: any plan gives exact tiles.
+//
+// With L == 0 (or no time for the late groups) the R = T mod G leftover tiles
+// go first and are shared among min(G, TAIL_SPLIT R) GEMM groups.
+void plan_split(const tpo_ctx* c, Params& p, int tiles, int G, int L) {
+  const long long kbu = p.kb_per_seg / p.kps;  // K units of a tile (AG: one K segment)
+  p.tail_split = 0;
+  p.late_groups = 0;
+  if (G < 1 || kbu < 1) return;
+  if (L > 0) {
+    const int P = L * p.cta_group;
+    const double t_copy = c->tp * static_cast<double>(p.chunk_bytes) / (P * 31e9) + 3e-6;
+    const double late = 1.2 * t_copy / (p.kps * 0.36e-6);  // planned late start, in K units
+    const double E = (static_cast<double>(tiles) * kbu + L * late) / (G + L);  // units per GEMM group
+    if (E > late + 1.0) {
+      int full = static_cast<int>(E / kbu);
+      if (full > tiles / G) full = tiles / G;
+      const long long wt = static_cast<long long>(tiles - full * G) * kbu;
+      long long sm = static_cast<long long>(E - static_cast<double>(full) * kbu);
+      if (sm < 0) sm = 0;
+      if (sm * G > wt) sm = wt / G;
+      if (wt - sm * G > 0) {
+        p.tail_split = 1;
+        p.split_tail_first = 0;
+        p.split_full = full;
+        p.split_ga = G;
+        p.split_wa = sm * G;
+        p.split_gb = L;
+        p.split_wb = wt - sm * G;
+        p.late_groups = L;
+        return;
+      }
+    }
+  }
+  const int full = tiles / G, R = tiles - full * G;
+  if (R == 0) return;
+  p.tail_split = 1;
+  p.split_tail_first = 1;
+  p.split_full = full;
+  p.split_ga = std::min(G, tpo::TAIL_SPLIT * R);
+  p.split_wa = static_cast<long long>(R) * kbu;
+  p.split_gb = 0;
+  p.split_wb = 0;
 }
 
 // Validation shared by RS and AR.
@@ -479,6 +574,8 @@ tpo_status tpo_get_opt(tpo_ctx* c, const char* key, int64_t* value) {
   if (std::strcmp(key, "last_producer_ctas") == 0) return *value = c->last_producers, TPO_OK;
   if (std::strcmp(key, "last_gemm_ctas") == 0) return *value = c->last_gemm_ctas, TPO_OK;
   if (std::strcmp(key, "last_cta_group") == 0) return *value = c->last_cta_group, TPO_OK;
+  if (std::strcmp(key, "last_split_tiles") == 0) return *value = c->last_split_tiles, TPO_OK;
+  if (std::strcmp(key, "last_late_groups") == 0) return *value = c->last_late_groups, TPO_OK;
   if (std::strcmp(key, "coop_clusters") == 0) return *value = c->coop_clusters ? 1 : 0, TPO_OK;
   if (std::strcmp(key, "tp") == 0) return *value = c->tp, TPO_OK;
   if (std::strcmp(key, "n") == 0) return *value = c->n, TPO_OK;
@@ -520,6 +617,8 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   base_params(c, p);
   p.op = tpo::OP_AG;
   p.cta_group = cg;
+  p.ws = c->ws;
+  p.skip_part = static_cast<int>(c->debug_skip_partial);
   const void* key[5] = {c->staging, x[c->self_rank], w, y, reinterpret_cast<const void*>(static_cast<intptr_t>(cg))};
   if (!cache_lookup(c, tpo::OP_AG, key, 5, p)) {
     const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -551,17 +650,38 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   tpo_status st = reset_trace(c, s);
   if (st != TPO_OK) return st;
   const int64_t gemm_want = c->gemm_ctas ? c->gemm_ctas : c->num_sms;
+  // The tail split (modes 0, 1, 2) stores partials in the workspace (one block
+  // per GEMM CTA).  Its sums depend on the launch shape and the plan, so modes
+  // 1 and 2 run the GEMM with mode 0's groups and plan (the producer CTAs
+  // then skip the copy and run their share at once): all three give the same
+  // bits.
+  const int split = (c->mode == 0 || c->mode == 1 || c->mode == 2) ? static_cast<int>(c->tail_split) : 0;
+  const int nkb = p.kb_per_seg;
+  auto overlap_grid = [&](int* P, int* G) {
+    *P = producer_count(c, cg, tiles, nkb, p.chunk_bytes, split == 1);  // even for CTA pairs: clusters of two
+    *G = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - *P, *P, tiles);
+  };
+  // The GEMM launch of modes 0-2 with G GEMM CTAs and P producer CTAs.
+  auto gemm_launch = [&](int P, int G, bool copy, bool coop) {
+    p.num_producers = P;
+    p.num_gemm = G;
+    p.copy_on = copy ? 1 : 0;
+    if (split && P + G <= c->num_sms && P + G <= tpo::MAX_GEMM_CTAS)
+      plan_split(c, p, tiles, G / cg, split == 2 ? P / cg : 0);
+    if (p.tail_split) p.part_target = ++c->part_epoch;
+    if (!copy && !p.late_groups) p.num_producers = 0;  // nothing for the producer CTAs to do
+    const int grid = p.num_producers + p.num_gemm;
+    return launch(c, p, grid, coop || p.tail_split != 0, s);  // split tiles: every CTA co-resident
+  };
   switch (c->mode) {
     case 0: {  // overlapped: one cooperative launch, producer and GEMM co-resident
-      const int P = producer_count(c, cg, tiles);  // even for CTA pairs: clusters of two
-      const int G = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, P, tiles);
+      int P, G;
+      overlap_grid(&P, &G);
       if (P < 1 || c->num_sms - P < cg || P + G > c->max_coop_grid)
         return fail(TPO_ERR_INVALID_ARG, "producer_sms=%d + gemm CTAs=%d exceed the %d co-resident CTAs", P, G,
                     c->max_coop_grid);
       advance_targets(c, p, P);
-      p.num_producers = P;
-      p.num_gemm = G;
-      return launch(c, p, P + G, true, s);
+      return gemm_launch(P, G, true, true);
     }
     case 1: {  // sequential: the copy to completion, then the same GEMM
       const int Pc = static_cast<int>(c->seq_copy_ctas ? c->seq_copy_ctas : c->num_sms);
@@ -572,18 +692,18 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       st = launch(c, p, Pc, false, s);
       if (st != TPO_OK) return st;
       p.cta_group = cg;
-      p.num_producers = 0;
-      p.num_gemm = gemm_grid(c, cg, gemm_want, 0, tiles);
-      return launch(c, p, p.num_gemm, false, s);
+      int P = 0, G = gemm_grid(c, cg, gemm_want, 0, tiles);
+      if (split) overlap_grid(&P, &G);
+      return gemm_launch(P, G, false, false);
     }
     case 2: {  // GEMM only: chunks published by an earlier call
       std::memcpy(p.target, c->target, sizeof(p.target));
-      p.num_producers = 0;
-      p.num_gemm = gemm_grid(c, cg, gemm_want, 0, tiles);
-      return launch(c, p, p.num_gemm, false, s);
+      int P = 0, G = gemm_grid(c, cg, gemm_want, 0, tiles);
+      if (split) overlap_grid(&P, &G);
+      return gemm_launch(P, G, false, false);
     }
     case 4: {  // split: per ring step a chunk copy, then a GEMM launch over that slot
-      const int P = producer_count(c, cg, tiles);
+      const int P = producer_count(c, cg, tiles, nkb, p.chunk_bytes, false);
       const int G = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, P, tiles / c->tp);
       cudaError_t e = cudaEventRecord(c->ev_fork, s);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(c->copy, c->ev_fork, 0);
@@ -629,7 +749,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       return e == cudaSuccess ? TPO_OK : cuda_fail(e, "split join");
     }
     default: {  // producer only
-      const int P = producer_count(c, cg, tiles);
+      const int P = producer_count(c, cg, tiles, nkb, p.chunk_bytes, c->tail_split != 0);
       if (P > c->max_coop_grid) return fail(TPO_ERR_INVALID_ARG, "producer_sms too large");
       advance_targets(c, p, P);
       p.num_producers = P;
@@ -772,6 +892,7 @@ tpo_status tpo_sync_status(tpo_ctx* c) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->aux);
   if (e != cudaSuccess) return cuda_fail(e, "reset after device failure");
   std::memset(c->target, 0, sizeof(c->target));
+  c->part_epoch = 0;
   c->done_target = 0;
   c->done_op = -1;
   c->done_groups = 0;

@@ -190,6 +190,9 @@ __device__ __forceinline__ uint32_t atom_add_release(uint32_t* ptr, uint32_t v) 
   asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
   return old;
 }
+__device__ __forceinline__ void st_release(uint32_t* ptr, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* ptr) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
@@ -443,6 +446,112 @@ __device__ __forceinline__ Tile tile_at(const Params& p, int t) {
   return T;
 }
 
+// The work of CTA group g (a CTA, or a pair of them).  Groups 0 .. G-1 are
+// the GEMM CTAs; with late groups (p.late_groups > 0) the producer CTAs join
+// as groups G, G+1, ... once their copy is done.
+//
+// Without the tail split: tiles t = g, g+G, g+2G, ... in rounds.
+//
+// With it (AG), some tiles are "tail" tiles whose K units (kps K blocks each)
+// are laid end to end and cut into consecutive ranges, one per group, in two
+// bands: groups [0, ga) share the first wa units evenly, groups [ga, ga+gb)
+// the next wb units.  A range holds at most a later part of one tile first
+// (SEG_WRITE: stored as an fp32 partial to the group's workspace block), then
+// whole tiles, and at most the first part of one more tile last (SEG_FINISH:
+// its accumulator plus the later parts' partials in K order, then the
+// output).  A finisher only ever waits for higher groups' first tail segment,
+// which waits for nothing the finisher holds.
+//
+//  * tail first (no late groups): the R = T mod G leftover tiles are the
+//    first tiles (the observer's own chunk, readable at once), shared by
+//    ga = min(G, TAIL_SPLIT R) groups; the whole rounds follow from tile R,
+//    the groups without tail work taking each round's lowest tiles.
+//  * tail last (late groups): the GEMM groups first take p.split_full whole
+//    rounds; the remaining tiles are shared by the GEMM groups (band a, a
+//    short range each) and the late groups (band b, the rest), sized on the
+//    host so that both end together given when the copy should finish.
+enum SegKind : int { SEG_WHOLE = 0, SEG_FINISH = 1, SEG_WRITE = 2 };
+struct Seg {
+  int t, kb_lo, kb_hi, kind;
+  int w0, nw;  // SEG_FINISH: the groups w0, ..., w0 + nw - 1 hold the tile's later parts
+};
+template <bool SPLIT>  // false: a kernel built without the split (round robin only)
+struct SegIter {
+  int g, s, nfull, G, whole_base, slot, tail_base, kbu, kps, ga, gb;
+  bool first;
+  long long wa, wb, pos, end;
+  __device__ long long start_of(int w) const {  // first tail unit of group w (w <= ga + gb)
+    if (w <= ga) return ga > 0 ? wa * w / ga : 0;
+    return wa + wb * (w - ga) / gb;
+  }
+  __device__ SegIter(const Params& p, int g_, int G_, int T, int nkb) : g(g_), s(0), G(G_), kps(p.kps) {
+    kbu = nkb / kps;
+    ga = gb = 0;
+    wa = wb = pos = end = 0;
+    tail_base = 0;
+    first = true;
+    if (!SPLIT || !p.tail_split) {
+      nfull = g < T && g < G ? (T - g + G - 1) / G : 0;
+      whole_base = 0;
+      slot = g;
+      return;
+    }
+    ga = p.split_ga;
+    gb = p.split_gb;
+    wa = p.split_wa;
+    wb = p.split_wb;
+    first = p.split_tail_first != 0;
+    if (first) {
+      const int R = T - p.split_full * G;
+      nfull = g < G ? p.split_full : 0;
+      whole_base = R;
+      slot = (g - ga + G) % G;
+    } else {
+      nfull = g < G ? p.split_full : 0;
+      whole_base = 0;
+      slot = g;
+      tail_base = p.split_full * G;
+    }
+    if (g < ga + gb) {
+      pos = start_of(g);
+      end = start_of(g + 1);
+    }
+  }
+  __device__ bool tail_next(Seg& o) {
+    if (pos >= end) return false;
+    const long long tt = pos / kbu;
+    const int lo = static_cast<int>(pos - tt * kbu);
+    const int hi = static_cast<int>(min(static_cast<long long>(kbu), lo + (end - pos)));
+    o.t = tail_base + static_cast<int>(tt);
+    o.kb_lo = lo * kps;
+    o.kb_hi = hi * kps;
+    o.kind = (lo == 0 && hi == kbu) ? SEG_WHOLE : (lo == 0 ? SEG_FINISH : SEG_WRITE);
+    if (o.kind == SEG_FINISH) {
+      const long long tile_end = (tt + 1) * kbu;
+      o.w0 = g + 1;
+      for (int w = g + 1; w < ga + gb && start_of(w) < tile_end; ++w) ++o.nw;
+    }
+    pos += hi - lo;
+    return true;
+  }
+  __device__ bool next(Seg& o) {
+    if constexpr (SPLIT) {
+      o.w0 = o.nw = 0;
+      if (first && tail_next(o)) return true;
+    }
+    if (s < nfull) {
+      o.t = whole_base + slot + s * G;
+      o.kb_lo = 0;
+      o.kb_hi = kbu * kps;
+      o.kind = SEG_WHOLE;
+      ++s;
+      return true;
+    }
+    if constexpr (SPLIT) return !first && tail_next(o);
+    return false;
+  }
+};
+
 // ------------------------------------------------------------------ producer role
 
 __device__ __forceinline__ uint32_t piece_bytes(const Params& p, long long piece) {
@@ -543,6 +652,21 @@ __device__ bool wait_counter(const Params& p, int slot) {
   return true;
 }
 
+// Bounded wait (every lane of a warp) until a split tile's partial of this
+// launch is in the workspace; the acquire orders the lane's later loads.
+__device__ bool wait_partial(const Params& p, const uint32_t* flag) {
+  const unsigned long long t0 = gtime();
+  while (static_cast<int>(ld_acquire(flag) - p.part_target) < 0) {
+    if (aborted(p)) return false;
+    if (gtime() - t0 > p.timeout_ns) {
+      raise_error(p, DEV_TIMEOUT, SITE_PARTIAL, static_cast<uint32_t>(flag - p.words->part_ready));
+      return false;
+    }
+    __nanosleep(32);
+  }
+  return true;
+}
+
 struct Bars {
   uint32_t full0, empty0, tfull0, tempty0, drain;
 };
@@ -550,7 +674,7 @@ struct Bars {
 // The TMA issuer: one thread keeps every stage of the pipeline in flight.  Like
 // the MMA issuer it runs from registers only (tensor-map addresses, ring
 // position, stage and phase), so that refills follow stage releases closely.
-template <int CG, bool AG>
+template <int CG, bool AG, bool SPLIT>
 __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_t rank, int g, int G,
                          int total_tiles, int nkb, bool trace) {
   using PP = Pipe<CG>;
@@ -568,8 +692,10 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
   uint32_t ready = 0, stage = 0, phase = 0, blk = 0, armed = 0;
   bool ok = true;
   unsigned long long cyc_empty = 0;
-  for (int t = g; t < total_tiles && ok; t += G) {
-    const Tile T = tile_at<PP::TILE_M>(p, t);
+  SegIter<SPLIT> it(p, g, G, total_tiles, nkb);
+  Seg sg;
+  while (ok && it.next(sg)) {
+    const Tile T = tile_at<PP::TILE_M>(p, sg.t);
     if (AG && T.gate >= 0 && !((ready >> T.gate) & 1u)) {
       if (!wait_counter(p, T.gate)) {
         ok = false;
@@ -578,9 +704,9 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
       ready |= 1u << T.gate;
     }
     int r = AG ? T.a_map : T.seg0;  // tensor map of the current K segment
-    int kk = 0;
+    int kk = sg.kb_lo;               // (RS/AR segments always start at K block 0)
     const int a_row = T.a_row + a_off, a_z = T.a_z, b_row = T.col + b_off;
-    for (int i = 0; i < nkb; ++i) {
+    for (int i = sg.kb_lo; i < sg.kb_hi; ++i) {
       const uint32_t sbase_stage = sbase + SMEM_STAGES + stage * stage_bytes;
       if (blk == 0) {  // a new stage: wait until the MMAs released it, then arm its barrier
         const uint32_t eb = empty0 + 8u * stage;
@@ -633,14 +759,14 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
   if (trace) atomicAdd(&p.words->trace[TPO_TRACE_CYC_TMA_EMPTY], cyc_empty);
 }
 
-template <int CG>
+template <int CG, bool SPLIT>
 __device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, uint32_t rank, int g, int G,
                          int total_tiles, int nkb) {
   const bool trace = p.trace_on != 0;
   if (p.op == OP_AG)
-    tma_loop<CG, true>(p, sbase, B, rank, g, G, total_tiles, nkb, trace);
+    tma_loop<CG, true, SPLIT>(p, sbase, B, rank, g, G, total_tiles, nkb, trace);
   else
-    tma_loop<CG, false>(p, sbase, B, rank, g, G, total_tiles, nkb, trace);
+    tma_loop<CG, false, false>(p, sbase, B, rank, g, G, total_tiles, nkb, trace);
 }
 
 // The MMA issuer.  tcgen05.mma issue returns only once the tensor core can take
@@ -648,7 +774,7 @@ __device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, uint32_
 // thread spends between two MMAs is tensor-pipe idle time.  The loop therefore
 // keeps all state in registers (no parameter reloads), tests each stage's
 // barrier inline and only falls back to the bounded wait when it is not ready.
-template <int CG, bool FP8>
+template <int CG, bool FP8, bool SPLIT>
 __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
                          int total_tiles, int nkb, bool trace) {
   using PP = Pipe<CG>;
@@ -671,7 +797,9 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   uint32_t stage = 0, phase = 0, blk = 0, ul = 0, issued = 0;
   bool ok = true;
   unsigned long long cyc_full = 0, cyc_tempty = 0;
-  for (int t = g; t < total_tiles && ok; t += G)
+  SegIter<SPLIT> it(p, g, G, total_tiles, nkb);
+  Seg sg;
+  while (ok && it.next(sg))
    for (int u = 0; u < units; ++u, ++ul) {
     const uint32_t acc = ul & 1u;
     const uint32_t te = tempty0 + 8u * acc;
@@ -682,7 +810,8 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
     }
     tc_fence_after();
     const uint32_t d = tmem + acc * BN;
-    for (int i = 0; i < kpu; ++i) {
+    const int nk = per_rank ? kpu : sg.kb_hi - sg.kb_lo;
+    for (int i = 0; i < nk; ++i) {
       if (blk == 0) {
         const uint32_t fb = full0 + 8u * stage;
         if (!mbar_test(fb, phase) && !mbar_wait_timed(p, fb, phase, SITE_FULL, true, &cyc_full)) {
@@ -721,17 +850,17 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   }
 }
 
-template <int CG>
+template <int CG, bool SPLIT>
 __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
                          int total_tiles, int nkb) {
   const bool trace = p.trace_on != 0;
   if (p.fp8)
-    mma_loop<CG, true>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
+    mma_loop<CG, true, SPLIT>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
   else
-    mma_loop<CG, false>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
+    mma_loop<CG, false, SPLIT>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
 }
 
-template <int CG>
+template <int CG, bool SPLIT>
 __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, const Bars& B, uint32_t rank, int g,
                               int G, int total_tiles) {
   using PP = Pipe<CG>;
@@ -750,12 +879,23 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
                                     static_cast<size_t>(blockIdx.x - p.num_producers) * (BM * BN / 4) + quad * 32 + lane
                               : nullptr;
   uint64_t ws_pol = 0;
-  if (rmode) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(ws_pol));
+  if (rmode || SPLIT) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(ws_pol));
+  // Split tiles (AG tail split): a CTA's partial of a later part of a tile sits
+  // in its own workspace block in the same layout, unscaled fp32.
+  const int cta = g * CG + static_cast<int>(rank);  // workspace block and partial flags of this CTA
+  const uint4* const part_lane = reinterpret_cast<const uint4*>(p.ws) + quad * 32 + lane;
   uint32_t ul = 0, nst = 0;
   unsigned long long cyc_tfull = 0;
   bool ok_all = true;
-  for (int t = g; t < total_tiles && ok_all; t += G) {
-    const Tile T = tile_at<PP::TILE_M>(p, t);
+  SegIter<SPLIT> it(p, g, G, total_tiles, p.num_segs * p.kb_per_seg);
+  Seg sg;
+  while (ok_all && it.next(sg)) {
+    const Tile T = tile_at<PP::TILE_M>(p, sg.t);
+    if (SPLIT && sg.kind == SEG_FINISH) {  // the later parts' partials of this warp's rows must be stored
+      for (int j = 0; j < sg.nw && ok_all; ++j)
+        ok_all = wait_partial(p, &p.words->part_ready[((sg.w0 + j) * CG + static_cast<int>(rank)) * EPI_WARPS + quad]);
+      if (!ok_all) break;
+    }
     for (int u = 0; u < units; ++u, ++ul) {
       const uint32_t acc = ul & 1u;
       const uint32_t bar = B.tfull0 + 8u * acc, par = (ul >> 1) & 1u;
@@ -831,6 +971,30 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
               mbar_arrive_cluster(map_to_rank(B.tempty0 + 8u * acc, 0));
           }
         }
+        if (SPLIT && sg.kind == SEG_WRITE) {  // a later part of a split tile: keep the fp32 partial
+          uint4* w4 = const_cast<uint4*>(part_lane) + static_cast<size_t>(cta) * (BM * BN / 4) + c * 8 * BM;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) st_global_v4_keep(w4 + v * BM, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3], ws_pol);
+          return;
+        }
+        if (SPLIT && sg.kind == SEG_FINISH) {  // the first part: add the later parts in K order
+          for (int j = 0; j < sg.nw; ++j) {
+            const uint4* w4 = part_lane + static_cast<size_t>((sg.w0 + j) * CG + static_cast<int>(rank)) * (BM * BN / 4) +
+                              c * 8 * BM;
+            uint32_t h[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              uint32_t x[4];
+              ld_global_v4_keep(w4 + v * BM, x, ws_pol);
+              h[4 * v] = x[0];
+              h[4 * v + 1] = x[1];
+              h[4 * v + 2] = x[2];
+              h[4 * v + 3] = x[3];
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(h[e]));
+          }
+        }
         float out_scale = scale;
         if (rmode) {
           // this rank's partial, added in ring order to the running sum
@@ -852,6 +1016,11 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
             return;
           }
         }
+        // A box wholly past the output's edge is neither staged nor stored.  It
+        // must not take a staging buffer either: the wait below counts issued
+        // stores, so a buffer may only alternate with boxes that were stored.
+        const int ox = T.col + c * EPI_COLS, oy = T.y_row + row_off + quad * 32;
+        if (ox >= p.m || oy >= p.y_rows) return;
         uint32_t packed[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -861,7 +1030,7 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
         }
         const uint32_t buf = ebase + (nst & 1u) * EPI_BUF_BYTES;
         ++nst;
-        if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer two boxes ago has read it
+        if (lane == 0) bulk_wait_read<1>();  // the store that used this buffer (the one before last) has read it
         __syncwarp();
         // row `lane` of a 32 x 64-byte box in the 64-byte swizzle layout the
         // output tensor map expects (16-byte chunk index XOR (row / 2) % 4)
@@ -872,8 +1041,7 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
         }
         fence_proxy_async_smem();
         __syncwarp();
-        const int ox = T.col + c * EPI_COLS, oy = T.y_row + row_off + quad * 32;
-        if (lane == 0 && ox < p.m && oy < p.y_rows) {  // boxes wholly past the output's edge are skipped
+        if (lane == 0) {
           tma_store_3d(&p.mapY[T.y_map], buf, ox, oy, T.y_z);
           bulk_commit();
         }
@@ -895,6 +1063,13 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
         for (int c = 0; c < BN / EPI_COLS; ++c) chunk(c, none, false);
       }
     }
+    if (SPLIT && ok_all && sg.kind == SEG_WRITE) {  // this warp's rows of the partial are stored: publish them
+      __syncwarp();
+      if (lane == 0 && cta != p.skip_part) {
+        __threadfence();
+        st_release(&p.words->part_ready[cta * EPI_WARPS + quad], p.part_target);
+      }
+    }
     if (ok_all && p.op != OP_AG && lane == 0) {  // this warp's rows of the tile are in memory: count them
       bulk_wait<0>();
       fence_proxy_async_global();
@@ -907,7 +1082,7 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
   __syncwarp();
 }
 
-template <int CG>
+template <int CG, bool SPLIT>
 __device__ void gemm_role(const Params& p, uint8_t* smem) {
   using PP = Pipe<CG>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -944,17 +1119,19 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  const int g = (static_cast<int>(blockIdx.x) - p.num_producers) / CG, G = p.num_gemm / CG;
+  // GEMM CTAs are groups 0 .. G-1; producer CTAs that join afterwards follow
+  const int bid = static_cast<int>(blockIdx.x), G = p.num_gemm / CG;
+  const int g = bid >= p.num_producers ? (bid - p.num_producers) / CG : G + bid / CG;
   const int total_tiles = p.num_groups * p.row_tiles * p.col_tiles;
   const int nkb = p.num_segs * p.kb_per_seg;
   if (warp == 0) {
-    if (lane == 0) tma_role<CG>(p, sbase, B, rank, g, G, total_tiles, nkb);
+    if (lane == 0) tma_role<CG, SPLIT>(p, sbase, B, rank, g, G, total_tiles, nkb);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_role<CG>(p, sbase, tmem, B, g, G, total_tiles, nkb);
+    if (lane == 0 && rank == 0) mma_role<CG, SPLIT>(p, sbase, tmem, B, g, G, total_tiles, nkb);
     __syncwarp();
   } else {
-    epilogue_role<CG>(p, smem, tmem, B, rank, g, G, total_tiles);
+    epilogue_role<CG, SPLIT>(p, smem, tmem, B, rank, g, G, total_tiles);
   }
   tc_fence_before();
   __syncthreads();
@@ -967,16 +1144,24 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
     atomicAdd(&p.words->trace[TPO_TRACE_CYC_GEMM], static_cast<unsigned long long>(clock64() - cyc_start));
 }
 
-template <int CG>
+// SPLIT: the build with the AG tail split (launched only when p.tail_split is
+// set); the default build carries none of its code.
+template <int CG, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   if (p.trace_on && threadIdx.x == 0) atomicMin(&p.words->trace[TPO_TRACE_START], gtime());
   if (static_cast<int>(blockIdx.x) < p.num_producers) {
-    producer_role(p, smem);
+    if (p.copy_on) producer_role(p, smem);
+    if constexpr (SPLIT) {
+      if (p.late_groups > 0) {  // the copy is done: join the GEMM (its ring buffers are free)
+        __syncthreads();
+        gemm_role<CG, SPLIT>(p, smem);
+      }
+    }
   } else if (static_cast<int>(blockIdx.x) < p.num_producers + p.num_gemm) {
-    gemm_role<CG>(p, smem);
+    gemm_role<CG, SPLIT>(p, smem);
   }
   if (p.trace_on && threadIdx.x == 0) atomicMax(&p.words->trace[TPO_TRACE_END], gtime());
 }
@@ -984,14 +1169,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_kernel(const __grid_cons
 // ------------------------------------------------------------------ host side launch
 
 cudaError_t configure_kernel() {
-  cudaError_t e = cudaFuncSetAttribute(fused_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  cudaError_t e = cudaFuncSetAttribute(fused_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fused_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    e = cudaFuncSetAttribute(fused_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
   return e;
 }
 
 cudaError_t max_blocks_per_sm(int* n) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fused_kernel<1>, NUM_THREADS, SMEM_ALLOC);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fused_kernel<1, false>, NUM_THREADS, SMEM_ALLOC);
 }
 
 cudaError_t max_active_pairs(int* n) {
@@ -1006,7 +1195,7 @@ cudaError_t max_active_pairs(int* n) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(n, fused_kernel<2>, &cfg);
+  return cudaOccupancyMaxActiveClusters(n, fused_kernel<2, false>, &cfg);
 }
 
 cudaError_t launch_fused(const Params& p, int grid, bool cooperative, cudaStream_t stream) {
@@ -1031,8 +1220,12 @@ cudaError_t launch_fused(const Params& p, int grid, bool cooperative, cudaStream
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  if (p.cta_group == 2) return cudaLaunchKernelEx(&cfg, fused_kernel<2>, p);
-  return cudaLaunchKernelEx(&cfg, fused_kernel<1>, p);
+  if (p.tail_split) {
+    if (p.cta_group == 2) return cudaLaunchKernelEx(&cfg, fused_kernel<2, true>, p);
+    return cudaLaunchKernelEx(&cfg, fused_kernel<1, true>, p);
+  }
+  if (p.cta_group == 2) return cudaLaunchKernelEx(&cfg, fused_kernel<2, false>, p);
+  return cudaLaunchKernelEx(&cfg, fused_kernel<1, false>, p);
 }
 
 }  // namespace tpo

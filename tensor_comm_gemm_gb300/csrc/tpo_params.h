@@ -61,6 +61,11 @@ static_assert(SMEM_ALLOC <= 232448, "exceeds the per-CTA shared memory limit");
 
 enum Op : int { OP_AG = 0, OP_RS = 1, OP_AR = 2 };
 
+constexpr int MAX_GEMM_CTAS = 256;  // GEMM CTAs of one launch (at most one per SM)
+// AG tail split: the tiles left over after the whole rounds are divided along
+// K among at most TAIL_SPLIT x (leftover tiles) CTA groups.
+constexpr int TAIL_SPLIT = 2;
+
 // Device error word layout: [0] code, [1] site, [2] block, [3] slot/extra.
 enum DevErr : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1 };
 enum Site : uint32_t {
@@ -70,7 +75,8 @@ enum Site : uint32_t {
   SITE_TMEM_EMPTY = 4, // MMA thread waiting for a drained accumulator
   SITE_TMEM_FULL = 5,  // epilogue waiting for a finished accumulator
   SITE_COPY = 6,       // producer waiting for a bulk load
-  SITE_DRAIN = 7       // clean-up waits after a failure
+  SITE_DRAIN = 7,      // clean-up waits after a failure
+  SITE_PARTIAL = 8     // epilogue waiting for a split tile's partial
 };
 
 // Per-context device words (one allocation).
@@ -78,6 +84,7 @@ struct DevWords {
   uint32_t counters[TPO_MAX_TP];        // per-slot chunk counters (monotonic)
   uint32_t err[4];
   uint32_t done[TPO_MAX_ROW_CHUNKS];    // per output group done counters (RS owner block, AR row chunk; monotonic)
+  uint32_t part_ready[MAX_GEMM_CTAS * 4];  // per GEMM CTA and epilogue warp: launch number of its last stored partial
   uint32_t pad[12];
   unsigned long long trace[TPO_TRACE_WORDS];
 };
@@ -99,6 +106,7 @@ struct Params {
   unsigned long long delay_ns;
   uint32_t target[TPO_MAX_TP];  // per slot: counter value once this call has published it
   uint32_t done_target;   // RS/AR done-counter value once this call stored the whole group
+  uint32_t part_target;   // AG tail split: this launch's number (part_ready value of a stored partial)
   uint32_t pad1;
   int op;
   int fp8;
@@ -126,6 +134,14 @@ struct Params {
                           // partial and running sum (a bf16 ring's wire format)
   int trace_on;
   int cta_group;          // 1: single-SM MMA, 2: CTA pairs (cluster of 2) with the 2-SM MMA
+  int tail_split;         // AG: split tail tiles along K (see SegIter in the kernel)
+  int split_tail_first;   // tail tiles first (1) or after split_full whole rounds (0)
+  int split_full;         // whole rounds of the GEMM groups
+  int split_ga, split_gb; // groups of the two tail bands
+  long long split_wa, split_wb;  // tail K units of the two bands
+  int late_groups;        // producer CTA groups that join the GEMM after their copy
+  int copy_on;            // producer CTAs copy (0: they only run as late GEMM groups)
+  int skip_part;          // test hook: this GEMM CTA never publishes its partial (-1: none)
 };
 
 // Zeroes a launch description and sets every field whose "off" value is not 0.
@@ -134,6 +150,8 @@ inline void init_params(Params& p) {
   p.skip_slot = -1;
   p.last_step = -1;
   p.only_step = -1;
+  p.skip_part = -1;
+  p.copy_on = 1;
   p.cta_group = 1;
   p.kps = 1;
 }

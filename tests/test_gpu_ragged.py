@@ -58,6 +58,7 @@ def test_ag_ragged_parity_every_observer(tp, n, k, m, dtype):
     run = AgRun(wl)
     out = Guarded(n, m)
     try:
+        t.tpo_set_opt(run.ctx, "tail_split", 0)   # whole tiles: modes 0, 1 and 4 give the same bits
         first = None
         for self_rank in sorted({0, tp - 1}):
             t.tpo_set_opt(run.ctx, "self_rank", self_rank)
@@ -93,6 +94,7 @@ def test_ag_noalloc_ragged_matches_context_path():
     run = AgRun(wl)
     out = Guarded(wl.n, wl.m)
     try:
+        t.tpo_set_opt(run.ctx, "tail_split", 0)   # the no-alloc entry point computes whole tiles
         run.run()
         want = host_bits(run.y)
         out.poison()
@@ -171,5 +173,63 @@ def test_ar_ragged_one_chunk_equals_rs_bitwise():
         run.rs()
         rs = np.concatenate([host_bits(y) for y in run.yb], 0)
         assert np.array_equal(ar, rs)
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("tp,n,k,m,dtype", [(3, 600, 200, 264, "bf16"), (2, 1000, 48, 520, "e4m3"),
+                                            (4, 1200, 1000, 1000, "bf16")])
+@pytest.mark.parametrize("gemm_ctas", [2, 5])
+def test_ag_ragged_several_tiles_per_cta_every_launch(tp, n, k, m, dtype, gemm_ctas):
+    """Few GEMM CTAs, so that each stores several ragged tiles one after the
+    other, and repeated launches: an output box past the edge must not give
+    up a staging buffer that a store in flight still reads."""
+    wl = synth.make_ag(tp, n, k, m, seed=60 + tp, dist="uniform", dtype=dtype)
+    ref = oracle.ag(oracle.gather(wl.x), wl.w[0], wl.scale_inv_x, wl.scale_inv_w)
+    run = AgRun(wl)
+    out = Guarded(n, m)
+    try:
+        t.tpo_set_opt(run.ctx, "gemm_ctas", gemm_ctas)
+        t.tpo_set_opt(run.ctx, "tail_split", 0)
+        first = None
+        for _ in range(6):
+            out.poison()
+            run.run(y=out.y)
+            assert out.guards_intact()
+            if first is None:
+                assert_close(host_f64(out.y), ref, dtype)
+                first = host_bits(out.y)
+            assert np.array_equal(host_bits(out.y), first)
+    finally:
+        run.close()
+
+
+@pytest.mark.parametrize("op,tp,n,k,m,chunks,dtype", [("rs", 3, 390, 48, 24, 1, "bf16"),
+                                                       ("ar", 2, 600, 32, 40, 3, "bf16"),
+                                                       ("rs", 2, 1030, 96, 776, 1, "bf16")])
+def test_ksplit_ragged_several_tiles_per_cta_every_launch(op, tp, n, k, m, chunks, dtype):
+    wl = synth.make_ksplit(op, tp, n, k, m, seed=85 + tp, n_row_chunks=chunks, dtype=dtype, sigma=k ** -0.25)
+    ref = oracle.ksplit(wl.x, wl.w, sx=wl.scale_inv_x, sw=wl.scale_inv_w)
+    run = KsplitRun(wl)
+    try:
+        t.tpo_set_opt(run.ctx, "gemm_ctas", 2)
+        first = None
+        for _ in range(6):
+            if op == "rs":
+                for y in run.yb:
+                    y.fill_(float("nan"))
+                t.tpo_gemm_rs(run.ctx, run.xs, run.ws, run.yb)
+                assert t.tpo_sync_status(run.ctx) == 0, t.tpo_last_error()
+                got = np.concatenate([host_f64(y) for y in run.yb], 0)
+                bits = np.concatenate([host_bits(y) for y in run.yb], 0)
+            else:
+                run.y.fill_(float("nan"))
+                t.tpo_gemm_ar(run.ctx, run.xs, run.ws, run.y, chunks)
+                assert t.tpo_sync_status(run.ctx) == 0, t.tpo_last_error()
+                got, bits = host_f64(run.y), host_bits(run.y)
+            if first is None:
+                assert_close(got, ref, dtype)
+                first = bits
+            assert np.array_equal(bits, first)
     finally:
         run.close()

@@ -163,3 +163,164 @@ def test_workload_shapes_fit_the_tiling():
         else:
             assert k % tp == 0 and (k // tp) % 64 == 0
             assert n % (chunks * tp * BM) == 0
+
+
+TAIL_SPLIT = 2
+
+
+def plan_split(T, G, L, kbu, kps=2, tp=4, chunk_bytes=1 << 23, cg=2):
+    """The host's plan: (tail_first, full, ga, wa, gb, wb) or None (no split)."""
+    if L > 0:
+        P = L * cg
+        t_copy = tp * chunk_bytes / (P * 31e9) + 3e-6
+        late = 1.2 * t_copy / (kps * 0.36e-6)
+        E = (T * kbu + L * late) / (G + L)
+        if E > late + 1.0:
+            full = min(int(E / kbu), T // G)
+            wt = (T - full * G) * kbu
+            sm = max(int(E - full * kbu), 0)
+            if sm * G > wt:
+                sm = wt // G
+            if wt - sm * G > 0:
+                return (0, full, G, sm * G, L, wt - sm * G)
+    full, R = divmod(T, G)
+    if R == 0:
+        return None
+    return (1, full, min(G, TAIL_SPLIT * R), R * kbu, 0, 0)
+
+
+def segments(g, G, T, nkb, kps, plan):
+    """The kernel's SegIter for group g (GEMM groups 0..G-1, late groups after):
+    (tile, K-block range, kind, writer groups) in order.  Kinds: whole, finish
+    (first part of a split tile), write (a later part)."""
+    kbu = nkb // kps
+    out = []
+    if plan is None:
+        if g < G:
+            for t in range(g, T, G):
+                out.append((t, 0, nkb, "whole", []))
+        return out
+    first, full, ga, wa, gb, wb = plan
+
+    def start_of(w):
+        if w <= ga:
+            return wa * w // ga if ga else 0
+        return wa + wb * (w - ga) // gb
+
+    nfull = full if g < G else 0
+    if first:
+        whole_base, slot, tail_base = T - full * G, (g - ga + G) % G, 0
+    else:
+        whole_base, slot, tail_base = 0, g, full * G
+    pos, end = (start_of(g), start_of(g + 1)) if g < ga + gb else (0, 0)
+    tail = []
+    while pos < end:
+        tt, lo = divmod(pos, kbu)
+        hi = min(kbu, lo + (end - pos))
+        kind = "whole" if (lo == 0 and hi == kbu) else ("finish" if lo == 0 else "write")
+        writers = []
+        if kind == "finish":
+            w = g + 1
+            while w < ga + gb and start_of(w) < (tt + 1) * kbu:
+                writers.append(w)
+                w += 1
+        tail.append((tail_base + tt, lo * kps, hi * kps, kind, writers))
+        pos += hi - lo
+    whole = [(whole_base + slot + s * G, 0, kbu * kps, "whole", []) for s in range(nfull)]
+    return tail + whole if first else whole + tail
+
+
+# (T tiles, G GEMM groups, L late groups, K blocks, kps)
+SPLIT_CASES = [(256, 64, 0, 64, 2), (256, 68, 0, 64, 2), (256, 70, 0, 64, 2), (256, 76, 0, 64, 2),
+               (7168, 72, 0, 64, 2), (7168, 75, 0, 64, 2), (3, 70, 0, 4, 1), (1, 152, 0, 1, 1), (5, 4, 0, 3, 1),
+               (9, 4, 0, 7, 1), (130, 64, 0, 2, 2), (100, 152, 0, 32, 1), (64, 2, 0, 1, 1), (17, 16, 0, 5, 1),
+               (33, 16, 0, 64, 2), (1, 2, 0, 8, 2), (2, 3, 0, 1, 1),
+               (256, 64, 12, 64, 2), (256, 68, 8, 64, 2), (7168, 72, 4, 64, 2), (7168, 64, 12, 64, 2),
+               (24, 5, 2, 8, 2), (16, 3, 1, 8, 2), (12, 5, 3, 4, 1), (20, 7, 2, 5, 1), (256, 60, 16, 16, 1)]
+
+
+def all_groups(G, L, plan):
+    return G + (L if plan is not None and not plan[0] else 0)
+
+
+@pytest.mark.parametrize("T,G,L,nkb,kps", SPLIT_CASES)
+@pytest.mark.parametrize("split", [0, 1])
+def test_segments_cover_every_k_block_once(T, G, L, nkb, kps, split):
+    plan = plan_split(T, G, L, nkb // kps, kps) if split else None
+    seen = {}
+    for g in range(all_groups(G, L, plan)):
+        for t, lo, hi, kind, _ in segments(g, G, T, nkb, kps, plan):
+            assert 0 <= t < T and 0 <= lo < hi <= nkb and lo % kps == 0 and hi % kps == 0
+            for kb in range(lo, hi):
+                assert (t, kb) not in seen
+                seen[(t, kb)] = g
+    assert len(seen) == T * nkb
+
+
+@pytest.mark.parametrize("T,G,L,nkb,kps", SPLIT_CASES)
+def test_no_split_keeps_round_robin(T, G, L, nkb, kps):
+    for g in range(G):
+        assert [s[0] for s in segments(g, G, T, nkb, kps, None)] == list(range(g, T, G))
+    if T % G == 0 and L == 0:  # whole rounds: nothing to split
+        assert plan_split(T, G, L, nkb // kps, kps) is None
+
+
+@pytest.mark.parametrize("T,G,L,nkb,kps", SPLIT_CASES)
+def test_split_parts_and_dependencies(T, G, L, nkb, kps):
+    """Each group writes at most one partial, as its first tail segment (after
+    which it waits for nothing a lower group holds), and finishes at most one
+    split tile, as its last tail segment; a finisher's writer list is exactly
+    the higher groups holding the tile's later parts, in K order."""
+    plan = plan_split(T, G, L, nkb // kps, kps)
+    if plan is None:
+        return
+    parts, finish = {}, {}
+    for g in range(all_groups(G, L, plan)):
+        seg = segments(g, G, T, nkb, kps, plan)
+        kinds = [x[3] for x in seg]
+        assert kinds.count("write") <= 1 and kinds.count("finish") <= 1
+        if "write" in kinds:
+            i = kinds.index("write")
+            assert all(k == "whole" for k in kinds[:i])       # only whole tiles (no waits) before it
+        if "finish" in kinds:
+            i = kinds.index("finish")
+            assert all(w > g for w in seg[i][4])
+            if not plan[0]:
+                assert i == len(seg) - 1                       # tail last: the finish is the last segment
+            finish[seg[i][0]] = (g, seg[i][4])
+        for t, lo, hi, kind, _ in seg:
+            if kind != "whole":
+                parts.setdefault(t, []).append((lo, hi, g, kind))
+    for t, ps in parts.items():
+        ps.sort()
+        assert len(ps) >= 2
+        assert ps[0][3] == "finish" and all(p[3] == "write" for p in ps[1:])
+        assert [p[2] for p in ps] == sorted(p[2] for p in ps)  # later K, higher group
+        assert finish[t] == (ps[0][2], [p[2] for p in ps[1:]])
+        if plan[0]:
+            assert len(ps) <= 3
+
+
+@pytest.mark.parametrize("T,G,L,nkb,kps", [c for c in SPLIT_CASES if c[2] == 0])
+def test_split_balances_work(T, G, L, nkb, kps):
+    """Tail first: no group holds more than a whole round plus one share of
+    the leftover tiles."""
+    kbu = nkb // kps
+    plan = plan_split(T, G, 0, kbu, kps)
+    load = [sum(hi - lo for _, lo, hi, _, _ in segments(g, G, T, nkb, kps, plan)) // kps for g in range(G)]
+    R = T % G
+    share = cdiv(R * kbu, min(G, TAIL_SPLIT * R)) if R else 0
+    assert max(load) <= (T // G) * kbu + share
+    if R and kbu >= 2 * cdiv(R, G):  # a tile's K units can be spread: shorter than whole rounds
+        assert max(load) < cdiv(T, G) * kbu
+
+
+def test_late_groups_plan_for_the_headline_shape():
+    """AG tp=4, 4096^3 with 24 producer CTAs (12 pairs) and 64 GEMM pairs: the
+    GEMM pairs keep three whole rounds, the producer pairs take the rest of the
+    last chunk's tiles after their copy, and no GEMM pair does a fourth tile."""
+    T, G, L, kbu = 256, 64, 12, 32
+    plan = plan_split(T, G, L, kbu)
+    assert plan is not None and plan[0] == 0 and plan[1] == 3
+    loads = [sum(hi - lo for _, lo, hi, _, _ in segments(g, G, T, 64, 2, plan)) // 2 for g in range(G + L)]
+    assert max(loads[:G]) < 4 * kbu and min(loads[G:]) > 0

@@ -51,12 +51,16 @@ def test_noalloc_matches_context_entry_point_on_consecutive_calls(cases):
             wl = synth.make_ag(tp, n, k, m, seed=seed, dtype="e4m3")
         run = AgRun(wl)
         try:
+            t.tpo_set_opt(run.ctx, "tail_split", 0)     # the no-alloc entry point computes whole tiles
             run.run()                                   # existing entry point, through a context
             ref = host_f64(run.y)
             y = torch.full_like(run.y, float("nan"))
             _noalloc(run, y)                            # returns once the GPU work is done
             assert_close(host_f64(y), ref, wl.dtype)    # the tolerance of every parity test
             assert np.array_equal(host_bits(y), host_bits(run.y))  # same kernel, same tile arithmetic
+            t.tpo_set_opt(run.ctx, "tail_split", 2)     # the split schedule meets the same bar
+            run.run()
+            assert_close(host_f64(run.y), host_f64(y), wl.dtype)
         finally:
             run.close()
 
