@@ -404,12 +404,13 @@ def gpu_arm(args, rank, world, local_rank, dist):
     del xs, w, y, xs_sets, w_sets, y_sets, hx, hy, dx, dy
 
     # ---- the other workloads, one line each inside "also"
+    cpu_others = {} if (rank == 0 and not args.no_cpu) else None
     if not args.headline_only:
-        result["also"] = other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch)
+        result["also"] = other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch, cpu_others)
 
     # ---- the oracle on the host cores, bounded sample
     if rank == 0 and not args.no_cpu:
-        result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, cpu_others)
     return result
 
 
@@ -471,7 +472,7 @@ def library_gemm_4096(torch, dev, sets=3, calls=60):
         return None
 
 
-def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
+def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch, cpu_others=None):
     out = {}
     steps = min(40, max(5, args.steps // 2))
     # the small AG workload: latency-bound (2 output tiles), reported in microseconds per call
@@ -529,6 +530,8 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
                "frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / pk, 4), "peak_tflops": pk}
         if dt == "e4m3" and fp8_lib:
             rec["frac_of_library_fp8"] = round(flops / (ms * 1e-3) / 1e12 / fp8_lib, 4)
+        if cpu_others is not None:  # the CPU-baseline leg: the oracle on a sample of this workload
+            cpu_others[name] = other_sample(wl, max(1.0, args.cpu_seconds / 4))
         if op in ("rs", "ar"):
             # when each output group (RS owner block, AR row chunk) was complete, as a
             # fraction of the call: the point at which its communication could start
@@ -584,27 +587,61 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch):
 
 # ---------------------------------------------------------------------------- CPU oracle
 
-def cpu_baseline(wl, seconds):
-    """The oracle as it stands, on the host cores, over a bounded sample of the
-    workload's output tiles (16 x 16 each); throughput scaled to TFLOP/s."""
+def oracle_sample(wl, seconds, nthreads=None, seed=None):
+    """The oracle as it stands over a bounded sample of the workload's 16 x 16
+    output tiles (about `seconds` of work): (tiles timed, seconds, total tiles,
+    FLOP per tile)."""
     import oracle
 
-    g = oracle.gather(wl.x)
     tile = 16
-    per_tile = 2.0 * tile * tile * wl.k
-    probe = synth.sample_tiles(wl.n, wl.m, tile, 32, seed=7)
+    if wl.op == "ag":
+        g = oracle.gather(wl.x)
+
+        def run(tl):
+            oracle.ag(g, wl.w[0], wl.scale_inv_x, wl.scale_inv_w, tiles=tl, nthreads=nthreads)
+    else:
+        def run(tl):
+            oracle.ksplit(wl.x, wl.w, tiles=tl, nthreads=nthreads, sx=wl.scale_inv_x, sw=wl.scale_inv_w)
+    probe = synth.sample_tiles(wl.n, wl.m, tile, 16, seed=7)
     t0 = time.perf_counter()
-    oracle.ag(g, wl.w[0], tiles=probe)
+    run(probe)
     rate = len(probe) / max(time.perf_counter() - t0, 1e-6)
-    count = int(max(32, min(65536, rate * seconds)))
-    tiles = synth.sample_tiles(wl.n, wl.m, tile, count, seed=1000 + wl.seed)
+    count = int(max(16, min(65536, rate * seconds)))
+    tiles = synth.sample_tiles(wl.n, wl.m, tile, count, seed=(1000 + wl.seed) if seed is None else seed)
     t0 = time.perf_counter()
-    oracle.ag(g, wl.w[0], tiles=tiles)
+    run(tiles)
     dt = time.perf_counter() - t0
-    return {"value": per_tile * len(tiles) / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
-            "kind": "oracle",
-            "sample": "%d of %d output tiles of 16x16 (FP64 loops over k=%d), %.1f s" % (
-                len(tiles), (wl.n // tile) * (wl.m // tile), wl.k, dt)}
+    return len(tiles), dt, (wl.n // tile) * (wl.m // tile), 2.0 * tile * tile * wl.k
+
+
+def cpu_baseline(wl, seconds, others=None):
+    """The oracle as it stands, on the host cores, over a bounded sample of the
+    workload's output tiles (16 x 16 each); throughput scaled to TFLOP/s.  Also:
+    one core, the full problem's time extrapolated from the sample, and the
+    same for the other workloads (`others`: name -> sampled record)."""
+    import oracle
+
+    n, dt, total, per_tile = oracle_sample(wl, seconds)
+    n1, dt1, _, _ = oracle_sample(wl, max(1.0, seconds / 5), nthreads=1, seed=2000 + wl.seed)
+    out = {"value": per_tile * n / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+           "sample": "%d of %d output tiles of 16x16 (FP64 loops over k=%d), %.1f s" % (n, total, wl.k, dt),
+           "full_problem_s_extrapolated": round(dt * total / n, 1),
+           "single_core": {"value": per_tile * n1 / dt1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                           "sample": "%d output tiles, %.1f s" % (n1, dt1)}}
+    if others:
+        out["other_workloads"] = others
+    return out
+
+
+def other_sample(wl, seconds):
+    """cpu_baseline's record of another workload: the oracle on a bounded
+    sample of its output tiles, all host cores."""
+    import oracle
+
+    n, dt, total, per_tile = oracle_sample(wl, seconds)
+    return {"value": per_tile * n / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+            "sample": "%d of %d output tiles of 16x16 (FP64 loops over k=%d), %.1f s" % (n, total, wl.k, dt),
+            "full_problem_s_extrapolated": round(dt * total / n, 1)}
 
 
 def reference_arm(args):
