@@ -774,12 +774,14 @@ __device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, uint32_
 // thread spends between two MMAs is tensor-pipe idle time.  The loop therefore
 // keeps all state in registers (no parameter reloads), tests each stage's
 // barrier inline and only falls back to the bounded wait when it is not ready.
-template <int CG, bool FP8, bool SPLIT>
+// KPS: K blocks per pipeline stage (p.kps), fixed at compile time so that a
+// stage's MMAs issue back to back with no per-block bookkeeping between them.
+template <int CG, bool FP8, bool SPLIT, int KPS>
 __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
                          int total_tiles, int nkb, bool trace) {
   using PP = Pipe<CG>;
   constexpr uint32_t idesc = make_idesc(FP8, PP::TILE_M);
-  const uint32_t kps = static_cast<uint32_t>(p.kps);
+  constexpr uint32_t kps = KPS;
   const uint32_t stage_bytes = kps * PP::STAGE_BYTES;
   const uint32_t nstages = STAGE_AREA / stage_bytes;
   const uint64_t kStageDesc = static_cast<uint64_t>(stage_bytes >> 4);  // stage step in the address field
@@ -794,7 +796,7 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   const bool per_rank = p.reduce_mode != 0;
   const int units = per_rank ? p.num_segs : 1;
   const int kpu = per_rank ? p.kb_per_seg : nkb;
-  uint32_t stage = 0, phase = 0, blk = 0, ul = 0, issued = 0;
+  uint32_t stage = 0, phase = 0, ul = 0, issued = 0;
   bool ok = true;
   unsigned long long cyc_full = 0, cyc_tempty = 0;
   SegIter<SPLIT> it(p, g, G, total_tiles, nkb);
@@ -810,30 +812,29 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
     }
     tc_fence_after();
     const uint32_t d = tmem + acc * BN;
-    const int nk = per_rank ? kpu : sg.kb_hi - sg.kb_lo;
-    for (int i = 0; i < nk; ++i) {
-      if (blk == 0) {
-        const uint32_t fb = full0 + 8u * stage;
-        if (!mbar_test(fb, phase) && !mbar_wait_timed(p, fb, phase, SITE_FULL, true, &cyc_full)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+    const int nk = per_rank ? kpu : sg.kb_hi - sg.kb_lo;  // a multiple of KPS
+    for (int i = 0; i < nk; i += KPS) {
+      const uint32_t fb = full0 + 8u * stage;
+      if (!mbar_test(fb, phase) && !mbar_wait_timed(p, fb, phase, SITE_FULL, true, &cyc_full)) {
+        ok = false;
+        break;
       }
-      const uint64_t da = da0 + kStageDesc * stage + kBlkA * blk, db = db0 + kStageDesc * stage + kBlkB * blk;
-      // four MMAs of K = 32 bytes each cover the 128-byte K block
-      mma_cg<CG>(FP8, d, da, db, idesc, i > 0 ? 1u : 0u);
-      mma_cg<CG>(FP8, d, da + 2u, db + 2u, idesc, 1u);
-      mma_cg<CG>(FP8, d, da + 4u, db + 4u, idesc, 1u);
-      mma_cg<CG>(FP8, d, da + 6u, db + 6u, idesc, 1u);
-      ++issued;
-      if (++blk == kps) {
-        blk = 0;
-        mma_commit_cg<CG>(empty0 + 8u * stage);  // frees the stage (in both CTAs) once read
-        if (++stage == nstages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+      tc_fence_after();
+      const uint64_t das = da0 + kStageDesc * stage, dbs = db0 + kStageDesc * stage;
+#pragma unroll
+      for (int b = 0; b < KPS; ++b) {
+        const uint64_t da = das + kBlkA * b, db = dbs + kBlkB * b;
+        // four MMAs of K = 32 bytes each cover the 128-byte K block
+        mma_cg<CG>(FP8, d, da, db, idesc, (i + b) > 0 ? 1u : 0u);
+        mma_cg<CG>(FP8, d, da + 2u, db + 2u, idesc, 1u);
+        mma_cg<CG>(FP8, d, da + 4u, db + 4u, idesc, 1u);
+        mma_cg<CG>(FP8, d, da + 6u, db + 6u, idesc, 1u);
+      }
+      issued += KPS;
+      mma_commit_cg<CG>(empty0 + 8u * stage);  // frees the stage (in both CTAs) once read
+      if (++stage == nstages) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
     if (!ok) break;
@@ -854,10 +855,17 @@ template <int CG, bool SPLIT>
 __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
                          int total_tiles, int nkb) {
   const bool trace = p.trace_on != 0;
-  if (p.fp8)
-    mma_loop<CG, true, SPLIT>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
-  else
-    mma_loop<CG, false, SPLIT>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
+  if (CG == 2 && p.kps == 2) {
+    if (p.fp8)
+      mma_loop<CG, true, SPLIT, 2>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
+    else
+      mma_loop<CG, false, SPLIT, 2>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
+  } else {
+    if (p.fp8)
+      mma_loop<CG, true, SPLIT, 1>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
+    else
+      mma_loop<CG, false, SPLIT, 1>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
+  }
 }
 
 template <int CG, bool SPLIT>
