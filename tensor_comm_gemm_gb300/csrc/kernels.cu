@@ -674,7 +674,7 @@ struct Bars {
 // The TMA issuer: one thread keeps every stage of the pipeline in flight.  Like
 // the MMA issuer it runs from registers only (tensor-map addresses, ring
 // position, stage and phase), so that refills follow stage releases closely.
-template <int CG, bool AG, bool SPLIT>
+template <int CG, bool AG, bool SPLIT, int KPS>
 __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_t rank, int g, int G,
                          int total_tiles, int nkb, bool trace) {
   using PP = Pipe<CG>;
@@ -686,10 +686,10 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
   const uint32_t full0 = B.full0, empty0 = B.empty0;
   const uint32_t full0_leader = (CG == 2) ? map_to_rank(full0, 0) : full0;
   const int a_off = BM * static_cast<int>(rank), b_off = PP::B_ROWS * static_cast<int>(rank);
-  const uint32_t kps = static_cast<uint32_t>(p.kps);
-  const uint32_t stage_bytes = kps * PP::STAGE_BYTES;
-  const uint32_t nstages = STAGE_AREA / stage_bytes;
-  uint32_t ready = 0, stage = 0, phase = 0, blk = 0, armed = 0;
+  constexpr uint32_t kps = KPS;
+  constexpr uint32_t stage_bytes = kps * PP::STAGE_BYTES;
+  constexpr uint32_t nstages = STAGE_AREA / stage_bytes;
+  uint32_t ready = 0, stage = 0, phase = 0, armed = 0;
   bool ok = true;
   unsigned long long cyc_empty = 0;
   SegIter<SPLIT> it(p, g, G, total_tiles, nkb);
@@ -706,42 +706,41 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
     int r = AG ? T.a_map : T.seg0;  // tensor map of the current K segment
     int kk = sg.kb_lo;               // (RS/AR segments always start at K block 0)
     const int a_row = T.a_row + a_off, a_z = T.a_z, b_row = T.col + b_off;
-    for (int i = sg.kb_lo; i < sg.kb_hi; ++i) {
+    for (int i = sg.kb_lo; i < sg.kb_hi; i += KPS) {  // one stage of KPS K blocks per pass
       const uint32_t sbase_stage = sbase + SMEM_STAGES + stage * stage_bytes;
-      if (blk == 0) {  // a new stage: wait until the MMAs released it, then arm its barrier
-        const uint32_t eb = empty0 + 8u * stage;
-        if (!mbar_test(eb, phase ^ 1u) && !mbar_wait_timed(p, eb, phase ^ 1u, SITE_EMPTY, true, &cyc_empty)) {
-          ok = false;
-          break;
+      // wait until the MMAs released the stage, then arm its barrier
+      const uint32_t eb = empty0 + 8u * stage;
+      if (!mbar_test(eb, phase ^ 1u) && !mbar_wait_timed(p, eb, phase ^ 1u, SITE_EMPTY, true, &cyc_empty)) {
+        ok = false;
+        break;
+      }
+      if (CG == 1 || rank == 0) mbar_expect_tx(full0 + 8u * stage, CG * stage_bytes);
+      ++armed;
+#pragma unroll
+      for (int blk = 0; blk < KPS; ++blk) {
+        const CUtensorMap* ma = reinterpret_cast<const CUtensorMap*>(mapA0 + kMap * static_cast<uint64_t>(r));
+        const CUtensorMap* mb = reinterpret_cast<const CUtensorMap*>(mapB0 + kMap * static_cast<uint64_t>(AG ? 0 : r));
+        const uint32_t sa = sbase_stage + blk * A_STAGE_BYTES;
+        const uint32_t sb = sbase_stage + kps * A_STAGE_BYTES + blk * PP::B_STAGE_BYTES;
+        const int kx = kk * kelems;
+        if constexpr (CG == 1) {
+          const uint32_t fb = full0 + 8u * stage;
+          tma_load_3d(sa, ma, fb, kx, a_row, a_z);
+          tma_load_2d(sb, mb, fb, kx, b_row);
+        } else {
+          // both halves complete on the even CTA's barrier, which expects the pair's bytes
+          const uint32_t fl = full0_leader + 8u * stage;
+          tma_load_3d_pair(sa, ma, fl, kx, a_row, a_z);
+          tma_load_2d_pair(sb, mb, fl, kx, b_row);
         }
-        if (CG == 1 || rank == 0) mbar_expect_tx(full0 + 8u * stage, CG * stage_bytes);
-        ++armed;
-      }
-      const CUtensorMap* ma = reinterpret_cast<const CUtensorMap*>(mapA0 + kMap * static_cast<uint64_t>(r));
-      const CUtensorMap* mb = reinterpret_cast<const CUtensorMap*>(mapB0 + kMap * static_cast<uint64_t>(AG ? 0 : r));
-      const uint32_t sa = sbase_stage + blk * A_STAGE_BYTES;
-      const uint32_t sb = sbase_stage + kps * A_STAGE_BYTES + blk * PP::B_STAGE_BYTES;
-      const int kx = kk * kelems;
-      if constexpr (CG == 1) {
-        const uint32_t fb = full0 + 8u * stage;
-        tma_load_3d(sa, ma, fb, kx, a_row, a_z);
-        tma_load_2d(sb, mb, fb, kx, b_row);
-      } else {
-        // both halves complete on the even CTA's barrier, which expects the pair's bytes
-        const uint32_t fl = full0_leader + 8u * stage;
-        tma_load_3d_pair(sa, ma, fl, kx, a_row, a_z);
-        tma_load_2d_pair(sb, mb, fl, kx, b_row);
-      }
-      if (++kk == kb_per_seg) {  // next K segment: the next rank in ring order
-        kk = 0;
-        if (!AG && ++r == tp) r = 0;
-      }
-      if (++blk == kps) {
-        blk = 0;
-        if (++stage == nstages) {
-          stage = 0;
-          phase ^= 1u;
+        if (++kk == kb_per_seg) {  // next K segment: the next rank in ring order
+          kk = 0;
+          if (!AG && ++r == tp) r = 0;
         }
+      }
+      if (++stage == nstages) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
   }
@@ -764,9 +763,11 @@ __device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, uint32_
                          int total_tiles, int nkb) {
   const bool trace = p.trace_on != 0;
   if (p.op == OP_AG)
-    tma_loop<CG, true, SPLIT>(p, sbase, B, rank, g, G, total_tiles, nkb, trace);
+    (CG == 2 && p.kps == 2) ? tma_loop<CG, true, SPLIT, 2>(p, sbase, B, rank, g, G, total_tiles, nkb, trace)
+                            : tma_loop<CG, true, SPLIT, 1>(p, sbase, B, rank, g, G, total_tiles, nkb, trace);
   else
-    tma_loop<CG, false, false>(p, sbase, B, rank, g, G, total_tiles, nkb, trace);
+    (CG == 2 && p.kps == 2) ? tma_loop<CG, false, false, 2>(p, sbase, B, rank, g, G, total_tiles, nkb, trace)
+                            : tma_loop<CG, false, false, 1>(p, sbase, B, rank, g, G, total_tiles, nkb, trace);
 }
 
 // The MMA issuer.  tcgen05.mma issue returns only once the tensor core can take
