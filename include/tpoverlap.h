@@ -166,11 +166,12 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
 /*
  * Options (integers).  Keys:
  *   "producer_sms"     CTAs given to the chunk producer in overlapped AG; 0 (the
- *                      default) picks the largest count in [8, 32] that does
- *                      not add a round of GEMM tiles (rounded up to even for
- *                      pairs); with tail_split 1, the smallest count from 4
- *                      whose copy stays ahead of the GEMM by a model of both
- *                      rates
+ *                      default) picks, from a model of the copy and GEMM rates
+ *                      and the round-robin tile schedule, the fewest CTAs
+ *                      whose copy does not delay the GEMM (at most 32; even
+ *                      for pairs); with tail_split 1, the smallest count from
+ *                      4 whose copy stays ahead of the split schedule; an odd
+ *                      count for pairs is rounded up
  *   "gemm_ctas"        CTAs given to the GEMM (0 = all SMs not producing)
  *   "tail_split"       AG, modes 0-2 (default 0: whole tiles only, and every
  *                      grid, mode and producer count gives the same bits).

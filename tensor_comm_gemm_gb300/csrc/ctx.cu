@@ -116,6 +116,8 @@ struct tpo_ctx {
   const float* ks_scale_w = nullptr;
   int64_t last_producers = 0, last_gemm_ctas = 0, last_cta_group = 0;  // shape of the latest kernel launch
   int64_t last_split_tiles = 0;  // tail tiles of the latest kernel launch (AG tail split)
+  int64_t pc_key[4] = {-1, -1, -1, -1};  // producer count of the last AG launch shape (see producer_count)
+  int pc_val = 0;
   int64_t last_late_groups = 0;  // producer CTA groups that joined its GEMM
   uint32_t part_epoch = 0;       // launches with the AG tail split so far (part_ready value of this launch)
   // tensor-map cache: the maps of the latest kCacheWays pointer sets of each op
@@ -301,6 +303,29 @@ int gemm_grid(const tpo_ctx* c, int cg, int64_t want, int producers, int tiles) 
   return static_cast<int>(2 * pairs);
 }
 
+// Estimated end (seconds) of an overlapped AG launch with P producer CTAs and
+// whole tiles: each GEMM group runs its round-robin tiles one after another,
+// none before its chunk has landed (ring step j at j times the chunk copy
+// time), and the launch also lasts until the copy of the observer's own
+// chunk (last) is done.  Rates as measured next to a running GEMM: a producer
+// CTA moves up to 37 GB/s of chunk data and all of them together up to
+// 705 GB/s, taken 1.25 times slower for margin; a CTA group spends 0.33 us
+// per 128-byte K block of a tile.
+double overlap_end(const tpo_ctx* c, int cg, int tiles, int nkb, int64_t chunk_bytes, int P) {
+  const int G = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, P, tiles) / cg;
+  const int per_group = std::max(1, tiles / c->tp);
+  const double rate = std::min(37e9, 705e9 / P) / 1.25;
+  const double tau = static_cast<double>(chunk_bytes) / (P * rate);
+  const double t_tile = nkb * 0.33e-6;
+  double end = c->tp * tau;
+  for (int g = 0; g < G; ++g) {
+    double t_end = 0;
+    for (int t = g; t < tiles; t += G) t_end = std::max(t_end, (t / per_group) * tau) + t_tile;
+    end = std::max(end, t_end);
+  }
+  return end;
+}
+
 // Producer CTAs of an overlapped AG call.  An explicit option wins.
 //
 // With the tail split every GEMM group shortens the GEMM, so the count is the
@@ -311,10 +336,12 @@ int gemm_grid(const tpo_ctx* c, int cg, int64_t want, int producers, int tiles) 
 // writes, whatever its depth of copies in flight), and a CTA group spends
 // about 0.3 us per 128-byte K block of a tile.
 //
-// Without it (or when no count passes), whole rounds decide: the largest count
-// in [8, 32] that leaves the GEMM as many rounds of tiles as 8 producers would,
-// since SMs beyond the last full round are free for copying.
-int producer_count(const tpo_ctx* c, int cg, int tiles, int nkb, int64_t chunk_bytes, bool split) {
+// Without it (or when no count passes), a model of the whole-tile schedule
+// decides (overlap_end): the smallest count whose estimated end is within
+// 0.5 % of the best, i.e. the fewest copy SMs that do not delay the GEMM, so
+// that the copy disturbs the GEMM's loads least.  Computed once per launch
+// shape and kept in the context.
+int producer_count(tpo_ctx* c, int cg, int tiles, int nkb, int64_t chunk_bytes, bool split) {
   if (c->producer_sms > 0) return static_cast<int>(c->producer_sms) + ((cg == 2) ? static_cast<int>(c->producer_sms & 1) : 0);
   if (split) {
     const double rate = 47e9, t_tile = nkb * 0.3e-6;
@@ -338,14 +365,22 @@ int producer_count(const tpo_ctx* c, int cg, int tiles, int nkb, int64_t chunk_b
       if (ok) return P;
     }
   }
-  auto rounds = [&](int P) {
-    const int units = gemm_grid(c, cg, c->num_sms - P, P, tiles) / cg;
-    return (tiles + units - 1) / units;
-  };
-  const int r8 = rounds(8);
+  const int64_t key[4] = {cg, c->gemm_ctas, tiles, nkb};
+  if (std::memcmp(key, c->pc_key, sizeof(key)) == 0) return c->pc_val;
+  double best_end = 0;
+  double ends[33] = {};
+  for (int P = cg; P <= 32 && P <= c->num_sms - 2 * cg; P += cg) {
+    ends[P] = overlap_end(c, cg, tiles, nkb, chunk_bytes, P);
+    if (best_end == 0 || ends[P] < best_end) best_end = ends[P];
+  }
   int best = 8;
-  for (int P = 8; P <= 32 && P < c->num_sms - 2 * cg; P += cg)
-    if (rounds(P) == r8) best = P;
+  for (int P = cg; P <= 32 && P <= c->num_sms - 2 * cg; P += cg)
+    if (ends[P] <= best_end * 1.005) {
+      best = P;
+      break;
+    }
+  std::memcpy(c->pc_key, key, sizeof(key));
+  c->pc_val = best;
   return best;
 }
 

@@ -127,13 +127,14 @@ def test_split_every_observer_meets_the_bar(schedule):
 
 
 def test_split_join_schedule_large_shape():
-    """The join schedule on a large shape with the default grid: the producer
-    CTAs join, sampled parity, modes 0 and 1 agree bitwise."""
+    """The join schedule on a large shape (24 producer CTAs, so that their copy
+    ends early enough to join): sampled parity, modes 0 and 1 agree bitwise."""
     tp, n, k, m = 4, 4096, 1024, 4096
     wl = synth.make_ag(tp, n, k, m, seed=11, dist="normal", sigma=k ** -0.25)
     run = AgRun(wl)
     try:
         t.tpo_set_opt(run.ctx, "tail_split", 2)
+        t.tpo_set_opt(run.ctx, "producer_sms", 24)
         run.run()
         assert t.tpo_get_opt(run.ctx, "last_split_tiles") > 0 and t.tpo_get_opt(run.ctx, "last_late_groups") > 0
         bits = host_bits(run.y)
