@@ -299,3 +299,28 @@ def test_pair_variant_rejected_for_128_row_slots():
         assert_close(host_f64(run.y), ref_ag(wl))
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("tp,n,k,m,dtype", [(4, 4096, 4096, 4096, "bf16"), (8, 16384, 8192, 28672, "e4m3")])
+def test_default_producer_count_follows_the_schedule_model(tp, n, k, m, dtype):
+    """The library's default producer count for the C2 and C5 shapes is the
+    one the host schedule model (restated in test_schedule) picks."""
+    from test_schedule import producer_choice
+    fp8 = dtype == "e4m3"
+    el = torch.uint8 if fp8 else torch.bfloat16
+    xs = [torch.zeros((n // tp, k), dtype=el, device="cuda") for _ in range(tp)]
+    w = torch.zeros((m, k), dtype=el, device="cuda")
+    y = torch.empty((n, m), dtype=torch.bfloat16, device="cuda")
+    sx = torch.ones(1, device="cuda") if fp8 else None
+    ctx = t.tpo_ctx_create(tp, n, k, m, t.TPO_FP8_E4M3 if fp8 else t.TPO_BF16)
+    try:
+        t.tpo_ag_gemm(ctx, xs, w, y, sx, sx)
+        assert t.tpo_sync_status(ctx) == 0, t.tpo_last_error()
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        nkb = -(-k * (1 if fp8 else 2) // 128)
+        tiles = tp * (n // tp // 256) * (m // 256)
+        want = producer_choice(tp, tiles, nkb, n // tp * k * (1 if fp8 else 2), cg=2, num_sms=sms)
+        assert t.tpo_get_opt(ctx, "last_producer_ctas") == want
+        assert not torch.isnan(y).any()
+    finally:
+        t.tpo_ctx_destroy(ctx)

@@ -324,3 +324,52 @@ def test_late_groups_plan_for_the_headline_shape():
     assert plan is not None and plan[0] == 0 and plan[1] == 3
     loads = [sum(hi - lo for _, lo, hi, _, _ in segments(g, G, T, 64, 2, plan)) // 2 for g in range(G + L)]
     assert max(loads[:G]) < 4 * kbu and min(loads[G:]) > 0
+
+
+def gemm_grid(cg, want, P, tiles, max_pairs=76):
+    """The host's GEMM grid: single CTAs up to the tile count, or pairs up to
+    the co-resident pairs left next to the producers."""
+    if cg == 1:
+        return max(1, min(want, tiles))
+    return 2 * max(1, min(want // 2, max_pairs - P // 2, tiles))
+
+
+def overlap_end(tp, tiles, nkb, chunk_bytes, P, cg=2, num_sms=152):
+    """The host's model of an overlapped whole-tile launch (producer_count)."""
+    G = gemm_grid(cg, num_sms - P, P, tiles, max_pairs=num_sms // 2) // cg
+    per = max(1, tiles // tp)
+    rate = min(37e9, 705e9 / P) / 1.25
+    tau = chunk_bytes / (P * rate)
+    t_tile = nkb * 0.33e-6
+    end = tp * tau
+    for g in range(G):
+        t_end = 0.0
+        for t in range(g, tiles, G):
+            t_end = max(t_end, (t // per) * tau) + t_tile
+        end = max(end, t_end)
+    return end
+
+
+def producer_choice(tp, tiles, nkb, chunk_bytes, cg=2, num_sms=152):
+    ends = {P: overlap_end(tp, tiles, nkb, chunk_bytes, P, cg, num_sms)
+            for P in range(cg, 33, cg) if P <= num_sms - 2 * cg}
+    best = min(ends.values())
+    return min(P for P, e in ends.items() if e <= best * 1.005)
+
+
+def test_producer_model_choices():
+    """C2 (4096^3, 4 chunks of 8 MiB): the fewest producers whose copy keeps
+    ahead of 4 rounds; C5 (e4m3, 8 chunks of 16 MiB, 7168 tiles): a handful,
+    since the first gathered chunk is needed only after ~12 rounds."""
+    assert producer_choice(4, 256, 64, 1024 * 4096 * 2) == 14
+    assert producer_choice(8, 7168, 64, 2048 * 8192) == 4
+
+
+def test_producer_model_properties():
+    # more producers never delay the chunks: the model's end is monotone in
+    # the copy time as long as the GEMM grid is unchanged
+    for P in (2, 4, 8):
+        assert overlap_end(4, 256, 64, 1 << 23, P) >= overlap_end(4, 256, 64, 1 << 23, P + 2) or \
+            gemm_grid(2, 152 - P - 2, P + 2, 256) != gemm_grid(2, 152 - P, P, 256)
+    # a group never starts a tile before that tile's chunk could have landed
+    assert overlap_end(2, 2, 64, 1 << 30, 2) >= 2 * (1 << 30) / (2 * 37e9 / 1.25)
