@@ -477,62 +477,98 @@ struct Seg {
 };
 template <bool SPLIT>  // false: a kernel built without the split (round robin only)
 struct SegIter {
-  int g, s, nfull, G, whole_base, slot, tail_base, kbu, kps, ga, gb;
-  bool first;
-  long long wa, wb, pos, end;
-  __device__ long long start_of(int w) const {  // first tail unit of group w (w <= ga + gb)
-    if (w <= ga) return ga > 0 ? wa * w / ga : 0;
-    return wa + wb * (w - ga) / gb;
-  }
+  int g, s, nfull, G, whole_base, slot, kbu, kps;
+  // split only: the group's tail range, worked out once: a later part of one
+  // tile (K units [wr_lo, wr_hi)), whole tiles [tw0, tw1), and the first part
+  // of one more tile (K units [0, fin_hi)); ts steps through them
+  bool first, has_wr, has_fin;
+  int tail_base, ts, wr_t, wr_lo, wr_hi, tw0, tw1, fin_t, fin_hi, fin_w0, fin_nw;
   __device__ SegIter(const Params& p, int g_, int G_, int T, int nkb) : g(g_), s(0), G(G_), kps(p.kps) {
     kbu = nkb / kps;
-    ga = gb = 0;
-    wa = wb = pos = end = 0;
-    tail_base = 0;
     first = true;
+    has_wr = has_fin = false;
+    tail_base = ts = wr_t = wr_lo = wr_hi = tw0 = tw1 = fin_t = fin_hi = fin_w0 = fin_nw = 0;
     if (!SPLIT || !p.tail_split) {
       nfull = g < T && g < G ? (T - g + G - 1) / G : 0;
       whole_base = 0;
       slot = g;
       return;
     }
-    ga = p.split_ga;
-    gb = p.split_gb;
-    wa = p.split_wa;
-    wb = p.split_wb;
+    const int ga = p.split_ga, gb = p.split_gb;
+    const long long wa = p.split_wa, wb = p.split_wb;
+    auto start_of = [&](int w) -> long long {  // first tail unit of group w (w <= ga + gb)
+      if (w <= ga) return ga > 0 ? wa * w / ga : 0;
+      return wa + wb * (w - ga) / gb;
+    };
     first = p.split_tail_first != 0;
+    nfull = g < G ? p.split_full : 0;
     if (first) {
-      const int R = T - p.split_full * G;
-      nfull = g < G ? p.split_full : 0;
-      whole_base = R;
+      whole_base = T - p.split_full * G;
       slot = (g - ga + G) % G;
     } else {
-      nfull = g < G ? p.split_full : 0;
       whole_base = 0;
       slot = g;
       tail_base = p.split_full * G;
     }
-    if (g < ga + gb) {
-      pos = start_of(g);
-      end = start_of(g + 1);
+    if (g >= ga + gb) return;
+    const long long pos = start_of(g), end = start_of(g + 1);
+    long long p2 = pos;
+    if (pos < end && pos % kbu != 0) {  // the range starts inside a tile: a later part of it
+      const long long t0 = pos / kbu;
+      wr_lo = static_cast<int>(pos - t0 * kbu);
+      wr_hi = static_cast<int>(min(static_cast<long long>(kbu), wr_lo + (end - pos)));
+      wr_t = static_cast<int>(t0);
+      has_wr = true;
+      p2 = pos + (wr_hi - wr_lo);
+    }
+    if (p2 < end) {  // from a tile boundary: whole tiles, then perhaps the first part of one more
+      tw0 = static_cast<int>(p2 / kbu);
+      tw1 = static_cast<int>(end / kbu);
+      const long long rem = end - static_cast<long long>(tw1) * kbu;
+      if (rem > 0) {
+        has_fin = true;
+        fin_t = tw1;
+        fin_hi = static_cast<int>(rem);
+        fin_w0 = g + 1;
+        const long long tile_end = static_cast<long long>(tw1 + 1) * kbu;
+        for (int w = g + 1; w < ga + gb && start_of(w) < tile_end; ++w) ++fin_nw;
+      }
     }
   }
   __device__ bool tail_next(Seg& o) {
-    if (pos >= end) return false;
-    const long long tt = pos / kbu;
-    const int lo = static_cast<int>(pos - tt * kbu);
-    const int hi = static_cast<int>(min(static_cast<long long>(kbu), lo + (end - pos)));
-    o.t = tail_base + static_cast<int>(tt);
-    o.kb_lo = lo * kps;
-    o.kb_hi = hi * kps;
-    o.kind = (lo == 0 && hi == kbu) ? SEG_WHOLE : (lo == 0 ? SEG_FINISH : SEG_WRITE);
-    if (o.kind == SEG_FINISH) {
-      const long long tile_end = (tt + 1) * kbu;
-      o.w0 = g + 1;
-      for (int w = g + 1; w < ga + gb && start_of(w) < tile_end; ++w) ++o.nw;
+    if (ts == 0) {
+      ts = 1;
+      if (has_wr) {
+        o.t = tail_base + wr_t;
+        o.kb_lo = wr_lo * kps;
+        o.kb_hi = wr_hi * kps;
+        o.kind = SEG_WRITE;
+        return true;
+      }
     }
-    pos += hi - lo;
-    return true;
+    if (ts == 1) {
+      if (tw0 < tw1) {
+        o.t = tail_base + tw0++;
+        o.kb_lo = 0;
+        o.kb_hi = kbu * kps;
+        o.kind = SEG_WHOLE;
+        return true;
+      }
+      ts = 2;
+    }
+    if (ts == 2) {
+      ts = 3;
+      if (has_fin) {
+        o.t = tail_base + fin_t;
+        o.kb_lo = 0;
+        o.kb_hi = fin_hi * kps;
+        o.kind = SEG_FINISH;
+        o.w0 = fin_w0;
+        o.nw = fin_nw;
+        return true;
+      }
+    }
+    return false;
   }
   __device__ bool next(Seg& o) {
     if constexpr (SPLIT) {
@@ -896,14 +932,101 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
   uint32_t ul = 0, nst = 0;
   unsigned long long cyc_tfull = 0;
   bool ok_all = true;
+  // A part of a split tile, on its own path so that whole tiles run the same
+  // code as in the build without the split.  A later part (SEG_WRITE) goes to
+  // this CTA's workspace block as unscaled fp32 and is published per warp; the
+  // first part (SEG_FINISH) waits for the later parts' flags, adds them in K
+  // order and stores the tile like a whole one.
+  auto split_part = [&](const Tile& T, const Seg& sg, uint32_t ul_) -> bool {
+    const bool write = sg.kind == SEG_WRITE;
+    if (!write)
+      for (int j = 0; j < sg.nw; ++j)
+        if (!wait_partial(p, &p.words->part_ready[((sg.w0 + j) * CG + static_cast<int>(rank)) * EPI_WARPS + quad]))
+          return false;
+    const uint32_t acc = ul_ & 1u;
+    const uint32_t bar = B.tfull0 + 8u * acc, par = (ul_ >> 1) & 1u;
+    int okw = (lane == 0) ? (mbar_wait_timed(p, bar, par, SITE_TMEM_FULL, true, &cyc_tfull) ? 1 : 0) : 0;
+    if (!__shfl_sync(0xffffffffu, okw, 0)) return false;
+    mbar_wait(p, bar, par, SITE_TMEM_FULL, false);
+    tc_fence_after();
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+#pragma unroll 1
+    for (int c = 0; c < BN / EPI_COLS; ++c) {
+      uint32_t r[32];
+      tmem_ld32_sync(taddr + c * EPI_COLS, r);
+      if (c == BN / EPI_COLS - 1) {  // accumulator fully read: hand it back to the MMA issuer
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (CG == 1)
+            mbar_arrive(B.tempty0 + 8u * acc);
+          else
+            mbar_arrive_cluster(map_to_rank(B.tempty0 + 8u * acc, 0));
+        }
+      }
+      if (write) {
+        uint4* w4 = const_cast<uint4*>(part_lane) + static_cast<size_t>(cta) * (BM * BN / 4) + c * 8 * BM;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) st_global_v4_keep(w4 + v * BM, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3], ws_pol);
+        continue;
+      }
+      for (int j = 0; j < sg.nw; ++j) {
+        const uint4* w4 =
+            part_lane + static_cast<size_t>((sg.w0 + j) * CG + static_cast<int>(rank)) * (BM * BN / 4) + c * 8 * BM;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          uint32_t x[4];
+          ld_global_v4_keep(w4 + v * BM, x, ws_pol);
+          r[4 * v] = __float_as_uint(__uint_as_float(r[4 * v]) + __uint_as_float(x[0]));
+          r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + __uint_as_float(x[1]));
+          r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + __uint_as_float(x[2]));
+          r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + __uint_as_float(x[3]));
+        }
+      }
+      const int ox = T.col + c * EPI_COLS, oy = T.y_row + row_off + quad * 32;
+      if (ox >= p.m || oy >= p.y_rows) continue;  // wholly past the output's edge: no buffer, no store
+      uint32_t packed[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * scale,
+                                                       __uint_as_float(r[2 * j + 1]) * scale);
+        packed[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      const uint32_t buf = ebase + (nst & 1u) * EPI_BUF_BYTES;
+      ++nst;
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const uint32_t addr = buf + lane * 64 + (static_cast<uint32_t>(ch ^ ((lane >> 1) & 3)) << 4);
+        st_shared_v4(addr, packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(&p.mapY[T.y_map], buf, ox, oy, T.y_z);
+        bulk_commit();
+      }
+    }
+    if (write) {  // this warp's rows of the partial are stored: publish them
+      __syncwarp();
+      if (lane == 0 && cta != p.skip_part) {
+        __threadfence();
+        st_release(&p.words->part_ready[cta * EPI_WARPS + quad], p.part_target);
+      }
+    }
+    return true;
+  };
   SegIter<SPLIT> it(p, g, G, total_tiles, p.num_segs * p.kb_per_seg);
   Seg sg;
   while (ok_all && it.next(sg)) {
     const Tile T = tile_at<PP::TILE_M>(p, sg.t);
-    if (SPLIT && sg.kind == SEG_FINISH) {  // the later parts' partials of this warp's rows must be stored
-      for (int j = 0; j < sg.nw && ok_all; ++j)
-        ok_all = wait_partial(p, &p.words->part_ready[((sg.w0 + j) * CG + static_cast<int>(rank)) * EPI_WARPS + quad]);
-      if (!ok_all) break;
+    if constexpr (SPLIT) {
+      if (sg.kind != SEG_WHOLE) {  // a part of a split tile (AG: one accumulation unit)
+        ok_all = split_part(T, sg, ul);
+        ++ul;
+        continue;
+      }
     }
     for (int u = 0; u < units; ++u, ++ul) {
       const uint32_t acc = ul & 1u;
@@ -980,30 +1103,6 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
               mbar_arrive_cluster(map_to_rank(B.tempty0 + 8u * acc, 0));
           }
         }
-        if (SPLIT && sg.kind == SEG_WRITE) {  // a later part of a split tile: keep the fp32 partial
-          uint4* w4 = const_cast<uint4*>(part_lane) + static_cast<size_t>(cta) * (BM * BN / 4) + c * 8 * BM;
-#pragma unroll
-          for (int v = 0; v < 8; ++v) st_global_v4_keep(w4 + v * BM, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3], ws_pol);
-          return;
-        }
-        if (SPLIT && sg.kind == SEG_FINISH) {  // the first part: add the later parts in K order
-          for (int j = 0; j < sg.nw; ++j) {
-            const uint4* w4 = part_lane + static_cast<size_t>((sg.w0 + j) * CG + static_cast<int>(rank)) * (BM * BN / 4) +
-                              c * 8 * BM;
-            uint32_t h[32];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              uint32_t x[4];
-              ld_global_v4_keep(w4 + v * BM, x, ws_pol);
-              h[4 * v] = x[0];
-              h[4 * v + 1] = x[1];
-              h[4 * v + 2] = x[2];
-              h[4 * v + 3] = x[3];
-            }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(h[e]));
-          }
-        }
         float out_scale = scale;
         if (rmode) {
           // this rank's partial, added in ring order to the running sum
@@ -1070,13 +1169,6 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
         const uint32_t none[32] = {};
 #pragma unroll 1
         for (int c = 0; c < BN / EPI_COLS; ++c) chunk(c, none, false);
-      }
-    }
-    if (SPLIT && ok_all && sg.kind == SEG_WRITE) {  // this warp's rows of the partial are stored: publish them
-      __syncwarp();
-      if (lane == 0 && cta != p.skip_part) {
-        __threadfence();
-        st_release(&p.words->part_ready[cta * EPI_WARPS + quad], p.part_target);
       }
     }
     if (ok_all && p.op != OP_AG && lane == 0) {  // this warp's rows of the tile are in memory: count them
