@@ -134,9 +134,10 @@ struct tpo_ctx {
 namespace {
 
 int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
+  using Field = int64_t tpo_ctx::*;
   struct E {
     const char* k;
-    int64_t tpo_ctx::*f;
+    Field f;
     int64_t lo, hi;
   };
   const E table[] = {
