@@ -191,3 +191,54 @@ def test_missing_partial_times_out_and_context_recovers():
             assert_close(host_f64(run.y), ref)
     finally:
         run.close()
+
+
+def test_join_schedule_with_slow_producer_keeps_bits():
+    """Schedule 2 with a producer that spins before every publish: the producer
+    CTAs join late, the finishers wait longer for their partials, and the
+    result is still the bits of the sequential run (same plan)."""
+    wl = synth.make_ag(4, 2048, 512, 768, seed=14, dist="uniform")
+    run = AgRun(wl)
+    try:
+        t.tpo_set_opt(run.ctx, "tail_split", 2)
+        t.tpo_set_opt(run.ctx, "gemm_ctas", 4)
+        t.tpo_set_opt(run.ctx, "producer_sms", 8)
+        t.tpo_set_opt(run.ctx, "mode", 1)
+        run.run()
+        assert t.tpo_get_opt(run.ctx, "last_late_groups") > 0
+        want = host_bits(run.y)
+        t.tpo_set_opt(run.ctx, "mode", 0)
+        t.tpo_set_opt(run.ctx, "debug_delay_ns", 200000)
+        for _ in range(2):
+            run.y.fill_(float("nan"))
+            run.run()
+            assert np.array_equal(host_bits(run.y), want)
+    finally:
+        run.close()
+
+
+def test_join_schedule_skipped_chunk_times_out_and_recovers():
+    """Schedule 2 with a chunk the producer never publishes: the waits on it
+    (GEMM and joined producer CTAs alike) end with a timeout; the context then
+    gives correct results."""
+    wl = synth.make_ag(4, 2048, 512, 768, seed=15, dist="uniform")
+    ref = oracle.ag(oracle.gather(wl.x), wl.w[0])
+    run = AgRun(wl)
+    try:
+        t.tpo_set_opt(run.ctx, "tail_split", 2)
+        t.tpo_set_opt(run.ctx, "gemm_ctas", 4)
+        t.tpo_set_opt(run.ctx, "producer_sms", 8)
+        t.tpo_set_opt(run.ctx, "wait_timeout_ms", 50)
+        t.tpo_set_opt(run.ctx, "debug_skip_chunk", 2)
+        t.tpo_ag_gemm(run.ctx, run.xs, run.w, run.y)
+        assert t.tpo_sync_status(run.ctx) == 4
+        code, site, _, _ = t.tpo_last_device_error(run.ctx)
+        assert code == 1 and site in (1, 2, 3, 4, 5, 8)
+        t.tpo_set_opt(run.ctx, "debug_skip_chunk", -1)
+        t.tpo_set_opt(run.ctx, "wait_timeout_ms", 2000)
+        run.y.fill_(float("nan"))
+        run.run()
+        assert t.tpo_get_opt(run.ctx, "last_late_groups") > 0
+        assert_close(host_f64(run.y), ref)
+    finally:
+        run.close()
