@@ -324,3 +324,34 @@ def test_default_producer_count_follows_the_schedule_model(tp, n, k, m, dtype):
         assert not torch.isnan(y).any()
     finally:
         t.tpo_ctx_destroy(ctx)
+
+
+def test_two_contexts_on_two_streams():
+    """An AG context and a GEMM+RS context enqueued on two side streams at the
+    same time: both results meet the oracle bar (the overlapped AG launch is
+    cooperative, so its producer and GEMM CTAs are placed together whatever
+    the other stream runs)."""
+    from gpu_util import KsplitRun
+    wl_ag = synth.make_ag(4, 2048, 512, 768, seed=21, dist="uniform")
+    wl_rs = synth.make_ksplit("rs", 4, 2048, 1024, 512, seed=22, sigma=1024 ** -0.25)
+    ref_a = ref_ag(wl_ag)
+    ref_r = oracle.ksplit(wl_rs.x, wl_rs.w)
+    ag, rs = AgRun(wl_ag), KsplitRun(wl_rs)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    try:
+        torch.cuda.synchronize()
+        for _ in range(3):
+            ag.y.fill_(float("nan"))
+            for y in rs.yb:
+                y.fill_(float("nan"))
+            torch.cuda.synchronize()
+            t.tpo_ag_gemm(ag.ctx, ag.xs, ag.w, ag.y, stream=s1)
+            t.tpo_gemm_rs(rs.ctx, rs.xs, rs.ws, rs.yb, stream=s2)
+            t.tpo_ag_gemm(ag.ctx, ag.xs, ag.w, ag.y, stream=s1)
+            assert t.tpo_sync_status(ag.ctx) == 0 and t.tpo_sync_status(rs.ctx) == 0
+            torch.cuda.synchronize()
+            assert_close(host_f64(ag.y), ref_a)
+            assert_close(np.concatenate([host_f64(y) for y in rs.yb], 0), ref_r)
+    finally:
+        ag.close()
+        rs.close()
