@@ -180,7 +180,8 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      2: the producer CTAs join the GEMM once their copy is
  *                      done, and the last tiles are divided along K between
  *                      the GEMM CTAs (a short share each) and them (the rest),
- *                      sized from a model of both rates.  Each later K part of
+ *                      sized from a model of both rates; 3: as 1 but the
+ *                      leftover tiles come after the whole rounds.  Each later K part of
  *                      a split tile is an fp32 partial in the context's
  *                      workspace, added in K order to the first part before
  *                      the bf16 rounding, so the result depends on the plan:

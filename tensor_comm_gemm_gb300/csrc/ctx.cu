@@ -101,6 +101,9 @@ struct tpo_ctx {
   uint8_t* staging = nullptr;
   size_t staging_bytes = 0;
   float* ws = nullptr;  // epilogue-reduction running sums, one BM x BN fp32 block per SM
+  tpo::TailDesc* tail_dev = nullptr;               // AG tail split: per-group schedules (device)
+  tpo::TailDesc tail_host[tpo::MAX_GEMM_CTAS] = {};  // and their host copy
+  int64_t tail_key[11] = {};                       // the plan the device table holds
   tpo::DevWords* words = nullptr;
   uint32_t target[TPO_MAX_TP] = {};  // per slot: counter value once the latest call published it
   uint32_t done_target = 0;  // RS/AR done-counter value after the latest call
@@ -154,7 +157,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
       {"cta_group", &tpo_ctx::cta_group, 0, 2},
       {"cooperative", &tpo_ctx::cooperative, 0, 1},
       {"reduce", &tpo_ctx::reduce, 0, 2},
-      {"tail_split", &tpo_ctx::tail_split, 0, 2},
+      {"tail_split", &tpo_ctx::tail_split, 0, 3},
       {"debug_skip_partial", &tpo_ctx::debug_skip_partial, -1, tpo::MAX_GEMM_CTAS - 1},
   };
   for (const E& e : table)
@@ -180,6 +183,7 @@ void destroy_all(tpo_ctx* c) {
   if (c->aux) cudaStreamSynchronize(c->aux);
   if (c->staging) cudaFree(c->staging);
   if (c->ws) cudaFree(c->ws);
+  if (c->tail_dev) cudaFree(c->tail_dev);
   if (c->words) cudaFree(c->words);
   if (c->copy) cudaStreamSynchronize(c->copy);
   if (c->last) cudaEventDestroy(c->last);
@@ -397,8 +401,10 @@ int producer_count(tpo_ctx* c, int cg, int tiles, int nkb, int64_t chunk_bytes, 
 // end instead.  The plan only moves time: any plan gives exact tiles.
 //
 // With L == 0 (or no time for the late groups) the R = T mod G leftover tiles
-// go first and are shared among min(G, TAIL_SPLIT R) GEMM groups.
-void plan_split(const tpo_ctx* c, Params& p, int tiles, int G, int L) {
+// are shared among min(G, TAIL_SPLIT R) GEMM groups, first (schedule 1) or
+// after the whole rounds (`last`, schedule 3: the operands are then warm in
+// L2, where split parts that start at different K offsets find them).
+void plan_split(const tpo_ctx* c, Params& p, int tiles, int G, int L, bool last) {
   const long long kbu = p.kb_per_seg / p.kps;  // K units of a tile (AG: one K segment)
   p.tail_split = 0;
   p.late_groups = 0;
@@ -431,12 +437,76 @@ void plan_split(const tpo_ctx* c, Params& p, int tiles, int G, int L) {
   const int full = tiles / G, R = tiles - full * G;
   if (R == 0) return;
   p.tail_split = 1;
-  p.split_tail_first = 1;
+  p.split_tail_first = last ? 0 : 1;
   p.split_full = full;
   p.split_ga = std::min(G, tpo::TAIL_SPLIT * R);
   p.split_wa = static_cast<long long>(R) * kbu;
   p.split_gb = 0;
   p.split_wb = 0;
+}
+
+// The schedule of CTA group g under the plan in `p` (see TailDesc), in the
+// 32-bit arithmetic the plan's bounds allow.
+tpo::TailDesc make_tail(const Params& p, int g, int G, int T, int kbu_i) {
+  tpo::TailDesc d{};
+  const uint32_t kbu = static_cast<uint32_t>(kbu_i);
+  const uint32_t ga = static_cast<uint32_t>(p.split_ga), gb = static_cast<uint32_t>(p.split_gb);
+  const uint32_t wa = static_cast<uint32_t>(p.split_wa), wb = static_cast<uint32_t>(p.split_wb);
+  auto start_of = [&](uint32_t w) -> uint32_t {  // first tail unit of group w (w <= ga + gb)
+    if (w <= ga) return ga > 0 ? wa * w / ga : 0u;
+    return wa + wb * (w - ga) / gb;
+  };
+  d.first = p.split_tail_first != 0;
+  d.nfull = g < G ? p.split_full : 0;
+  if (d.first) {
+    d.whole_base = T - p.split_full * G;
+    d.slot = (g - static_cast<int>(ga) + G) % G;
+  } else {
+    d.slot = g;
+    d.tail_base = p.split_full * G;
+  }
+  const uint32_t ug = static_cast<uint32_t>(g);
+  if (ug >= ga + gb) return d;
+  const uint32_t pos = start_of(ug), end = start_of(ug + 1);
+  uint32_t p2 = pos;
+  if (pos < end && pos % kbu != 0) {  // the range starts inside a tile: a later part of it
+    const uint32_t t0 = pos / kbu;
+    d.wr_lo = static_cast<int>(pos - t0 * kbu);
+    d.wr_hi = static_cast<int>(std::min(kbu, static_cast<uint32_t>(d.wr_lo) + (end - pos)));
+    d.wr_t = static_cast<int>(t0);
+    d.has_wr = 1;
+    p2 = pos + static_cast<uint32_t>(d.wr_hi - d.wr_lo);
+  }
+  if (p2 < end) {  // from a tile boundary: whole tiles, then perhaps the first part of one more
+    d.tw0 = static_cast<int>(p2 / kbu);
+    d.tw1 = static_cast<int>(end / kbu);
+    const uint32_t rem = end - static_cast<uint32_t>(d.tw1) * kbu;
+    if (rem > 0) {
+      d.has_fin = 1;
+      d.fin_t = d.tw1;
+      d.fin_hi = static_cast<int>(rem);
+      d.fin_w0 = g + 1;
+      const uint32_t tile_end = static_cast<uint32_t>(d.tw1 + 1) * kbu;
+      for (uint32_t w = ug + 1; w < ga + gb && start_of(w) < tile_end; ++w) ++d.fin_nw;
+    }
+  }
+  return d;
+}
+
+// Fill the device table of per-group schedules for the plan in `p` (copied
+// only when the plan changed) and point the launch at it.
+tpo_status upload_tails(tpo_ctx* c, Params& p, int T, int G, cudaStream_t s) {
+  const int groups = G + p.late_groups, kbu = p.kb_per_seg / p.kps;
+  const int64_t key[11] = {p.split_tail_first, p.split_full, p.split_ga, p.split_gb, p.split_wa,
+                           p.split_wb, T, G, groups, kbu, p.kps};
+  p.tail_tab = c->tail_dev;
+  if (std::memcmp(key, c->tail_key, sizeof(key)) == 0) return TPO_OK;
+  if (groups > tpo::MAX_GEMM_CTAS) return fail(TPO_ERR_INVALID_ARG, "too many CTA groups for the tail split");
+  for (int g = 0; g < groups; ++g) c->tail_host[g] = make_tail(p, g, G, T, kbu);
+  cudaError_t e = cudaMemcpyAsync(c->tail_dev, c->tail_host, sizeof(tpo::TailDesc) * groups, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "tail table upload");
+  std::memcpy(c->tail_key, key, sizeof(key));
+  return TPO_OK;
 }
 
 // Validation shared by RS and AR.
@@ -554,6 +624,7 @@ tpo_ctx* tpo_ctx_create(int tp, int64_t n, int64_t k, int64_t m, int dtype) {
   e = cudaMalloc(&c->words, sizeof(tpo::DevWords));
   if (e == cudaSuccess)
     e = cudaMalloc(&c->ws, static_cast<size_t>(c->num_sms) * tpo::BM * tpo::BN * sizeof(float));
+  if (e == cudaSuccess) e = cudaMalloc(&c->tail_dev, sizeof(c->tail_host));
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->aux, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->last, cudaEventDisableTiming);
   if (e == cudaSuccess) {
@@ -703,8 +774,16 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
     p.num_gemm = G;
     p.copy_on = copy ? 1 : 0;
     if (split && P + G <= c->num_sms && P + G <= tpo::MAX_GEMM_CTAS)
-      plan_split(c, p, tiles, G / cg, split == 2 ? P / cg : 0);
-    if (p.tail_split) p.part_target = ++c->part_epoch;
+      plan_split(c, p, tiles, G / cg, split == 2 ? P / cg : 0, split == 3);
+    // the kernel's tail arithmetic is 32-bit: units times groups must stay below 2^31
+    if (p.tail_split && (p.split_wa * (p.split_ga + 1) >= (1ll << 31) || p.split_wb * (p.split_gb + 1) >= (1ll << 31) ||
+                         static_cast<long long>(tiles) * (p.kb_per_seg / p.kps) >= (1ll << 31)))
+      p.tail_split = p.late_groups = 0;
+    if (p.tail_split) {
+      p.part_target = ++c->part_epoch;
+      const tpo_status ts = upload_tails(c, p, tiles, G / cg, s);
+      if (ts != TPO_OK) return ts;
+    }
     if (!copy && !p.late_groups) p.num_producers = 0;  // nothing for the producer CTAs to do
     const int grid = p.num_producers + p.num_gemm;
     return launch(c, p, grid, coop || p.tail_split != 0, s);  // split tiles: every CTA co-resident

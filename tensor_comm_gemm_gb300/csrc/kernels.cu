@@ -478,12 +478,12 @@ struct Seg {
 template <bool SPLIT>  // false: a kernel built without the split (round robin only)
 struct SegIter {
   int g, s, nfull, G, whole_base, slot, kbu, kps;
-  // split only: the group's tail range, worked out once: a later part of one
-  // tile (K units [wr_lo, wr_hi)), whole tiles [tw0, tw1), and the first part
-  // of one more tile (K units [0, fin_hi)); ts steps through them
-  bool first, has_wr, has_fin;
+  bool first;
   int tail_base, ts, wr_t, wr_lo, wr_hi, tw0, tw1, fin_t, fin_hi, fin_w0, fin_nw;
-  __device__ SegIter(const Params& p, int g_, int G_, int T, int nkb) : g(g_), s(0), G(G_), kps(p.kps) {
+  bool has_wr, has_fin;
+  // `tail`: the CTA's TailDesc in shared memory (split builds with the split on)
+  __device__ SegIter(const Params& p, int g_, int G_, int T, int nkb, const TailDesc* tail)
+      : g(g_), s(0), G(G_), kps(p.kps) {
     kbu = nkb / kps;
     first = true;
     has_wr = has_fin = false;
@@ -494,46 +494,23 @@ struct SegIter {
       slot = g;
       return;
     }
-    const int ga = p.split_ga, gb = p.split_gb;
-    const long long wa = p.split_wa, wb = p.split_wb;
-    auto start_of = [&](int w) -> long long {  // first tail unit of group w (w <= ga + gb)
-      if (w <= ga) return ga > 0 ? wa * w / ga : 0;
-      return wa + wb * (w - ga) / gb;
-    };
-    first = p.split_tail_first != 0;
-    nfull = g < G ? p.split_full : 0;
-    if (first) {
-      whole_base = T - p.split_full * G;
-      slot = (g - ga + G) % G;
-    } else {
-      whole_base = 0;
-      slot = g;
-      tail_base = p.split_full * G;
-    }
-    if (g >= ga + gb) return;
-    const long long pos = start_of(g), end = start_of(g + 1);
-    long long p2 = pos;
-    if (pos < end && pos % kbu != 0) {  // the range starts inside a tile: a later part of it
-      const long long t0 = pos / kbu;
-      wr_lo = static_cast<int>(pos - t0 * kbu);
-      wr_hi = static_cast<int>(min(static_cast<long long>(kbu), wr_lo + (end - pos)));
-      wr_t = static_cast<int>(t0);
-      has_wr = true;
-      p2 = pos + (wr_hi - wr_lo);
-    }
-    if (p2 < end) {  // from a tile boundary: whole tiles, then perhaps the first part of one more
-      tw0 = static_cast<int>(p2 / kbu);
-      tw1 = static_cast<int>(end / kbu);
-      const long long rem = end - static_cast<long long>(tw1) * kbu;
-      if (rem > 0) {
-        has_fin = true;
-        fin_t = tw1;
-        fin_hi = static_cast<int>(rem);
-        fin_w0 = g + 1;
-        const long long tile_end = static_cast<long long>(tw1 + 1) * kbu;
-        for (int w = g + 1; w < ga + gb && start_of(w) < tile_end; ++w) ++fin_nw;
-      }
-    }
+    const TailDesc d = *tail;
+    first = d.first != 0;
+    nfull = d.nfull;
+    whole_base = d.whole_base;
+    slot = d.slot;
+    tail_base = d.tail_base;
+    has_wr = d.has_wr != 0;
+    wr_t = d.wr_t;
+    wr_lo = d.wr_lo;
+    wr_hi = d.wr_hi;
+    tw0 = d.tw0;
+    tw1 = d.tw1;
+    has_fin = d.has_fin != 0;
+    fin_t = d.fin_t;
+    fin_hi = d.fin_hi;
+    fin_w0 = d.fin_w0;
+    fin_nw = d.fin_nw;
   }
   __device__ bool tail_next(Seg& o) {
     if (ts == 0) {
@@ -712,7 +689,7 @@ struct Bars {
 // position, stage and phase), so that refills follow stage releases closely.
 template <int CG, bool AG, bool SPLIT, int KPS>
 __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_t rank, int g, int G,
-                         int total_tiles, int nkb, bool trace) {
+                         int total_tiles, int nkb, bool trace, const TailDesc* tail) {
   using PP = Pipe<CG>;
   const uint64_t mapA0 = reinterpret_cast<uint64_t>(&p.mapA[0]);
   const uint64_t mapB0 = reinterpret_cast<uint64_t>(&p.mapB[0]);
@@ -728,7 +705,7 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
   uint32_t ready = 0, stage = 0, phase = 0, armed = 0;
   bool ok = true;
   unsigned long long cyc_empty = 0;
-  SegIter<SPLIT> it(p, g, G, total_tiles, nkb);
+  SegIter<SPLIT> it(p, g, G, total_tiles, nkb, tail);
   Seg sg;
   while (ok && it.next(sg)) {
     const Tile T = tile_at<PP::TILE_M>(p, sg.t);
@@ -796,14 +773,14 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
 
 template <int CG, bool SPLIT>
 __device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, uint32_t rank, int g, int G,
-                         int total_tiles, int nkb) {
+                         int total_tiles, int nkb, const TailDesc* tail) {
   const bool trace = p.trace_on != 0;
   if (p.op == OP_AG)
-    (CG == 2 && p.kps == 2) ? tma_loop<CG, true, SPLIT, 2>(p, sbase, B, rank, g, G, total_tiles, nkb, trace)
-                            : tma_loop<CG, true, SPLIT, 1>(p, sbase, B, rank, g, G, total_tiles, nkb, trace);
+    (CG == 2 && p.kps == 2) ? tma_loop<CG, true, SPLIT, 2>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail)
+                            : tma_loop<CG, true, SPLIT, 1>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail);
   else
-    (CG == 2 && p.kps == 2) ? tma_loop<CG, false, false, 2>(p, sbase, B, rank, g, G, total_tiles, nkb, trace)
-                            : tma_loop<CG, false, false, 1>(p, sbase, B, rank, g, G, total_tiles, nkb, trace);
+    (CG == 2 && p.kps == 2) ? tma_loop<CG, false, false, 2>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail)
+                            : tma_loop<CG, false, false, 1>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail);
 }
 
 // The MMA issuer.  tcgen05.mma issue returns only once the tensor core can take
@@ -815,7 +792,7 @@ __device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, uint32_
 // stage's MMAs issue back to back with no per-block bookkeeping between them.
 template <int CG, bool FP8, bool SPLIT, int KPS>
 __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
-                         int total_tiles, int nkb, bool trace) {
+                         int total_tiles, int nkb, bool trace, const TailDesc* tail) {
   using PP = Pipe<CG>;
   constexpr uint32_t idesc = make_idesc(FP8, PP::TILE_M);
   constexpr uint32_t kps = KPS;
@@ -836,7 +813,7 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   uint32_t stage = 0, phase = 0, ul = 0, issued = 0;
   bool ok = true;
   unsigned long long cyc_full = 0, cyc_tempty = 0;
-  SegIter<SPLIT> it(p, g, G, total_tiles, nkb);
+  SegIter<SPLIT> it(p, g, G, total_tiles, nkb, tail);
   Seg sg;
   while (ok && it.next(sg))
    for (int u = 0; u < units; ++u, ++ul) {
@@ -890,24 +867,24 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
 
 template <int CG, bool SPLIT>
 __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
-                         int total_tiles, int nkb) {
+                         int total_tiles, int nkb, const TailDesc* tail) {
   const bool trace = p.trace_on != 0;
   if (CG == 2 && p.kps == 2) {
     if (p.fp8)
-      mma_loop<CG, true, SPLIT, 2>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
+      mma_loop<CG, true, SPLIT, 2>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace, tail);
     else
-      mma_loop<CG, false, SPLIT, 2>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
+      mma_loop<CG, false, SPLIT, 2>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace, tail);
   } else {
     if (p.fp8)
-      mma_loop<CG, true, SPLIT, 1>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
+      mma_loop<CG, true, SPLIT, 1>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace, tail);
     else
-      mma_loop<CG, false, SPLIT, 1>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace);
+      mma_loop<CG, false, SPLIT, 1>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace, tail);
   }
 }
 
 template <int CG, bool SPLIT>
 __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, const Bars& B, uint32_t rank, int g,
-                              int G, int total_tiles) {
+                              int G, int total_tiles, const TailDesc* tail) {
   using PP = Pipe<CG>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;  // tensor-memory lanes this warp may read: [32*quad, 32*quad+32)
@@ -950,8 +927,30 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
     mbar_wait(p, bar, par, SITE_TMEM_FULL, false);
     tc_fence_after();
     const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
+    // the first later part's partial is fetched one chunk ahead of its use
+    auto load_part = [&](int j, int c, uint32_t(&h)[32]) {
+      const uint4* w4 =
+          part_lane + static_cast<size_t>((sg.w0 + j) * CG + static_cast<int>(rank)) * (BM * BN / 4) + c * 8 * BM;
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        uint32_t x[4];
+        ld_global_v4_keep(w4 + v * BM, x, ws_pol);
+        h[4 * v] = x[0];
+        h[4 * v + 1] = x[1];
+        h[4 * v + 2] = x[2];
+        h[4 * v + 3] = x[3];
+      }
+    };
+    auto add_part = [&](uint32_t(&r)[32], const uint32_t(&h)[32]) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(h[e]));
+    };
+    uint32_t pa[32];
+    if (!write && sg.nw > 0) load_part(0, 0, pa);
 #pragma unroll 1
     for (int c = 0; c < BN / EPI_COLS; ++c) {
+      uint32_t pn[32];
+      if (!write && sg.nw > 0 && c + 1 < BN / EPI_COLS) load_part(0, c + 1, pn);
       uint32_t r[32];
       tmem_ld32_sync(taddr + c * EPI_COLS, r);
       if (c == BN / EPI_COLS - 1) {  // accumulator fully read: hand it back to the MMA issuer
@@ -970,19 +969,14 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
         for (int v = 0; v < 8; ++v) st_global_v4_keep(w4 + v * BM, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3], ws_pol);
         continue;
       }
-      for (int j = 0; j < sg.nw; ++j) {
-        const uint4* w4 =
-            part_lane + static_cast<size_t>((sg.w0 + j) * CG + static_cast<int>(rank)) * (BM * BN / 4) + c * 8 * BM;
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          uint32_t x[4];
-          ld_global_v4_keep(w4 + v * BM, x, ws_pol);
-          r[4 * v] = __float_as_uint(__uint_as_float(r[4 * v]) + __uint_as_float(x[0]));
-          r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + __uint_as_float(x[1]));
-          r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + __uint_as_float(x[2]));
-          r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + __uint_as_float(x[3]));
-        }
+      if (sg.nw > 0) add_part(r, pa);  // the later parts in K order
+      for (int j = 1; j < sg.nw; ++j) {
+        uint32_t h[32];
+        load_part(j, c, h);
+        add_part(r, h);
       }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) pa[e] = pn[e];
       const int ox = T.col + c * EPI_COLS, oy = T.y_row + row_off + quad * 32;
       if (ox >= p.m || oy >= p.y_rows) continue;  // wholly past the output's edge: no buffer, no store
       uint32_t packed[16];
@@ -1017,7 +1011,7 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
     }
     return true;
   };
-  SegIter<SPLIT> it(p, g, G, total_tiles, p.num_segs * p.kb_per_seg);
+  SegIter<SPLIT> it(p, g, G, total_tiles, p.num_segs * p.kb_per_seg, tail);
   Seg sg;
   while (ok_all && it.next(sg)) {
     const Tile T = tile_at<PP::TILE_M>(p, sg.t);
@@ -1197,6 +1191,12 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
   B.tempty0 = sbase + SMEM_BARS + 8u * BAR_TEMPTY;
   B.drain = sbase + SMEM_BARS + 8u * BAR_DRAIN;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_TMEM_SLOT);
+  TailDesc* tail = reinterpret_cast<TailDesc*>(smem + SMEM_TAIL);
+  // GEMM CTAs are groups 0 .. G-1; producer CTAs that join afterwards follow
+  const int bid = static_cast<int>(blockIdx.x), G = p.num_gemm / CG;
+  const int g = bid >= p.num_producers ? (bid - p.num_producers) / CG : G + bid / CG;
+  const int total_tiles = p.num_groups * p.row_tiles * p.col_tiles;
+  const int nkb = p.num_segs * p.kb_per_seg;
   if (threadIdx.x == 0) {
     for (int s = 0; s < MAX_STAGES; ++s) {
       mbar_init(B.full0 + 8u * s, 1);
@@ -1215,24 +1215,23 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
     tmem_alloc_cg<CG>(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish_cg<CG>();
   }
+  if constexpr (SPLIT) {  // the group's schedule (host-built), fetched while the tensor memory is allocated
+    if (warp == 2 && lane < 16 && p.tail_split)
+      reinterpret_cast<int*>(tail)[lane] = __ldg(reinterpret_cast<const int*>(p.tail_tab + g) + lane);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  // GEMM CTAs are groups 0 .. G-1; producer CTAs that join afterwards follow
-  const int bid = static_cast<int>(blockIdx.x), G = p.num_gemm / CG;
-  const int g = bid >= p.num_producers ? (bid - p.num_producers) / CG : G + bid / CG;
-  const int total_tiles = p.num_groups * p.row_tiles * p.col_tiles;
-  const int nkb = p.num_segs * p.kb_per_seg;
   if (warp == 0) {
-    if (lane == 0) tma_role<CG, SPLIT>(p, sbase, B, rank, g, G, total_tiles, nkb);
+    if (lane == 0) tma_role<CG, SPLIT>(p, sbase, B, rank, g, G, total_tiles, nkb, tail);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_role<CG, SPLIT>(p, sbase, tmem, B, g, G, total_tiles, nkb);
+    if (lane == 0 && rank == 0) mma_role<CG, SPLIT>(p, sbase, tmem, B, g, G, total_tiles, nkb, tail);
     __syncwarp();
   } else {
-    epilogue_role<CG, SPLIT>(p, smem, tmem, B, rank, g, G, total_tiles);
+    epilogue_role<CG, SPLIT>(p, smem, tmem, B, rank, g, G, total_tiles, tail);
   }
   tc_fence_before();
   __syncthreads();

@@ -53,7 +53,8 @@ constexpr int BAR_FULL = 0, BAR_EMPTY = MAX_STAGES, BAR_TFULL = 2 * MAX_STAGES, 
               BAR_DRAIN = BAR_TEMPTY + 2, BAR_COPY = BAR_DRAIN + 1;
 constexpr int NUM_BARS = BAR_COPY + COPY_BUFS;
 constexpr int SMEM_TMEM_SLOT = SMEM_BARS + NUM_BARS * 8;
-constexpr int SMEM_USED = SMEM_TMEM_SLOT + 16;
+constexpr int SMEM_TAIL = SMEM_TMEM_SLOT + 16;   // split builds: the CTA group's schedule (64 bytes)
+constexpr int SMEM_USED = SMEM_TAIL + 64;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(COPY_BUFS * COPY_PIECE <= STAGE_AREA, "copy ring must fit the stage area");
 static_assert(Pipe<1>::STAGES * Pipe<1>::STAGE_BYTES <= STAGE_AREA && Pipe<2>::STAGES <= MAX_STAGES, "stages");
@@ -79,6 +80,19 @@ enum Site : uint32_t {
   SITE_PARTIAL = 8     // epilogue waiting for a split tile's partial
 };
 
+// A CTA group's schedule with the AG tail split (see SegIter in the kernel),
+// worked out on the host once per plan and read by each CTA during its
+// set-up.  The tail range is a later part of one tile (K units [wr_lo,
+// wr_hi)), whole tiles [tw0, tw1), then the first part of one more tile (K
+// units [0, fin_hi), whose later parts the groups fin_w0 .. fin_w0+fin_nw-1
+// hold); whole rounds (nfull tiles from whole_base + slot, stride G) come
+// after the tail range (first) or before it.
+struct TailDesc {
+  int first, nfull, whole_base, slot, tail_base;
+  int has_wr, wr_t, wr_lo, wr_hi, tw0, tw1, has_fin, fin_t, fin_hi, fin_w0, fin_nw;
+};
+static_assert(sizeof(TailDesc) == 64, "one 64-byte line per group");
+
 // Per-context device words (one allocation).
 struct DevWords {
   uint32_t counters[TPO_MAX_TP];        // per-slot chunk counters (monotonic)
@@ -98,6 +112,7 @@ struct Params {
   const uint8_t* src[TPO_MAX_TP];  // producer sources X_r
   uint8_t* staging;
   float* ws;              // RS/AR epilogue-reduction modes: a BM x BN fp32 running sum per GEMM CTA
+  const TailDesc* tail_tab;  // AG tail split: one TailDesc per CTA group
   DevWords* words;
   const float* scale_x;
   const float* scale_w;
