@@ -63,7 +63,7 @@ class Guarded:
 
 
 @pytest.mark.parametrize("tp,n,k,m,dtype,cg,gemm1,gemm2", CASES)
-@pytest.mark.parametrize("schedule", [1, 2])
+@pytest.mark.parametrize("schedule", [1, 2, 3])
 def test_split_parity_and_same_bits_in_modes_0_1_2(tp, n, k, m, dtype, cg, gemm1, gemm2, schedule):
     wl = synth.make_ag(tp, n, k, m, seed=90 + tp, dist="normal", sigma=k ** -0.25, dtype=dtype)
     ref = oracle.ag(oracle.gather(wl.x), wl.w[0], wl.scale_inv_x, wl.scale_inv_w)
@@ -71,15 +71,15 @@ def test_split_parity_and_same_bits_in_modes_0_1_2(tp, n, k, m, dtype, cg, gemm1
     out = Guarded(n, m)
     try:
         t.tpo_set_opt(run.ctx, "cta_group", cg)
-        t.tpo_set_opt(run.ctx, "gemm_ctas", gemm1 if schedule == 1 else gemm2)
-        t.tpo_set_opt(run.ctx, "producer_sms", 0 if schedule == 1 else 8)
+        t.tpo_set_opt(run.ctx, "gemm_ctas", gemm1 if schedule != 2 else gemm2)
+        t.tpo_set_opt(run.ctx, "producer_sms", 0 if schedule != 2 else 8)
         t.tpo_set_opt(run.ctx, "tail_split", schedule)
         out.y.fill_(float("nan"))
         run.run(y=out.y)
         split = t.tpo_get_opt(run.ctx, "last_split_tiles")
         late = t.tpo_get_opt(run.ctx, "last_late_groups")
         assert split > 0
-        if schedule == 1:
+        if schedule != 2:
             assert late == 0 and split == leftover(run.ctx, tp, n, m)
         else:
             assert late > 0
@@ -105,15 +105,15 @@ def test_split_parity_and_same_bits_in_modes_0_1_2(tp, n, k, m, dtype, cg, gemm1
         run.close()
 
 
-@pytest.mark.parametrize("schedule", [1, 2])
+@pytest.mark.parametrize("schedule", [1, 2, 3])
 def test_split_every_observer_meets_the_bar(schedule):
     tp, n, k, m = 4, 2048, 512, 768
     wl = synth.make_ag(tp, n, k, m, seed=7, dist="uniform")
     ref = oracle.ag(oracle.gather(wl.x), wl.w[0])
     run = AgRun(wl)
     try:
-        t.tpo_set_opt(run.ctx, "gemm_ctas", 10 if schedule == 1 else 4)
-        t.tpo_set_opt(run.ctx, "producer_sms", 0 if schedule == 1 else 8)
+        t.tpo_set_opt(run.ctx, "gemm_ctas", 10 if schedule != 2 else 4)
+        t.tpo_set_opt(run.ctx, "producer_sms", 0 if schedule != 2 else 8)
         t.tpo_set_opt(run.ctx, "tail_split", schedule)
         for self_rank in range(tp):
             t.tpo_set_opt(run.ctx, "self_rank", self_rank)

@@ -168,7 +168,7 @@ def test_workload_shapes_fit_the_tiling():
 TAIL_SPLIT = 2
 
 
-def plan_split(T, G, L, kbu, kps=2, tp=4, chunk_bytes=1 << 23, cg=2):
+def plan_split(T, G, L, kbu, kps=2, tp=4, chunk_bytes=1 << 23, cg=2, last=False):
     """The host's plan: (tail_first, full, ga, wa, gb, wb) or None (no split)."""
     if L > 0:
         P = L * cg
@@ -186,7 +186,7 @@ def plan_split(T, G, L, kbu, kps=2, tp=4, chunk_bytes=1 << 23, cg=2):
     full, R = divmod(T, G)
     if R == 0:
         return None
-    return (1, full, min(G, TAIL_SPLIT * R), R * kbu, 0, 0)
+    return (0 if last else 1, full, min(G, TAIL_SPLIT * R), R * kbu, 0, 0)
 
 
 def segments(g, G, T, nkb, kps, plan):
@@ -244,9 +244,9 @@ def all_groups(G, L, plan):
 
 
 @pytest.mark.parametrize("T,G,L,nkb,kps", SPLIT_CASES)
-@pytest.mark.parametrize("split", [0, 1])
+@pytest.mark.parametrize("split", [0, 1, 3])
 def test_segments_cover_every_k_block_once(T, G, L, nkb, kps, split):
-    plan = plan_split(T, G, L, nkb // kps, kps) if split else None
+    plan = plan_split(T, G, L if split == 1 else 0, nkb // kps, kps, last=split == 3) if split else None
     seen = {}
     for g in range(all_groups(G, L, plan)):
         for t, lo, hi, kind, _ in segments(g, G, T, nkb, kps, plan):
@@ -266,12 +266,13 @@ def test_no_split_keeps_round_robin(T, G, L, nkb, kps):
 
 
 @pytest.mark.parametrize("T,G,L,nkb,kps", SPLIT_CASES)
-def test_split_parts_and_dependencies(T, G, L, nkb, kps):
+@pytest.mark.parametrize("last", [False, True])
+def test_split_parts_and_dependencies(T, G, L, nkb, kps, last):
     """Each group writes at most one partial, as its first tail segment (after
     which it waits for nothing a lower group holds), and finishes at most one
     split tile, as its last tail segment; a finisher's writer list is exactly
     the higher groups holding the tile's later parts, in K order."""
-    plan = plan_split(T, G, L, nkb // kps, kps)
+    plan = plan_split(T, G, 0 if last else L, nkb // kps, kps, last=last)
     if plan is None:
         return
     parts, finish = {}, {}
