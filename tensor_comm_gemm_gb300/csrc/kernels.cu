@@ -18,9 +18,15 @@
 //    bf16 and TMA-store the tile.  In the pair variant (CG = 2) two CTAs of a
 //    cluster share one 256 x 256 tile through the 2-SM MMA: each loads its own
 //    128 rows of A and half of the B tile, the even CTA issues the MMAs, and
-//    each CTA's tensor memory receives its own 128 rows of the result.  This replaces the counter-gated cuBLAS
-//    atomic GEMM of the same listing.  For GEMM+RS / GEMM+AR the K loop of a
-//    tile walks the ranks' K-slices in a fixed ring order into one accumulator.
+//    each CTA's tensor memory receives its own 128 rows of the result.  This
+//    replaces the counter-gated cuBLAS atomic GEMM of the same listing.  For
+//    GEMM+RS / GEMM+AR the K loop of a tile walks the ranks' K-slices in a
+//    fixed ring order into one accumulator.
+//
+// The kernel is built twice per tile variant: fused_kernel<CG, false> (the
+// default) and fused_kernel<CG, true> with the optional AG tail split (K-split
+// tiles, fp32 partials, producer CTAs joining the GEMM), launched only when a
+// call uses the split, so the default build carries none of its code.
 //
 // Every wait (mbarrier, chunk counter) is bounded by the device global timer.
 // On expiry the waiting thread records the failure in the context's error word
@@ -462,14 +468,17 @@ __device__ __forceinline__ Tile tile_at(const Params& p, int t) {
 // output).  A finisher only ever waits for higher groups' first tail segment,
 // which waits for nothing the finisher holds.
 //
-//  * tail first (no late groups): the R = T mod G leftover tiles are the
-//    first tiles (the observer's own chunk, readable at once), shared by
+//  * tail first (schedule 1): the R = T mod G leftover tiles are the first
+//    tiles (the observer's own chunk, readable at once), shared by
 //    ga = min(G, TAIL_SPLIT R) groups; the whole rounds follow from tile R,
 //    the groups without tail work taking each round's lowest tiles.
-//  * tail last (late groups): the GEMM groups first take p.split_full whole
-//    rounds; the remaining tiles are shared by the GEMM groups (band a, a
-//    short range each) and the late groups (band b, the rest), sized on the
-//    host so that both end together given when the copy should finish.
+//  * tail last: the GEMM groups first take p.split_full whole rounds; the
+//    remaining tiles are shared either by ga = min(G, TAIL_SPLIT R) GEMM
+//    groups (schedule 3), or by the GEMM groups (band a, a short range each)
+//    and the late groups (band b, the rest; schedule 2), sized on the host
+//    so that both end together given when the copy should finish.
+// The host works each group's ranges out once per plan (a TailDesc per
+// group in a device table); the kernel only steps through them.
 enum SegKind : int { SEG_WHOLE = 0, SEG_FINISH = 1, SEG_WRITE = 2 };
 struct Seg {
   int t, kb_lo, kb_hi, kind;
