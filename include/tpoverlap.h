@@ -63,13 +63,13 @@ typedef enum { TPO_BF16 = 0, TPO_FP8_E4M3 = 1 } tpo_dtype;
 typedef enum {
   TPO_OK = 0,
   TPO_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or option */
-  TPO_ERR_UNSUPPORTED = 2, /* valid request outside the tiling this build supports */
+  TPO_ERR_UNSUPPORTED = 2, /* valid request outside what the library supports */
   TPO_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
   TPO_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out */
   TPO_ERR_OOM = 5          /* device allocation failed in tpo_ctx_create */
 } tpo_status;
 
-/* Operation limits of this build. */
+/* Operation limits of the library. */
 #define TPO_MAX_TP 16
 #define TPO_MAX_ROW_CHUNKS 64
 #define TPO_BLOCK_M 128 /* rows of one output tile */

@@ -587,7 +587,7 @@ tpo_ctx* tpo_ctx_create(int tp, int64_t n, int64_t k, int64_t m, int dtype) {
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, c->device);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, c->device);
   if (major != 10 || minor != 3) {
-    fail(TPO_ERR_UNSUPPORTED, "this build targets sm_103a; device is sm_%d%d", major, minor);
+    fail(TPO_ERR_UNSUPPORTED, "libtpoverlap is compiled for sm_103a only; device is sm_%d%d", major, minor);
     destroy_all(c);
     return nullptr;
   }

@@ -74,7 +74,7 @@ tpo_status setup_device(int dev, DeviceSetup** out) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "device attributes");
-    if (major != 10 || minor != 3) return fail(TPO_ERR_UNSUPPORTED, "this build targets sm_103a (device is sm_%d%d)",
+    if (major != 10 || minor != 3) return fail(TPO_ERR_UNSUPPORTED, "libtpoverlap is compiled for sm_103a only (device is sm_%d%d)",
                                                major, minor);
     e = tpo::configure_kernel();
     if (e == cudaSuccess) e = tpo::max_blocks_per_sm(&per_sm);
