@@ -96,7 +96,7 @@ struct tpo_ctx {
   // options
   int64_t producer_sms = 0, gemm_ctas = 0, mode = 0, seq_copy_ctas = 0, self_rank = 0, wait_timeout_ms = 2000,
           trace = 0, debug_skip_chunk = -1, debug_delay_ns = 0, debug_last_step = -1, cta_group = 0,
-          cooperative = 1, reduce = 0, tail_split = 0, debug_skip_partial = -1;
+          cooperative = 1, reduce = 0, tail_split = 0, debug_skip_partial = -1, stage_kblocks = 1;
   // device memory
   uint8_t* staging = nullptr;
   size_t staging_bytes = 0;
@@ -159,6 +159,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
       {"reduce", &tpo_ctx::reduce, 0, 2},
       {"tail_split", &tpo_ctx::tail_split, 0, 3},
       {"debug_skip_partial", &tpo_ctx::debug_skip_partial, -1, tpo::MAX_GEMM_CTAS - 1},
+      {"stage_kblocks", &tpo_ctx::stage_kblocks, 1, 2},
   };
   for (const E& e : table)
     if (std::strcmp(e.k, key) == 0) {
@@ -175,7 +176,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
 const char* kOptKeys[] = {"producer_sms",     "gemm_ctas",      "mode",           "seq_copy_ctas",
                           "self_rank",        "wait_timeout_ms", "trace",          "debug_skip_chunk",
                           "debug_delay_ns",   "debug_last_step", "cta_group",      "cooperative",
-                          "reduce",           "tail_split",     "debug_skip_partial"};
+                          "reduce",           "tail_split",     "debug_skip_partial", "stage_kblocks"};
 
 void destroy_all(tpo_ctx* c) {
   if (!c) return;
@@ -751,7 +752,8 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   p.kb_per_seg = static_cast<int>(ceil_div(c->k * elem, tpo::BK_BYTES));
   p.num_segs = 1;
   p.gate = 1;
-  p.kps = (cg == 2 && p.kb_per_seg % 2 == 0) ? 2 : 1;  // pairs: two K blocks per stage when they divide
+  // K blocks per pipeline stage: one (six stages) unless two are asked for (pairs, when they divide)
+  p.kps = (cg == 2 && c->stage_kblocks == 2 && p.kb_per_seg % 2 == 0) ? 2 : 1;
   const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
 
   tpo_status st = reset_trace(c, s);
@@ -932,8 +934,9 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   p.scale_w = c->ks_scale_w;
   p.reduce_mode = static_cast<int>(c->reduce);
   p.ws = c->ws;
-  // pairs: two K blocks per stage when every accumulation unit has an even count
-  p.kps = (cg == 2 && (p.reduce_mode ? p.kb_per_seg : p.num_segs * p.kb_per_seg) % 2 == 0) ? 2 : 1;
+  // pairs with stage_kblocks 2: two K blocks per stage when every accumulation unit has an even count
+  p.kps = (cg == 2 && c->stage_kblocks == 2 &&
+           (p.reduce_mode ? p.kb_per_seg : p.num_segs * p.kb_per_seg) % 2 == 0) ? 2 : 1;
   const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
   tpo_status st = reset_trace(c, s);
   if (st != TPO_OK) return st;

@@ -242,7 +242,8 @@ def test_workload_ag_tp4_4096_sampled_parity():
 @pytest.mark.parametrize("tp,n,k,m", [(4, 2048, 512, 768), (3, 768, 192, 768), (2, 1024, 4096, 512)])
 def test_pair_and_single_sm_variants_agree(tp, n, k, m):
     """The 2-SM (CTA pair) MMA and the single-SM MMA compute every output
-    element with the same K order; both meet the oracle bar and agree bitwise."""
+    element with the same K order; so do the pairs' one- and two-block
+    pipeline stages.  All meet the oracle bar and agree bitwise."""
     wl = synth.make_ag(tp, n, k, m, seed=70 + tp, dist="normal", sigma=k ** -0.25)
     ref = ref_ag(wl)
     run = AgRun(wl)
@@ -251,14 +252,16 @@ def test_pair_and_single_sm_variants_agree(tp, n, k, m):
         t.tpo_set_opt(run.ctx, "tail_split", 0)   # whole tiles, so that both variants share the K order
         for cg in (1, 2):
             t.tpo_set_opt(run.ctx, "cta_group", cg)
-            for mode in (0, 1):
-                t.tpo_set_opt(run.ctx, "mode", mode)
-                run.y.fill_(float("nan"))
-                run.run()
-                assert_close(host_f64(run.y), ref)
-                bits[(cg, mode)] = host_bits(run.y)
-        assert np.array_equal(bits[(1, 0)], bits[(1, 1)]) and np.array_equal(bits[(2, 0)], bits[(2, 1)])
-        assert np.array_equal(bits[(1, 0)], bits[(2, 0)])
+            for kb in ((1,) if cg == 1 else (1, 2)):
+                t.tpo_set_opt(run.ctx, "stage_kblocks", kb)
+                for mode in (0, 1):
+                    t.tpo_set_opt(run.ctx, "mode", mode)
+                    run.y.fill_(float("nan"))
+                    run.run()
+                    assert_close(host_f64(run.y), ref)
+                    bits[(cg, kb, mode)] = host_bits(run.y)
+        for key, b in bits.items():
+            assert np.array_equal(b, bits[(1, 1, 0)]), key
     finally:
         run.close()
 

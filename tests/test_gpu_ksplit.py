@@ -159,8 +159,9 @@ def test_ksplit_pair_and_single_sm_variants_agree(op, tp, n, k, m, chunks):
     run = KsplitRun(wl)
     try:
         outs = {}
-        for cg in (1, 2):
+        for cg, kb in ((1, 1), (2, 1), (2, 2)):   # single SM; pairs with one- and two-block stages
             t.tpo_set_opt(run.ctx, "cta_group", cg)
+            t.tpo_set_opt(run.ctx, "stage_kblocks", kb)
             if op == "rs":
                 run.rs()
                 y = torch.cat(run.yb, 0)
@@ -168,8 +169,8 @@ def test_ksplit_pair_and_single_sm_variants_agree(op, tp, n, k, m, chunks):
                 run.ar(chunks)
                 y = run.y
             assert_close(host_f64(y), ref)
-            outs[cg] = host_bits(y)
-        assert np.array_equal(outs[1], outs[2])
+            outs[(cg, kb)] = host_bits(y)
+        assert np.array_equal(outs[(1, 1)], outs[(2, 1)]) and np.array_equal(outs[(1, 1)], outs[(2, 2)])
     finally:
         run.close()
 
@@ -247,12 +248,13 @@ def test_epilogue_reduction_modes(op, tp, n, k, m, chunks, dtype):
     ref = oracle.ksplit(wl.x, wl.w, sx=wl.scale_inv_x, sw=wl.scale_inv_w)
     wire = _wire_bound(wl, op, chunks)
     run = KsplitRun(wl)
-    errs = {}
+    errs, bits = {}, {}
     try:
         for mode in (0, 1, 2):
             t.tpo_set_opt(run.ctx, "reduce", mode)
-            for cg in (1, 2):
+            for cg, kb in ((1, 1), (2, 1), (2, 2)):   # pairs with one- and two-block pipeline stages
                 t.tpo_set_opt(run.ctx, "cta_group", cg)
+                t.tpo_set_opt(run.ctx, "stage_kblocks", kb)
                 try:
                     if op == "rs":
                         for y in run.yb:
@@ -268,6 +270,9 @@ def test_epilogue_reduction_modes(op, tp, n, k, m, chunks, dtype):
                     continue
                 assert np.all(np.isfinite(got))
                 errs[(mode, cg)] = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+                bits[(mode, cg, kb)] = got
+                if kb == 2:   # the stage layout does not change a single bit
+                    assert np.array_equal(got, bits[(mode, 2, 1)])
                 if mode < 2:
                     assert_close(got, ref, dtype)
                 else:
