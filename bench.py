@@ -370,6 +370,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
         "data": "synthetic (seeded splitmix64 normal inputs, sigma = K^-1/4)",
         "config": {"workload": "ag_tp4_4096: " + describe(HEADLINE), "mode": "overlapped (one launch)",
                    "producer_ctas": t.tpo_get_opt(ctx, "last_producer_ctas"), "gemm_ctas": t.tpo_get_opt(ctx, "last_gemm_ctas"), "cta_group": t.tpo_get_opt(ctx, "last_cta_group"),
+                   "stage_kblocks": t.tpo_get_opt(ctx, "last_stage_kblocks"),
                    "cooperative_launch": bool(t.tpo_get_opt(ctx, "cooperative") and t.tpo_get_opt(ctx, "coop_clusters")),
                    "l2": "inputs larger than L2: %d rotating sets of X_r, W, Y (%d MiB), steps back to back" % (
                        ROTATE, ROTATE * 96),

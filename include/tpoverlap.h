@@ -241,8 +241,9 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      (one 128 x 256 block per SM, fp32 in mode 1, bf16 in
  *                      mode 2), so the MMAs never wait for the additions.
  * Read-only keys for tpo_get_opt: "last_producer_ctas", "last_gemm_ctas",
- * "last_cta_group", "last_split_tiles" (shape of the context's latest kernel
- * launch: producer CTAs, GEMM CTAs, 1 or 2 CTAs per MMA, tiles split along K),
+ * "last_cta_group", "last_stage_kblocks", "last_split_tiles" (shape of the
+ * context's latest kernel launch: producer CTAs, GEMM CTAs, 1 or 2 CTAs per
+ * MMA, K blocks per pipeline stage, tiles split along K),
  * "coop_clusters" (0 once the driver refused a cooperative cluster launch),
  * "tp", "n", "k", "m", "dtype" (the sizes the context was created for).
  * Environment variables TPO_<KEY in upper case> override the defaults at

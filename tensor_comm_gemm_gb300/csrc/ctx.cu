@@ -118,6 +118,7 @@ struct tpo_ctx {
   const float* ks_scale_x = nullptr;  // e4m3 RS/AR scale_inv pointers (tpo_set_fp8_scales)
   const float* ks_scale_w = nullptr;
   int64_t last_producers = 0, last_gemm_ctas = 0, last_cta_group = 0;  // shape of the latest kernel launch
+  int64_t last_kps = 0;          // K blocks per pipeline stage of the latest kernel launch
   int64_t last_split_tiles = 0;  // tail tiles of the latest kernel launch (AG tail split)
   int64_t pc_key[4] = {-1, -1, -1, -1};  // producer count of the last AG launch shape (see producer_count)
   int pc_val = 0;
@@ -224,6 +225,7 @@ tpo_status launch(tpo_ctx* c, const Params& p, int grid, bool coop, cudaStream_t
   c->last_producers = p.num_producers;
   c->last_gemm_ctas = p.num_gemm;
   c->last_cta_group = p.cta_group;
+  c->last_kps = p.kps;
   c->last_split_tiles = 0;
   c->last_late_groups = p.late_groups;
   if (p.tail_split && p.num_gemm > 0)
@@ -682,6 +684,7 @@ tpo_status tpo_get_opt(tpo_ctx* c, const char* key, int64_t* value) {
   if (std::strcmp(key, "last_producer_ctas") == 0) return *value = c->last_producers, TPO_OK;
   if (std::strcmp(key, "last_gemm_ctas") == 0) return *value = c->last_gemm_ctas, TPO_OK;
   if (std::strcmp(key, "last_cta_group") == 0) return *value = c->last_cta_group, TPO_OK;
+  if (std::strcmp(key, "last_stage_kblocks") == 0) return *value = c->last_kps, TPO_OK;
   if (std::strcmp(key, "last_split_tiles") == 0) return *value = c->last_split_tiles, TPO_OK;
   if (std::strcmp(key, "last_late_groups") == 0) return *value = c->last_late_groups, TPO_OK;
   if (std::strcmp(key, "coop_clusters") == 0) return *value = c->coop_clusters ? 1 : 0, TPO_OK;

@@ -212,6 +212,10 @@ def test_call_argument_errors():
             t.tpo_set_opt(run.ctx, "self_rank", 2)
         with pytest.raises(t.TpoError):
             t.tpo_set_opt(run.ctx, "no_such_option", 1)
+        for bad in (0, 3):   # one or two K blocks per pipeline stage
+            with pytest.raises(t.TpoError):
+                t.tpo_set_opt(run.ctx, "stage_kblocks", bad)
+        assert t.tpo_get_opt(run.ctx, "stage_kblocks") == 1
         with pytest.raises(t.TpoError) as e:
             t.tpo_gemm_ar(run.ctx, [x.data_ptr() for x in run.xs], [run.w.data_ptr()] * 2, run.y,
                           3)   # n % (3*tp) != 0: unequal ring-order parts
@@ -260,6 +264,8 @@ def test_pair_and_single_sm_variants_agree(tp, n, k, m):
                     run.run()
                     assert_close(host_f64(run.y), ref)
                     bits[(cg, kb, mode)] = host_bits(run.y)
+                    even = (k // 64) % 2 == 0   # 64 bf16 elements per K block
+                    assert t.tpo_get_opt(run.ctx, "last_stage_kblocks") == (2 if kb == 2 and even else 1)
         for key, b in bits.items():
             assert np.array_equal(b, bits[(1, 1, 0)]), key
     finally:

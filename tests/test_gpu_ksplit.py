@@ -170,6 +170,8 @@ def test_ksplit_pair_and_single_sm_variants_agree(op, tp, n, k, m, chunks):
                 y = run.y
             assert_close(host_f64(y), ref)
             outs[(cg, kb)] = host_bits(y)
+            if kb == 2 and tp * (-(-(k // tp) // 64)) % 2 == 0:   # an even K-block count per tile
+                assert t.tpo_get_opt(run.ctx, "last_stage_kblocks") == 2
         assert np.array_equal(outs[(1, 1)], outs[(2, 1)]) and np.array_equal(outs[(1, 1)], outs[(2, 2)])
     finally:
         run.close()
