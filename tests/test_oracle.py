@@ -225,3 +225,139 @@ def test_ksplit_fp8_scales():
     # bf16 inputs ignore the scale arguments
     yb = oracle.ksplit([bf16(x) for x in xs_f], [bf16(w) for w in ws_f], sx=0.5, sw=0.25)
     assert np.array_equal(yb, ref / 0.125)
+
+
+# ---------------------------------------------------------------- bf16 ring (wire) reduction
+
+def _bf16_table():
+    """Every finite bf16 value (sorted) and its 16-bit code."""
+    codes = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        vals = (codes << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+    ok = np.isfinite(vals) & ~((vals == 0) & (codes >= 0x8000))     # one zero (+0)
+    order = np.argsort(vals[ok], kind="stable")
+    return vals[ok][order], codes[ok][order]
+
+
+def _nearest_even_by_search(v, table):
+    """Brute force: the nearest finite bf16 value, on a tie the one with an even
+    code; past the largest finite value by half a spacing or more, infinity."""
+    vals, codes = table
+    i = int(np.searchsorted(vals, v))
+    if i >= len(vals):
+        hi_gap = vals[-1] - vals[-2]
+        return np.inf if v - vals[-1] >= hi_gap / 2 else vals[-1]
+    if vals[i] == v:
+        return v
+    if i == 0:
+        lo_gap = vals[1] - vals[0]
+        return -np.inf if vals[0] - v >= lo_gap / 2 else vals[0]
+    lo, hi = vals[i - 1], vals[i]
+    if v - lo < hi - v:
+        return lo
+    if hi - v < v - lo:
+        return hi
+    return lo if codes[i - 1] % 2 == 0 else hi
+
+
+def test_round_bf16_matches_nearest_even_search():
+    table = _bf16_table()
+    vals = table[0]
+    rng = np.random.default_rng(12)
+    probes = [0.0, 1.0, -1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 2.0 ** -133, 2.0 ** -134,
+              3 * 2.0 ** -135, 2.0 ** -126 * (1 - 2 ** -9), 3.3895313892515355e38, 3.3961775292304e38,
+              3.4e38, -3.4e38]
+    pos = vals[vals > 0]
+    picks = rng.integers(0, len(pos) - 1, 4000)
+    mids = (pos[picks] + pos[picks + 1]) / 2                      # ties, every binade
+    probes += list(mids) + list(-mids)
+    probes += list(np.nextafter(mids, np.inf)) + list(np.nextafter(mids, -np.inf))
+    probes += list(rng.standard_normal(3000) * 10.0 ** rng.integers(-40, 38, 3000))
+    for v in probes:
+        assert oracle.round_bf16(v) == _nearest_even_by_search(v, table), v
+
+
+def _wire_golden():
+    d = {}
+    for ln in golden_lines("wire_bf16_tp3.txt"):
+        key, *v = ln.split()
+        d.setdefault(key, []).append([float(x) for x in v])
+    return d
+
+
+def _wire_inputs(d, rows, enc=None):
+    enc = enc or (lambda a: synth.f32_to_bf16_bits(np.asarray(a, dtype=np.float32)))
+    xs = [enc(np.repeat(np.array(d["x%d" % r]), rows, 0)) for r in range(3)]
+    ws = [enc(np.array(d["w%d" % r])) for r in range(3)]
+    return xs, ws
+
+
+def test_wire_bf16_golden_rs_and_ar():
+    d = _wire_golden()
+    xs, ws = _wire_inputs(d, 3)
+    want = np.array([d["rs%d" % b][0] for b in range(3)])
+    assert np.array_equal(oracle.ksplit_wire_bf16(xs, ws, op="rs"), want)
+    xs6, ws6 = _wire_inputs(d, 6)
+    want = np.array([d["ar%d" % i][0] for i in range(6)])
+    assert np.array_equal(oracle.ksplit_wire_bf16(xs6, ws6, op="ar", n_chunks=2), want)
+    # the golden rows differ from a single rounding of the exact sum
+    exact = oracle.ksplit(xs, ws)
+    single = np.vectorize(oracle.round_bf16)(exact)
+    assert not np.array_equal(single, oracle.ksplit_wire_bf16(xs, ws, op="rs"))
+
+
+@pytest.mark.parametrize("plant", [1, 2, 3])
+def test_wire_bf16_golden_catches_each_planted_mistake(plant, tmp_path):
+    """Oracle copies built with one deliberate mistake (partials not rounded,
+    running sums not rounded, ring starting at the owner) disagree with the
+    hand-worked golden rows."""
+    d = _wire_golden()
+    xs, ws = _wire_inputs(d, 3)
+    want = np.array([d["rs%d" % b][0] for b in range(3)])
+    bad = oracle.planted_variant(plant, str(tmp_path))
+    assert not np.array_equal(bad.ksplit_wire_bf16(xs, ws, op="rs"), want)
+
+
+def test_wire_bf16_golden_with_e4m3_scales():
+    """e4m3 inputs: the partials carry sx * sw before they are rounded; with a
+    power-of-two scale product the golden rows scale exactly."""
+    d = _wire_golden()
+    xs, ws = _wire_inputs(d, 3, enc=lambda a: synth.f32_to_e4m3_bits(np.asarray(a, dtype=np.float32)))
+    want = np.array([d["rs%d" % b][0] for b in range(3)]) * 0.125
+    assert np.array_equal(oracle.ksplit_wire_bf16(xs, ws, op="rs", sx=0.5, sw=0.25), want)
+
+
+@pytest.mark.parametrize("op,tp,n,kr,m,chunks", [("rs", 2, 4, 3, 5, 1), ("rs", 4, 8, 2, 3, 1),
+                                                 ("ar", 3, 12, 4, 6, 2), ("ar", 2, 8, 5, 4, 4)])
+def test_wire_bf16_exact_when_nothing_rounds(op, tp, n, kr, m, chunks):
+    """Small integers keep every partial and every running sum below 256 in
+    magnitude, all exact in bf16: the ring sum is then the exact sum."""
+    rng = np.random.default_rng(n * 7 + kr)
+    xs_i = [rng.integers(-3, 4, size=(n, kr)) for _ in range(tp)]
+    ws_i = [rng.integers(-3, 4, size=(m, kr)) for _ in range(tp)]
+    ref = sum(x.astype(np.float64) @ w.astype(np.float64).T for x, w in zip(xs_i, ws_i))
+    got = oracle.ksplit_wire_bf16([bf16(x) for x in xs_i], [bf16(w) for w in ws_i], op=op, n_chunks=chunks)
+    assert np.array_equal(got, ref)
+
+
+def test_wire_bf16_single_rank_is_the_rounded_product():
+    """tp = 1: no hop, so the result is the product rounded to bf16 once."""
+    rng = np.random.default_rng(4)
+    x = synth.f32_to_bf16_bits(rng.standard_normal((16, 24)).astype(np.float32))
+    w = synth.f32_to_bf16_bits(rng.standard_normal((8, 24)).astype(np.float32))
+    exact = oracle.ksplit([x], [w])
+    got = oracle.ksplit_wire_bf16([x], [w], op="rs")
+    table = _bf16_table()
+    assert np.array_equal(got, np.vectorize(lambda v: _nearest_even_by_search(v, table))(exact))
+
+
+def test_wire_bf16_tiles_match_full():
+    rng = np.random.default_rng(8)
+    xs = [synth.f32_to_bf16_bits(rng.standard_normal((32, 8)).astype(np.float32)) for _ in range(4)]
+    ws = [synth.f32_to_bf16_bits(rng.standard_normal((48, 8)).astype(np.float32)) for _ in range(4)]
+    for op, ch in (("rs", 1), ("ar", 2)):
+        full = oracle.ksplit_wire_bf16(xs, ws, op=op, n_chunks=ch)
+        tiles = synth.sample_tiles(32, 48, 16, 4, seed=3)
+        got = oracle.ksplit_wire_bf16(xs, ws, op=op, n_chunks=ch, tiles=tiles)
+        for t, (r0, c0) in enumerate(tiles):
+            assert np.array_equal(got[t], full[r0:r0 + 16, c0:c0 + 16])
