@@ -105,3 +105,99 @@ class KsplitRun:
 
     def close(self):
         t.tpo_ctx_destroy(self.ctx)
+
+
+# ---------------------------------------------------------------- bf16 ring (wire) reduction
+
+def decode(a: np.ndarray) -> np.ndarray:
+    """Values of bf16 bit patterns (uint16) or e4m3 codes (uint8) as float64."""
+    if a.dtype == np.uint16:
+        return synth.bf16_bits_to_f32(a).astype(np.float64)
+    return synth.e4m3_bits_to_f32(a).astype(np.float64)
+
+
+def row_owners(op: str, n: int, tp: int, chunks: int) -> np.ndarray:
+    """Rank each output row's ring sum ends at: its row block (reduce-scatter)
+    or its ring-order part of a row chunk (all-reduce)."""
+    i = np.arange(n)
+    if op == "rs":
+        return i // (n // tp)
+    rows_chunk = n // chunks
+    return (i % rows_chunk) // (rows_chunk // tp)
+
+
+def near_bf16_boundary(p: np.ndarray, eps: np.ndarray) -> np.ndarray:
+    """True where a value within eps of p could round to a different bf16
+    value than p: a rounding midpoint or a power of two (where the spacing
+    changes) lies within eps."""
+    a = np.abs(p)
+    tiny = 2.0 ** -140
+    e = np.floor(np.log2(np.maximum(a, tiny)))
+    h = 2.0 ** np.maximum(e - 7, -133)            # bf16 spacing in a's binade
+    frac = a / h - np.floor(a / h)
+    near_mid = np.abs(frac - 0.5) * h <= eps
+    near_edge = np.floor(np.log2(np.maximum(a - eps, tiny))) != np.floor(np.log2(np.maximum(a + eps, tiny)))
+    return (near_mid | near_edge) & (eps > 0)
+
+
+def wire_expectation(wl, op: str, chunks: int):
+    """What the bf16-ring mode (option reduce=2) must produce, from the oracle.
+
+    Returns (ref, risky, bound): the oracle's ring sum; per element, whether
+    any rank's exact partial P_r lies within eps_r of a bf16 rounding
+    boundary; and a bound on |result - ref|.  The kernel's partials are fp32
+    tensor-core sums, |P~_r - P_r| <= eps_r = (kr + 2) 2^-22 scale
+    sum_q |x_q w_q| (four times the first-order bound of a recursive fp32 sum
+    of kr products, plus the fp32 scale multiplies).  Where no partial is at
+    risk, every rounded partial equals the oracle's and the same fp32 hops on
+    the same values give the same bits.  Elsewhere each rounding of a partial
+    or a running sum can land one bf16 spacing away, and later hops carry the
+    difference: |result - ref| <= sum_r (u(P_r) + u(S_r)), S_r the exact
+    running sums in the row's ring order and u(v) = 2^-6 |v| + 2^-133 (one
+    spacing at |v| and in the binade above)."""
+    import oracle
+
+    tp, n = wl.tp, wl.n
+    sx = wl.scale_inv_x if wl.dtype == "e4m3" else 1.0
+    sw = wl.scale_inv_w if wl.dtype == "e4m3" else 1.0
+    scale = sx * sw
+    ref = oracle.ksplit_wire_bf16(wl.x, wl.w, op=op, n_chunks=chunks, sx=sx, sw=sw)
+    parts = [oracle.ksplit([wl.x[r]], [wl.w[r]], sx=sx, sw=sw) for r in range(tp)]
+    kr = wl.x[0].shape[1]
+    eps = [(kr + 2) * 2.0 ** -22 * scale * (np.abs(decode(wl.x[r])) @ np.abs(decode(wl.w[r])).T)
+           for r in range(tp)]
+    owners = row_owners(op, n, tp, chunks)
+    risky = np.zeros(ref.shape, dtype=bool)
+    bound = np.zeros(ref.shape)
+    for b in range(tp):
+        rows = owners == b
+        run = np.zeros((int(rows.sum()), ref.shape[1]))
+        for j in range(tp):
+            r = (b + 1 + j) % tp
+            p = parts[r][rows]
+            run = run + p
+            risky[rows] |= near_bf16_boundary(p, eps[r][rows])
+            bound[rows] += 2.0 ** -6 * (np.abs(p) + np.abs(run)) + 2 * 2.0 ** -133
+    return ref, risky, bound
+
+
+def check_wire(got, wire_ref, risky, bound, dtype):
+    """bf16-ring mode against the oracle's ring sum: bit-equal wherever no
+    rank's partial is within its fp32 error of a bf16 rounding boundary (bf16
+    inputs), within the rounding bound everywhere, and bit-equal on at least
+    WIRE_EXACT_FRAC of all elements (a wrong ring order or a dropped rounding
+    changes far more)."""
+    assert np.all(np.isfinite(got)), "non-finite outputs"
+    diff = np.abs(got - wire_ref)
+    if dtype == "bf16":
+        safe = ~risky
+        assert np.array_equal(got[safe], wire_ref[safe]), "%d of %d elements with no partial near a rounding " \
+            "boundary differ" % ((got[safe] != wire_ref[safe]).sum(), safe.sum())
+    assert np.all(diff <= bound), "worst excess %.3e" % (diff - bound).max()
+    if got.size >= 1000:   # a share is only meaningful over many elements
+        frac = float(np.mean(got == wire_ref))
+        assert frac >= WIRE_EXACT_FRAC[dtype], "only %.4f of the elements equal the oracle's ring sum" % frac
+
+
+# Share of elements that must match the oracle's bf16 ring sum bit for bit.
+WIRE_EXACT_FRAC = {"bf16": 0.9, "e4m3": 0.9}
