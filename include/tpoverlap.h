@@ -311,14 +311,19 @@ const char* tpo_version(void);
  * callers cannot hold a context.
  *
  * Computes what tpo_ag_gemm computes for observer rank 0 in one overlapped
- * launch (8 producer CTAs, single-SM 128 x 256 tiles, 2 s wait bound); the
- * result is bit-identical to tpo_ag_gemm's in every mode and MMA variant.  Arguments as tpo_ctx_create (tp, n, k, m,
+ * launch (8 producer CTAs, single-SM 128 x 256 tiles, 2 s wait bound).  The
+ * result is bit-identical to tpo_ag_gemm's whenever that call computes whole
+ * tiles (option tail_split 0, the default), in any mode and with either MMA
+ * variant; the tail-split schedules (tail_split 1 to 3) add K-split partials
+ * in an order that depends on their launch shape and agree with it only
+ * within the parity tolerance.  Arguments as tpo_ctx_create (tp, n, k, m,
  * dtype) plus tpo_ag_gemm (x, w, y, scale_inv pointers, stream).
  *
  * Scratch (the gathered staging buffer, the chunk counters and the error word)
  * lives in a static device array of the library: TPO_NOALLOC_MAX_STAGING_BYTES
- * plus a few hundred bytes, held by every GPU that loads the library until the
- * process exits.  n*k*element size above that limit is rejected with
+ * plus TPO_NOALLOC_WORDS_BYTES (the kernel's word block rounded up to 256
+ * bytes), held by every GPU that loads the library until the process exits.
+ * n*k*element size above TPO_NOALLOC_MAX_STAGING_BYTES is rejected with
  * TPO_ERR_INVALID_ARG and a message naming the limit.
  * The first call on a device sets that device up (looks up the array's device
  * address, configures the kernel); make it before any stream capture.
@@ -326,8 +331,13 @@ const char* tpo_version(void);
  * `stream` first; calls whose GPU work could overlap (other streams, other host
  * threads) race on the array.  The call blocks until its work on `stream` has
  * finished, then returns TPO_OK or TPO_ERR_TIMEOUT if a device wait ran out.
+ * If it returns TPO_ERR_CUDA after its launch (the error word could not be
+ * read back), it first tries to wait for `stream`; should that fail as well,
+ * the kernel may still be running and the array's contents stay undefined
+ * until the device is reset.
  */
 #define TPO_NOALLOC_MAX_STAGING_BYTES (32ull << 20) /* 32 MiB */
+#define TPO_NOALLOC_WORDS_BYTES 5632ull             /* counters, error word, trace: 5.5 KiB */
 tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t m, int dtype, const void* const* x,
                                const void* w, void* y, const float* d_scale_inv_x,
                                const float* d_scale_inv_w, void* stream);

@@ -31,6 +31,7 @@ namespace {
 // Staging buffer of up to TPO_NOALLOC_MAX_STAGING_BYTES, followed by the
 // counters and error word of the kernel.
 constexpr size_t kWordsBytes = (sizeof(tpo::DevWords) + 255) / 256 * 256;
+static_assert(kWordsBytes == TPO_NOALLOC_WORDS_BYTES, "the header states the size of the word block");
 static __device__ __align__(256) uint8_t g_noalloc_scratch[TPO_NOALLOC_MAX_STAGING_BYTES + kWordsBytes];
 
 constexpr int kMaxDevices = 64;
@@ -212,10 +213,16 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
 
   // Wait for the call and read its error word (16 bytes into host memory).
+  // On a failure here the kernel may still be running: wait for the stream
+  // before the lock is released, so that the next call's clearing of the
+  // counters cannot overtake it.
   uint32_t err[4] = {0, 0, 0, 0};
   e = cudaMemcpyAsync(err, words->err, sizeof(err), cudaMemcpyDeviceToHost, cs);
   if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
-  if (e != cudaSuccess) return cuda_fail(e, "waiting for the call");
+  if (e != cudaSuccess) {
+    cudaStreamSynchronize(cs);
+    return cuda_fail(e, "waiting for the call");
+  }
   if (err[0] != tpo::DEV_OK)
     return fail(TPO_ERR_TIMEOUT, "device wait timed out (site %u, block %u, extra %u)", err[1], err[2], err[3]);
   return TPO_OK;
