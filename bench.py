@@ -3,10 +3,14 @@
 One step = one overlapped AG+GEMM call of the 4096^3 workload (tp = 4 simulated
 ranks, X_r [1024, 4096], W [4096, 4096], bf16 in, Y [4096, 4096] bf16 out):
 ring-order chunk producer, per-chunk release counters, counter-gated tcgen05
-GEMM, rank-order epilogue, in one launch.  The line also reports the same
-call in sequential mode (copy, then GEMM), the GEMM alone, the producer alone,
-and the other workloads (row-parallel GEMM+AR, GEMM+RS, FP8 AG+GEMM) measured
-the same way.
+GEMM, rank-order epilogue, in one launch.  The block of K steps is repeated
+back to back until the timed region lasts --timed-seconds (clock record with
+>= 10 samples; the rate the power cap sustains), and the roofline fraction is
+taken against the measured sustained bf16 peak (the burst fraction beside it).
+The line also reports the same call in sequential mode (copy, then GEMM), the
+GEMM alone, the producer alone, the host link's copy bound beside the
+end-to-end rate, and the other workloads (row-parallel GEMM+AR, GEMM+RS, FP8
+AG+GEMM, the allocation-free entry point) each with its own clock record.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tpo|reference]
 
@@ -77,15 +81,19 @@ def load_peaks():
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    """nvidia-smi sampling of SM clock, power and throttle reasons for the whole
+    benchmark (one sampler, 50 ms period); each measured region keeps its host
+    wall-clock window and gets its own record from the samples inside it."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.rows = None
         self.path = os.path.join("/tmp", "tpo_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
 
     def start(self):
@@ -96,12 +104,20 @@ class Clocks:
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        if self.proc is not None:
+            import atexit
+            atexit.register(self._kill)   # never leave the sampler running past this process
+        time.sleep(0.5)                # let the sampler come up before the first region
 
-    def stop(self, t_begin=None, t_end=None):
-        """Median SM clock and the throttle reasons seen by samples taken between
-        t_begin and t_end (host wall-clock seconds)."""
+    def _kill(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.kill()
+
+    def stop(self):
+        """Ends sampling and reads every sample (timestamp, clock, max clock,
+        power, active throttle reasons)."""
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -109,8 +125,7 @@ class Clocks:
             self.proc.kill()
         self.f.close()
         import datetime
-        sm, smax, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        self.rows = []
         with open(self.path) as f:
             for ln in f:
                 parts = [p.strip() for p in ln.split(",")]
@@ -121,21 +136,28 @@ class Clocks:
                     clk, cmax = float(parts[1]), float(parts[2])
                 except ValueError:
                     continue
-                if t_begin is not None and not (t_begin - 0.05 <= ts <= t_end + 0.05):
-                    continue
-                sm.append(clk)
-                smax.append(cmax)
                 try:
-                    power.append(float(parts[3]))
+                    pw = float(parts[3])
                 except ValueError:
-                    pass
-                for nm, v in zip(names, parts[4:8]):
-                    if v.lower().startswith("active"):
-                        reasons.add(nm)
+                    pw = None
+                act = [nm for nm, v in zip(self.NAMES, parts[4:8]) if v.lower().startswith("active")]
+                self.rows.append((ts, clk, cmax, pw, act))
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None, "power_limits_w": self.power_limits()}
+
+    def window(self, t_begin, t_end, limits=False):
+        """Median SM clock, maximum clock, throttle reasons and sample count of
+        the samples taken between t_begin and t_end (host wall-clock seconds)."""
+        if self.rows is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sel = [r for r in self.rows if t_begin - 0.05 <= r[0] <= t_end + 0.05]
+        sm = [r[1] for r in sel]
+        power = [r[3] for r in sel if r[3] is not None]
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(r[2] for r in sel) if sel else None,
+               "reasons": sorted({a for r in sel for a in r[4]}), "samples": len(sel),
+               "power_w_max": max(power) if power else None, "window_s": round(t_end - t_begin, 3)}
+        if limits:
+            out["power_limits_w"] = self.power_limits()
+        return out
 
     def power_limits(self):
         """The board's enforced and maximum power limits (read only)."""
@@ -178,6 +200,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
     dev = torch.device("cuda", local_rank)
     peaks, peak_kind = load_peaks()
     stream = torch.cuda.current_stream()
+    clocks = Clocks(local_rank)          # one sampler for the whole run; regions keep their windows
+    clocks.start()
 
     def to_dev(a):
         if a.dtype == np.uint16:
@@ -198,6 +222,23 @@ def gpu_arm(args, rank, world, local_rank, dist):
             b.record(stream)
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in evs]
+
+    def time_row(fn, steps, warmup, seconds):
+        """A measured row: warm-up, then back-to-back steps for at least `seconds`
+        (and at least `steps` of them) in one timed region; returns (mean ms per
+        step, the region's wall-clock window for its clock record, step count)."""
+        probe = time_steps(fn, 2, warmup)
+        count = max(steps, int(np.ceil(seconds * 1e3 / max(min(probe), 1e-3))))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        e0.record(stream)
+        for i in range(count):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        return e0.elapsed_time(e1) / count, (t0, t1), count
 
     def mean(v):
         return sum(v) / len(v)
@@ -237,6 +278,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
         return v
 
     detail_steps = min(200, max(5, args.steps // 2))
+    detail_t0 = time.time()
     seq = mode_times(1, detail_steps, 3)
     prod_only = mode_times(3, detail_steps, 3)
     split = mode_times(4, detail_steps, 3)
@@ -246,26 +288,30 @@ def gpu_arm(args, rank, world, local_rank, dist):
     for _ in range(4):
         ov_blocks += mode_times(0, detail_steps // 2 or 1, 2)
         gemm_only += mode_times(2, detail_steps // 2 or 1, 2)
+    detail_t1 = time.time()
     t.tpo_set_opt(ctx, "mode", 0)
 
-    # ---- the timed region: K overlapped steps, barrier + synchronize on both sides
+    # ---- the timed region: the block of K overlapped steps, repeated back to back
+    # R times so that the region lasts at least --timed-seconds (the clock sampler's
+    # 50 ms period then gives >= 10 samples, and the rate is the sustained one the
+    # power cap allows), bracketed by a barrier + synchronize on both sides; the
+    # per-step time is the mean over all R x K steps.
     for i in range(args.warmup):
         call(i)
     check(ctx)
-    clocks = Clocks(local_rank)
+    est_ms = min(mean(ov_blocks), mean(gemm_only))
+    repeats = max(1, int(np.ceil(args.timed_seconds * 1e3 / (args.steps * est_ms))))
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)                    # let the sampler come up before the region starts
-    torch.cuda.synchronize()
     torch.cuda.nvtx.range_push("tpo_timed")
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(repeats)]
     wall0 = time.time()
     t0 = time.perf_counter()
-    for i, (a, b) in enumerate(evs):
+    for r, (a, b) in enumerate(evs):
         a.record(stream)
-        call(i)
+        for i in range(args.steps):
+            call(r * args.steps + i)
         b.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
@@ -273,11 +319,12 @@ def gpu_arm(args, rank, world, local_rank, dist):
     torch.cuda.nvtx.range_pop()
     if dist is not None:
         dist.barrier()
-    clk = clocks.stop(wall0, wall1)
     check(ctx)
-    step_ms = [a.elapsed_time(b) for a, b in evs]
-    ms = slowest_rank_ms(mean(step_ms), dist, dev)
+    block_ms = [a.elapsed_time(b) for a, b in evs]
+    step_ms = [bm / args.steps for bm in block_ms]
+    ms = slowest_rank_ms(sum(block_ms) / (repeats * args.steps), dist, dev)
     value = whole_job_tflops(flops, world, ms)
+    windows = {"headline": (wall0, wall1), "detail": (detail_t0, detail_t1)}
 
     # ---- the SM clock inside the kernel (GEMM CTAs' cycles per global-timer ns of the
     # kernel span, median of several traced calls); nvidia-smi's clocks.sm reading does
@@ -293,7 +340,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
         span_ns = max(1, tr[t.TPO_TRACE_END] - tr[t.TPO_TRACE_START])
         mhz.append(tr[t.TPO_TRACE_CYC_GEMM] / max(1, gemm_ctas) / span_ns * 1e3)
     t.tpo_set_opt(ctx, "trace", 0)
-    clk["sm_mhz_in_kernel"] = round(statistics.median(mhz), 0)
+    sm_mhz_in_kernel = round(statistics.median(mhz), 0)
 
     # ---- end to end through the C ABI with host buffers.  Every step uploads its
     # activations X_r from pinned host memory and reads its result Y back; W is the
@@ -345,11 +392,14 @@ def gpu_arm(args, rank, world, local_rank, dist):
     assert torch.equal(hy[(detail_steps - 1) & 1], y_sets[0].cpu()), "end-to-end result differs from the device run"
     h2d = sum(x.nbytes for x in wl.x)
     d2h = wl.n * wl.m * 2
+    link = host_link(torch, dev, h2d, d2h)
+    link["e2e_frac_of_copy_bound"] = round(link["copy_bound_ms"] / e2e_ms, 4)
 
     # ---- roofline of the dominant kernel (the fused launch) from the events above
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    achieved = flops / (mean(step_ms) * 1e-3) / 1e12
+    achieved = flops / (sum(block_ms) / (repeats * args.steps) * 1e-3) / 1e12
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
@@ -380,18 +430,23 @@ def gpu_arm(args, rank, world, local_rank, dist):
                    "l2": "inputs larger than L2: %d rotating sets of X_r, W, Y (%d MiB), steps back to back" % (
                        ROTATE, ROTATE * 96),
                    "parallelism": "replicas only (simulated ranks in one GPU's memory)"},
-        "gpu_launches": args.steps,
+        "gpu_launches": repeats * args.steps,
+        "timing": {"repeats": repeats, "steps_timed": repeats * args.steps,
+                   "block_ms_min": round(min(block_ms), 5), "block_ms_max": round(max(block_ms), 5),
+                   "note": "the K-step block run %d times back to back (>= %.1f s, sustained power state); "
+                           "ms_per_step is the mean over all of them" % (repeats, args.timed_seconds)},
         "wall_s_timed_region": round(wall, 4),
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
                 "note": "per step: X_r uploaded from pinned host memory, Y read back; W resident (layer "
-                        "weight); steps double-buffered on copy streams"},
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_kind if peak_kind == "measured"
-                     else "fallback 1.9 PFLOP/s",
-                     "nominal": nominal_peak(achieved, sms, clk.get("sm_max_mhz"), clk.get("sm_mhz_in_kernel"))},
-        "clocks": clk,
+                        "weight); steps double-buffered on copy streams",
+                "link": link},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak_sus, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_sus, 4), "traffic": traffic,
+                     "peak_source": ("%s bf16 sustained (MEASURED_PEAKS.json): the kernel is timed inside a "
+                                     "%.1f s run of back-to-back steps" % (peak_kind, wall)) if peak_kind == "measured"
+                     else "fallback 1.7 PFLOP/s sustained",
+                     "peak_burst": peak, "frac_of_burst": round(achieved / peak, 4)},
         "detail": {
             "sequential_ms": round(seq_ms, 5),
             "sequential_tflops": round(flops / (seq_ms * 1e-3) / 1e12, 2),
@@ -412,12 +467,66 @@ def gpu_arm(args, rank, world, local_rank, dist):
     # ---- the other workloads, one line each inside "also"
     cpu_others = {} if (rank == 0 and not args.no_cpu) else None
     if not args.headline_only:
-        result["also"] = other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch, cpu_others)
+        result["also"] = other_workloads(args, dev, to_dev, time_steps, time_row, mean, peak, peak_sus, check, t,
+                                         torch, cpu_others)
+
+    # ---- clock records: the headline's timed region, the detail modes, and every
+    # "also" row from its own window
+    clocks.stop()
+    clk = clocks.window(*windows["headline"], limits=True)
+    clk["sm_mhz_in_kernel"] = sm_mhz_in_kernel
+    result["clocks"] = clk
+    result["roofline"]["nominal"] = nominal_peak(achieved, sms, clk.get("sm_max_mhz"), sm_mhz_in_kernel)
+    result["detail"]["clocks"] = clocks.window(*windows["detail"])
+    for rec in (result.get("also") or {}).values():
+        if isinstance(rec, dict) and "_window" in rec:
+            rec["clocks"] = clocks.window(*rec.pop("_window"))
 
     # ---- the oracle on the host cores, bounded sample
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, cpu_others)
     return result
+
+
+def host_link(torch, dev, h2d_bytes, d2h_bytes, reps=10):
+    """The host link's own rate, for the end-to-end step's copy bound: one plain
+    pinned-memory cudaMemcpyAsync of the step's upload size host to device, one
+    of its download size device to host, each alone and both at once on two
+    streams (mean of `reps` copies)."""
+    hu = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+    du = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
+    hd = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+    dd = torch.empty(d2h_bytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    def up():
+        with torch.cuda.stream(s1):
+            du.copy_(hu, non_blocking=True)
+
+    def down():
+        with torch.cuda.stream(s2):
+            hd.copy_(dd, non_blocking=True)
+
+    def both():
+        up()
+        down()
+    t_up, t_down, t_both = timed(up), timed(down), timed(both)
+    bound_s = max(h2d_bytes / (h2d_bytes / t_up), d2h_bytes / (d2h_bytes / t_down), t_both)
+    return {"h2d_gbs": round(h2d_bytes / t_up / 1e9, 1), "d2h_gbs": round(d2h_bytes / t_down / 1e9, 1),
+            "both_directions_gbs": round((h2d_bytes + d2h_bytes) / t_both / 1e9, 1),
+            "copy_bound_ms": round(bound_s * 1e3, 5),
+            "note": "one pinned cudaMemcpyAsync of the step's upload and one of its download, alone and "
+                    "together; copy_bound_ms = the slower of the two alone or both at once"}
 
 
 def nominal_peak(achieved, sms, max_mhz, kernel_mhz):
@@ -478,7 +587,12 @@ def library_gemm_4096(torch, dev, sets=3, calls=60):
         return None
 
 
-def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch, cpu_others=None):
+def other_workloads(args, dev, to_dev, time_steps, time_row, mean, peak, peak_sus, check, t, torch,
+                    cpu_others=None):
+    """One record per other workload.  Each tensor-bound row times at least
+    args.row_seconds of back-to-back steps and keeps that window for its own
+    clock record; its rate is given against the sustained and the burst
+    measured peak (FP8 rows: twice each, the nominal dense ratio)."""
     out = {}
     steps = min(40, max(5, args.steps // 2))
     # the small AG workload: latency-bound (2 output tiles), reported in microseconds per call
@@ -493,18 +607,30 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch, 
         st = lib.tpo_ag_gemm(ctx, xa, w.data_ptr(), y.data_ptr(), None, None, sh)
         if st:
             raise t.TpoError(st, t.tpo_last_error())
+    t0 = time.time()
     ms = mean(time_steps(raw, 200, 10))
     ms_py = mean(time_steps(lambda i=0: t.tpo_ag_gemm(ctx, xs, w, y), 200, 10))
     check(ctx)
     # us_per_call: the C ABI call; us_per_call_python adds the binding's argument checks
     out[wl.name] = {"workload": describe(0), "us_per_call": round(ms * 1e3, 2),
                     "us_per_call_python": round(ms_py * 1e3, 2),
-                    "tflops": round(synth.flops(0) / (ms * 1e-3) / 1e12, 3)}
+                    "tflops": round(synth.flops(0) / (ms * 1e-3) / 1e12, 3), "_window": (t0, time.time())}
+    if cpu_others is not None:   # small enough for the oracle to run in full
+        cpu_others[wl.name] = oracle_full(wl)
     t.tpo_ctx_destroy(ctx)
     out["library_bf16_gemm_4096"] = library_gemm_4096(torch, dev)
     fp8_lib = cublas_fp8_tflops(torch, dev)
     out["fp8_library_gemm_8192"] = {"tflops": fp8_lib, "note": "torch._scaled_mm e4m3 8192^3 burst on this "
                                     "box; the FP8 rows' frac_of_peak uses 2 x the measured bf16 peak"}
+    out["ag_tp4_4096_noalloc"] = noalloc_row(t, torch, dev, to_dev, peak)
+
+    def rates(flops, ms, pk, pk_sus):
+        """Rate against the sustained measured peak (the row is timed over a long
+        back-to-back run) and against the burst peak."""
+        tf = flops / (ms * 1e-3) / 1e12
+        return {"tflops": round(tf, 2), "frac_of_peak": round(tf / pk_sus, 4), "peak_tflops": pk_sus,
+                "peak_kind": "sustained", "frac_of_burst_peak": round(tf / pk, 4), "burst_peak_tflops": pk}
+
     for idx in (2, 3, 4):
         op, dt, tp, n, k, m, ch = synth.WORKLOAD_SHAPES[idx]
         wl = synth.workload(idx)
@@ -518,7 +644,7 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch, 
             sw = torch.tensor([wl.scale_inv_w], dtype=torch.float32, device=dev)
             ctx = t.tpo_ctx_create(tp, n, k, m, t.TPO_FP8_E4M3)
             fn = lambda i=0: t.tpo_ag_gemm(ctx, xs, w, y, sx, sw)  # noqa: E731
-            pk = peak * FP8_OVER_BF16
+            pk, pk_sus = peak * FP8_OVER_BF16, peak_sus * FP8_OVER_BF16
         else:
             xs = [to_dev(x) for x in wl.x]
             ws = [to_dev(x) for x in wl.w]
@@ -529,11 +655,12 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch, 
             else:
                 y = torch.empty((n, m), dtype=torch.bfloat16, device=dev)
                 fn = lambda i=0: t.tpo_gemm_ar(ctx, xs, ws, y, ch)  # noqa: E731
-            pk = peak
-        ms = mean(time_steps(fn, steps, 3))
+            pk, pk_sus = peak, peak_sus
+        ms, window, count = time_row(fn, steps, 3, args.row_seconds)
         check(ctx)
-        rec = {"workload": describe(idx), "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
-               "frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / pk, 4), "peak_tflops": pk}
+        rec = {"workload": describe(idx), "ms": round(ms, 4), "steps_timed": count}
+        rec.update(rates(flops, ms, pk, pk_sus))
+        rec["_window"] = window
         if dt == "e4m3" and fp8_lib:
             rec["frac_of_library_fp8"] = round(flops / (ms * 1e-3) / 1e12 / fp8_lib, 4)
         if cpu_others is not None:  # the CPU-baseline leg: the oracle on a sample of this workload
@@ -578,17 +705,42 @@ def other_workloads(args, dev, to_dev, time_steps, mean, peak, check, t, torch, 
     sw = torch.tensor([wl.scale_inv_w], dtype=torch.float32, device=dev)
     ctx = t.tpo_ctx_create(wl.tp, wl.n, wl.k, wl.m, t.TPO_FP8_E4M3)
     t.tpo_set_fp8_scales(ctx, sx, sw)
-    ms = mean(time_steps(lambda i=0: t.tpo_gemm_rs(ctx, xs, ws, yb), steps, 3))
+    ms, window, count = time_row(lambda i=0: t.tpo_gemm_rs(ctx, xs, ws, yb), steps, 3, args.row_seconds)
     check(ctx)
     flops = 2.0 * wl.n * wl.k * wl.m
-    out[wl.name] = {"workload": "GEMM+RS e4m3 tp=8: X_r [16384,3584], W_r [8192,3584] -> 8 blocks [2048,8192]",
-                    "ms": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
-                    "frac_of_peak": round(flops / (ms * 1e-3) / 1e12 / (peak * FP8_OVER_BF16), 4),
-                    "peak_tflops": peak * FP8_OVER_BF16}
+    rec = {"workload": "GEMM+RS e4m3 tp=8: X_r [16384,3584], W_r [8192,3584] -> 8 blocks [2048,8192]",
+           "ms": round(ms, 4), "steps_timed": count}
+    rec.update(rates(flops, ms, peak * FP8_OVER_BF16, peak_sus * FP8_OVER_BF16))
+    rec["_window"] = window
     if fp8_lib:
-        out[wl.name]["frac_of_library_fp8"] = round(flops / (ms * 1e-3) / 1e12 / fp8_lib, 4)
+        rec["frac_of_library_fp8"] = round(flops / (ms * 1e-3) / 1e12 / fp8_lib, 4)
+    out[wl.name] = rec
     t.tpo_ctx_destroy(ctx)
     return out
+
+
+def noalloc_row(t, torch, dev, to_dev, peak, calls=50):
+    """The allocation-free AG entry point on the 4096^3 workload beside the
+    context call.  It returns only once its work is done (it reads the error
+    word back), so a call's time is the host's wall time around it."""
+    wl = synth.workload(HEADLINE)
+    xs = [to_dev(x) for x in wl.x]
+    w = to_dev(wl.w[0])
+    y = torch.empty((wl.n, wl.m), dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        t.tpo_ag_gemm_noalloc(wl.tp, wl.n, wl.k, wl.m, t.TPO_BF16, xs, w, y)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(calls):
+        t0 = time.perf_counter()
+        t.tpo_ag_gemm_noalloc(wl.tp, wl.n, wl.k, wl.m, t.TPO_BF16, xs, w, y)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.median(times)
+    tf = synth.flops(HEADLINE) / (ms * 1e-3) / 1e12
+    return {"workload": describe(HEADLINE), "ms_per_call_median": round(ms, 4), "tflops": round(tf, 2),
+            "frac_of_peak": round(tf / peak, 4), "peak_kind": "burst",
+            "note": "tpo_ag_gemm_noalloc: 8 producer CTAs, single-SM 128x256 tiles, blocking call (host wall "
+                    "time per call, median of %d, includes the launch and the read-back of the error word)" % calls}
 
 
 # ---------------------------------------------------------------------------- CPU oracle
@@ -637,6 +789,25 @@ def cpu_baseline(wl, seconds, others=None):
     if others:
         out["other_workloads"] = others
     return out
+
+
+def oracle_full(wl, reps=5):
+    """The oracle on the whole problem of a small workload (all host cores),
+    the fastest of `reps` runs."""
+    import oracle
+
+    g = oracle.gather(wl.x)
+    best = None
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.ag(g, wl.w[0], wl.scale_inv_x, wl.scale_inv_w)
+        dt = time.perf_counter() - t0
+        best = dt if best is None else min(best, dt)
+    flops = 2.0 * wl.n * wl.k * wl.m
+    return {"value": flops / best / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+            "sample": "the full problem (%d x %d output, FP64 loops over k=%d), fastest of %d runs" % (
+                wl.n, wl.m, wl.k, reps),
+            "full_problem_s": round(best, 5)}
 
 
 def other_sample(wl, seconds):
@@ -697,6 +868,10 @@ def main():
     ap.add_argument("--headline-only", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--timed-seconds", type=float, default=0.6,
+                    help="shortest timed region: the K-step block is repeated until it lasts this long")
+    ap.add_argument("--row-seconds", type=float, default=0.6,
+                    help="shortest timed region of each other workload")
     ap.add_argument("--reference-seconds", type=float, default=90.0,
                     help="oracle work for the whole reference-arm run (split over its steps)")
     args = ap.parse_args()

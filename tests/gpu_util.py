@@ -199,5 +199,10 @@ def check_wire(got, wire_ref, risky, bound, dtype):
         assert frac >= WIRE_EXACT_FRAC[dtype], "only %.4f of the elements equal the oracle's ring sum" % frac
 
 
-# Share of elements that must match the oracle's bf16 ring sum bit for bit.
-WIRE_EXACT_FRAC = {"bf16": 0.9, "e4m3": 0.9}
+# Share of elements that must match the oracle's bf16 ring sum bit for bit.  A
+# mismatch needs a partial within the kernel's fp32 error of a rounding
+# boundary: measured 0.99988-0.99999 of the elements match on the test cases
+# (bf16 and e4m3, tp 2 to 8); the kernel's arithmetic simulated on the CPU
+# with the ring starting at the owner, or with fp32 running sums, matches
+# 0.43-0.78 of them on the tp >= 3 cases.
+WIRE_EXACT_FRAC = {"bf16": 0.99, "e4m3": 0.99}

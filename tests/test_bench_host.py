@@ -57,3 +57,24 @@ def test_nominal_peak_fractions():
     assert nom["peak_at_max_clock"] == round(152 * 8192 * 2070e6 / 1e12, 1)
     assert abs(nom["frac_at_kernel_clock"] - 1000.0 / (152 * 8192 * 1850e6 / 1e12)) < 1e-4
     assert "peak_at_kernel_clock" not in bench.nominal_peak(1000.0, 152, 2070.0, None)
+
+
+def test_clock_windows_select_their_samples():
+    """Each measured region gets the samples inside its own wall-clock window:
+    median clock, maximum clock, the throttle reasons seen, sample count."""
+    import bench
+    c = bench.Clocks(0)
+    c.rows = [(10.0 + 0.05 * i, 1900.0 + i, 2070.0, 500.0, ["sw_power_cap"] if i == 3 else []) for i in range(40)]
+    w = c.window(10.01, 10.49)
+    assert w["samples"] == 11 and w["sm_max_mhz"] == 2070.0     # t = 10.00 .. 10.50 (50 ms margin)
+    assert w["sm_mhz"] == 1905.0 and w["reasons"] == ["sw_power_cap"]
+    w2 = c.window(11.01, 11.49)
+    assert w2["reasons"] == [] and w2["samples"] == 11
+    assert bench.Clocks(0).window(0, 1)["samples"] == 0          # no sampler: an empty record, no failure
+
+
+def test_oracle_full_problem_record():
+    import bench
+    from tensor_comm_gemm_gb300 import synth
+    rec = bench.oracle_full(synth.workload(0), reps=2)
+    assert rec["value"] > 0 and rec["cores"] >= 1 and rec["full_problem_s"] > 0

@@ -19,9 +19,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from tensor_comm_gemm_gb300 import synth
 from tensor_comm_gemm_gb300 import tpoverlap as t
-from gpu_util import AgRun, assert_close, host_bits, host_f64
+from gpu_util import AgRun, SAMPLE_TILE, SAMPLE_TILES, assert_close, gather_tiles, host_bits, host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -58,6 +59,10 @@ def test_noalloc_matches_context_entry_point_on_consecutive_calls(cases):
             _noalloc(run, y)                            # returns once the GPU work is done
             assert_close(host_f64(y), ref, wl.dtype)    # the tolerance of every parity test
             assert np.array_equal(host_bits(y), host_bits(run.y))  # same kernel, same tile arithmetic
+            if n * m > 1 << 22:   # large outputs: sampled tiles against the oracle itself as well
+                tiles = synth.sample_tiles(n, m, SAMPLE_TILE, SAMPLE_TILES, seed=1000 + seed)
+                want = oracle.ag(oracle.gather(wl.x), wl.w[0], wl.scale_inv_x, wl.scale_inv_w, tiles=tiles)
+                assert_close(gather_tiles(host_f64(y), tiles), want, wl.dtype)
             t.tpo_set_opt(run.ctx, "tail_split", 2)     # the split schedule meets the same bar
             run.run()
             assert_close(host_f64(run.y), host_f64(y), wl.dtype)
