@@ -219,6 +219,16 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      MMAs; used only where every accumulation unit has an
  *                      even number of K blocks).  Results are identical; one
  *                      block per stage measured 1.4-2.6 % faster on 4096^3.
+ *   "col_split"        column tiles per tile group (AG ring step, RS owner
+ *                      block, AR row chunk): 0 (default) the fewest tiles of
+ *                      at most 256 columns, the group's 32-column strips
+ *                      split evenly among them; otherwise 4 bits per group g
+ *                      < 16 ((v >> 4g) & 15) of extra tiles, splitting the
+ *                      strips into narrower tiles (down to 32 columns).
+ *                      Results are identical (the MMA computes every output
+ *                      element the same way whatever the tile width); a K
+ *                      block of a 128- to 256-column tile costs about the
+ *                      same time, so narrower tiles do not pay.
  *   "cta_group"        MMA variant: 0 automatic, 1 single-SM 128x256 tiles,
  *                      2 CTA pairs (2-SM MMA, 256x256 tiles; needs every tile
  *                      group a multiple of 256 rows).  Results are identical.
@@ -241,9 +251,11 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      (one 128 x 256 block per SM, fp32 in mode 1, bf16 in
  *                      mode 2), so the MMAs never wait for the additions.
  * Read-only keys for tpo_get_opt: "last_producer_ctas", "last_gemm_ctas",
- * "last_cta_group", "last_stage_kblocks", "last_split_tiles" (shape of the
- * context's latest kernel launch: producer CTAs, GEMM CTAs, 1 or 2 CTAs per
- * MMA, K blocks per pipeline stage, tiles split along K),
+ * "last_cta_group", "last_stage_kblocks", "last_split_tiles",
+ * "last_late_groups", "last_col_plan" (shape of the context's latest kernel
+ * launch: producer CTAs, GEMM CTAs, 1 or 2 CTAs per MMA, K blocks per
+ * pipeline stage, tiles split along K, producer CTA groups that joined the
+ * GEMM, extra column tiles per group in the col_split encoding),
  * "coop_clusters" (0 once the driver refused a cooperative cluster launch),
  * "tp", "n", "k", "m", "dtype" (the sizes the context was created for).
  * Environment variables TPO_<KEY in upper case> override the defaults at

@@ -15,6 +15,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "tpo_params.h"
 #include "tpoverlap.h"
@@ -96,7 +97,8 @@ struct tpo_ctx {
   // options
   int64_t producer_sms = 0, gemm_ctas = 0, mode = 0, seq_copy_ctas = 0, self_rank = 0, wait_timeout_ms = 2000,
           trace = 0, debug_skip_chunk = -1, debug_delay_ns = 0, debug_last_step = -1, cta_group = 0,
-          cooperative = 1, reduce = 0, tail_split = 0, debug_skip_partial = -1, stage_kblocks = 1;
+          cooperative = 1, reduce = 0, tail_split = 0, debug_skip_partial = -1, stage_kblocks = 1,
+          col_split = 0;
   // device memory
   uint8_t* staging = nullptr;
   size_t staging_bytes = 0;
@@ -120,8 +122,9 @@ struct tpo_ctx {
   int64_t last_producers = 0, last_gemm_ctas = 0, last_cta_group = 0;  // shape of the latest kernel launch
   int64_t last_kps = 0;          // K blocks per pipeline stage of the latest kernel launch
   int64_t last_split_tiles = 0;  // tail tiles of the latest kernel launch (AG tail split)
-  int64_t pc_key[4] = {-1, -1, -1, -1};  // producer count of the last AG launch shape (see producer_count)
-  int pc_val = 0;
+  int64_t pc_key[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};  // the last AG launch shape (see producer_count)
+  int pc_val = 0;                // its producer count
+  int64_t last_col_plan = 0;     // packed extra column tiles of the latest kernel launch (col_split encoding)
   int64_t last_late_groups = 0;  // producer CTA groups that joined its GEMM
   uint32_t part_epoch = 0;       // launches with the AG tail split so far (part_ready value of this launch)
   // tensor-map cache: the maps of the latest kCacheWays pointer sets of each op
@@ -161,6 +164,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
       {"tail_split", &tpo_ctx::tail_split, 0, 3},
       {"debug_skip_partial", &tpo_ctx::debug_skip_partial, -1, tpo::MAX_GEMM_CTAS - 1},
       {"stage_kblocks", &tpo_ctx::stage_kblocks, 1, 2},
+      {"col_split", &tpo_ctx::col_split, 0, INT64_MAX},
   };
   for (const E& e : table)
     if (std::strcmp(e.k, key) == 0) {
@@ -177,7 +181,8 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
 const char* kOptKeys[] = {"producer_sms",     "gemm_ctas",      "mode",           "seq_copy_ctas",
                           "self_rank",        "wait_timeout_ms", "trace",          "debug_skip_chunk",
                           "debug_delay_ns",   "debug_last_step", "cta_group",      "cooperative",
-                          "reduce",           "tail_split",     "debug_skip_partial", "stage_kblocks"};
+                          "reduce",           "tail_split",     "debug_skip_partial", "stage_kblocks",
+                          "col_split"};
 
 void destroy_all(tpo_ctx* c) {
   if (!c) return;
@@ -221,6 +226,8 @@ tpo_status reset_trace(tpo_ctx* c, cudaStream_t s) {
   return e == cudaSuccess ? TPO_OK : cuda_fail(e, "trace reset");
 }
 
+int64_t packed_columns(const Params& p);
+
 tpo_status launch(tpo_ctx* c, const Params& p, int grid, bool coop, cudaStream_t s) {
   c->last_producers = p.num_producers;
   c->last_gemm_ctas = p.num_gemm;
@@ -228,8 +235,9 @@ tpo_status launch(tpo_ctx* c, const Params& p, int grid, bool coop, cudaStream_t
   c->last_kps = p.kps;
   c->last_split_tiles = 0;
   c->last_late_groups = p.late_groups;
+  c->last_col_plan = packed_columns(p);
   if (p.tail_split && p.num_gemm > 0)
-    c->last_split_tiles = p.num_groups * p.row_tiles * p.col_tiles - p.split_full * (p.num_gemm / p.cta_group);
+    c->last_split_tiles = p.total_tiles - p.split_full * (p.num_gemm / p.cta_group);
   if (coop && (!c->cooperative || (p.cta_group == 2 && !c->coop_clusters))) coop = false;
   cudaError_t e = tpo::launch_fused(p, grid, coop, s);
   if (e != cudaSuccess && coop && p.cta_group == 2) {
@@ -311,47 +319,104 @@ int gemm_grid(const tpo_ctx* c, int cg, int64_t want, int producers, int tiles) 
   return static_cast<int>(2 * pairs);
 }
 
-// Estimated end (seconds) of an overlapped AG launch with P producer CTAs and
-// whole tiles: each GEMM group runs its round-robin tiles one after another,
-// none before its chunk has landed (ring step j at j times the chunk copy
-// time), and the launch also lasts until the copy of the observer's own
-// chunk (last) is done.  Rates as measured next to a running GEMM: a producer
-// CTA moves up to 37 GB/s of chunk data and all of them together up to
-// 705 GB/s, taken 1.25 times slower for margin; a CTA group spends 0.33 us
-// per 128-byte K block of a tile.
-double overlap_end(const tpo_ctx* c, int cg, int tiles, int nkb, int64_t chunk_bytes, int P) {
-  const int G = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, P, tiles) / cg;
-  const int per_group = std::max(1, tiles / c->tp);
-  const double rate = std::min(37e9, 705e9 / P) / 1.25;
-  const double tau = static_cast<double>(chunk_bytes) / (P * rate);
-  const double t_tile = nkb * 0.33e-6;
-  double end = c->tp * tau;
-  for (int g = 0; g < G; ++g) {
-    double t_end = 0;
-    for (int t = g; t < tiles; t += G) t_end = std::max(t_end, (t / per_group) * tau) + t_tile;
-    end = std::max(end, t_end);
+// ---------------------------------------------------------------- schedule model
+//
+// The host's model of a whole-tile launch: its G CTA groups take tiles round
+// robin, each group one tile after another, in the kernel's tile order; a
+// tile of AG ring step g waits until that step's chunk has landed
+// (ready_us[g]).  A tile costs nkb 128-byte K blocks of kKbUs x (0.91 + 0.09
+// w / 8) microseconds for w 32-column strips: measured on 256-row tile pairs,
+// a K block of a tile 128 to 256 columns wide costs 559 to 585 SM cycles,
+// with or without its operand loads (tcgen05.mma issue takes ~140 cycles per
+// instruction whatever its N), so narrower tiles save almost nothing.
+constexpr double kKbUs = 0.33;
+
+template <int TILE_M>
+double tiles_end_t(const Params& p, int G, const double* ready_us, int nkb) {
+  std::vector<double> ends(static_cast<size_t>(G), 0.0);
+  const double kb = nkb * kKbUs;
+  for (int t = 0; t < p.total_tiles; ++t) {
+    const tpo::TileIndex ti = tpo::tile_index<TILE_M>(p, t);
+    const int cols = tpo::group_cols_of(p, ti.group);
+    const int w = tpo::tile_strip0(p, cols, ti.c + 1) - tpo::tile_strip0(p, cols, ti.c);
+    double& e = ends[static_cast<size_t>(t % G)];
+    e = std::max(e, ready_us ? ready_us[ti.group] : 0.0) + kb * (0.91 + 0.09 * w / tpo::MAX_TILE_STRIPS);
   }
+  double end = 0;
+  for (double v : ends) end = std::max(end, v);
   return end;
 }
 
-// Producer CTAs of an overlapped AG call.  An explicit option wins.
+double tiles_end(const Params& p, int cg, int G, const double* ready_us, int nkb) {
+  return cg == 2 ? tiles_end_t<2 * tpo::BM>(p, G, ready_us, nkb) : tiles_end_t<tpo::BM>(p, G, ready_us, nkb);
+}
+
+// Column tiles of each group (sets p's column fields) for option col_split:
+// 0 (the default) gives every group the fewest tiles that are at most BN
+// wide; other values give group g (g < 16) ((v >> 4g) & 15) extra tiles,
+// splitting its strips evenly into narrower tiles.
+void plan_columns(const tpo_ctx* c, Params& p) {
+  tpo::set_columns(p, c->m, nullptr);
+  if (c->col_split <= 0) return;
+  int extra[tpo::MAX_GROUPS] = {};
+  const int most = std::min(p.strips, p.uniform_cols + 15);
+  for (int g = 0; g < p.num_groups && g < 16; ++g)
+    extra[g] = std::min(static_cast<int>((c->col_split >> (4 * g)) & 15), most - p.uniform_cols);
+  tpo::set_columns(p, c->m, extra);
+}
+
+// Packed extra column tiles of the first 16 groups (the col_split encoding).
+int64_t packed_columns(const Params& p) {
+  int64_t v = 0;
+  if (p.uniform_cols > 0) return 0;
+  const int base = (p.strips + tpo::MAX_TILE_STRIPS - 1) / tpo::MAX_TILE_STRIPS;
+  for (int g = 0; g < p.num_groups && g < 16; ++g)
+    v |= static_cast<int64_t>(std::min(15, p.group_cols[g] - base)) << (4 * g);
+  return v;
+}
+
+// Producer CTAs of an overlapped AG call, and the column tiles of its GEMM
+// (set in p).  An explicit producer_sms option wins.  `split` is the tail-split
+// schedule (0 none): its launches keep the fewest column tiles.
 //
-// With the tail split every GEMM group shortens the GEMM, so the count is the
-// smallest (from 4) that keeps the copy ahead of it.  Each gathered chunk must
-// land before the GEMM reaches its first tile, with 15% to spare, and the
-// whole staging copy (own chunk last) within 90% of the GEMM.  The model: a
-// producer CTA moves about 47 GB/s of chunk data (94 GB/s of HBM reads and
-// writes, whatever its depth of copies in flight), and a CTA group spends
-// about 0.3 us per 128-byte K block of a tile.
+// With the tail split's schedule 1 every GEMM group shortens the GEMM, so the
+// count is the smallest (from 4) that keeps the copy ahead of it.
+// Each gathered chunk must land before the GEMM reaches its first tile, with
+// 15% to spare, and the whole staging copy (own chunk last) within 90% of the
+// GEMM.  The model: a producer CTA moves about 47 GB/s of chunk data (94 GB/s
+// of HBM reads and writes, whatever its depth of copies in flight), and a CTA
+// group spends about 0.3 us per 128-byte K block of a tile.
 //
-// Without it (or when no count passes), a model of the whole-tile schedule
-// decides (overlap_end): the smallest count whose estimated end is within
-// 0.5 % of the best, i.e. the fewest copy SMs that do not delay the GEMM, so
-// that the copy disturbs the GEMM's loads least.  Computed once per launch
-// shape and kept in the context.
-int producer_count(tpo_ctx* c, int cg, int tiles, int nkb, int64_t chunk_bytes, bool split) {
-  if (c->producer_sms > 0) return static_cast<int>(c->producer_sms) + ((cg == 2) ? static_cast<int>(c->producer_sms & 1) : 0);
-  if (split) {
+// Without it, the schedule model decides for every producer count (even for
+// CTA pairs) up to 32: the GEMM grid that remains, a chunk copy time tau (a
+// producer CTA moves up to 37 GB/s of chunk data beside a running GEMM and all
+// of them together up to 705 GB/s, both taken 1.25 times slower for margin),
+// ring step g's chunk ready at g tau, and the launch lasting until the GEMM's
+// end and the copy of all tp chunks (the observer's own chunk last).  The fewest producers whose end is within 0.5 %
+// of the best win: fewer copy SMs disturb the GEMM's loads less.  Computed
+// once per launch shape and kept in the context.
+int producer_count(tpo_ctx* c, Params& p, int cg, int tiles, int nkb, int split) {
+  const int64_t chunk_bytes = p.chunk_bytes;
+  auto grid_of = [&](int P) {
+    return gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, P, tiles) / cg;
+  };
+  auto ready_of = [&](int P, double* ready) {
+    const double rate = std::min(37e9, 705e9 / P) / 1.25;
+    const double tau_us = static_cast<double>(chunk_bytes) / (P * rate) * 1e6;
+    for (int g = 0; g < c->tp; ++g) ready[g] = g * tau_us;
+    return c->tp * tau_us;
+  };
+  // the model's end for P producers over the launch's column tiles (the
+  // tail split keeps the fewest)
+  auto model_end = [&](int P, const double* ready) {
+    if (split)
+      tpo::set_columns(p, c->m, nullptr);
+    else
+      plan_columns(c, p);
+    return tiles_end(p, cg, grid_of(P), ready, nkb);
+  };
+  if (split == 1 && c->producer_sms <= 0) {
+    tpo::set_columns(p, c->m, nullptr);
     const double rate = 47e9, t_tile = nkb * 0.3e-6;
     const int per_group = tiles / c->tp;
     for (int P = 4; P <= 32 && P < c->num_sms - 2 * cg; P += cg) {
@@ -373,20 +438,35 @@ int producer_count(tpo_ctx* c, int cg, int tiles, int nkb, int64_t chunk_bytes, 
       if (ok) return P;
     }
   }
-  const int64_t key[4] = {cg, c->gemm_ctas, tiles, nkb};
-  if (std::memcmp(key, c->pc_key, sizeof(key)) == 0) return c->pc_val;
-  double best_end = 0;
-  double ends[33] = {};
-  for (int P = cg; P <= 32 && P <= c->num_sms - 2 * cg; P += cg) {
-    ends[P] = overlap_end(c, cg, tiles, nkb, chunk_bytes, P);
-    if (best_end == 0 || ends[P] < best_end) best_end = ends[P];
+  const int64_t key[9] = {cg, c->gemm_ctas, c->producer_sms, c->col_split, tiles, nkb, chunk_bytes, c->m, split};
+  if (std::memcmp(key, c->pc_key, sizeof(key)) == 0) {
+    if (split)
+      tpo::set_columns(p, c->m, nullptr);
+    else
+      plan_columns(c, p);
+    return c->pc_val;
   }
-  int best = 8;
-  for (int P = cg; P <= 32 && P <= c->num_sms - 2 * cg; P += cg)
-    if (ends[P] <= best_end * 1.005) {
-      best = P;
-      break;
+  int best = 0;
+  double ready[TPO_MAX_TP];
+  if (c->producer_sms > 0) {
+    best = static_cast<int>(c->producer_sms) + ((cg == 2) ? static_cast<int>(c->producer_sms & 1) : 0);
+  } else {
+    double ends[33] = {};
+    double best_end = 0;
+    for (int P = cg; P <= 32 && P <= c->num_sms - 2 * cg; P += cg) {
+      const double copy_end = ready_of(P, ready);
+      ends[P] = std::max(copy_end, model_end(P, ready));
+      if (best_end == 0 || ends[P] < best_end) best_end = ends[P];
     }
+    best = 8;
+    for (int P = cg; P <= 32 && P <= c->num_sms - 2 * cg; P += cg)
+      if (ends[P] <= best_end * 1.005) {
+        best = P;
+        break;
+      }
+  }
+  ready_of(best, ready);
+  model_end(best, ready);
   std::memcpy(c->pc_key, key, sizeof(key));
   c->pc_val = best;
   return best;
@@ -687,6 +767,7 @@ tpo_status tpo_get_opt(tpo_ctx* c, const char* key, int64_t* value) {
   if (std::strcmp(key, "last_stage_kblocks") == 0) return *value = c->last_kps, TPO_OK;
   if (std::strcmp(key, "last_split_tiles") == 0) return *value = c->last_split_tiles, TPO_OK;
   if (std::strcmp(key, "last_late_groups") == 0) return *value = c->last_late_groups, TPO_OK;
+  if (std::strcmp(key, "last_col_plan") == 0) return *value = c->last_col_plan, TPO_OK;
   if (std::strcmp(key, "coop_clusters") == 0) return *value = c->coop_clusters ? 1 : 0, TPO_OK;
   if (std::strcmp(key, "tp") == 0) return *value = c->tp, TPO_OK;
   if (std::strcmp(key, "n") == 0) return *value = c->n, TPO_OK;
@@ -748,7 +829,6 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   p.chunk_bytes = rows * c->k * elem;
   p.rows_per_group = static_cast<int>(rows);
   p.row_tiles = static_cast<int>(ceil_div(rows, tpo::BM * cg));
-  p.col_tiles = static_cast<int>(ceil_div(c->m, tpo::BN));
   p.m = static_cast<int>(c->m);
   p.y_rows = static_cast<int>(rows);
   p.num_groups = c->tp;
@@ -757,7 +837,8 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   p.gate = 1;
   // K blocks per pipeline stage: one (six stages) unless two are asked for (pairs, when they divide)
   p.kps = (cg == 2 && c->stage_kblocks == 2 && p.kb_per_seg % 2 == 0) ? 2 : 1;
-  const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
+  tpo::set_columns(p, c->m, nullptr);
+  const int tiles = p.total_tiles;  // with the fewest column tiles (the grid sizes follow this count)
 
   tpo_status st = reset_trace(c, s);
   if (st != TPO_OK) return st;
@@ -769,8 +850,9 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   // bits.
   const int split = (c->mode == 0 || c->mode == 1 || c->mode == 2) ? static_cast<int>(c->tail_split) : 0;
   const int nkb = p.kb_per_seg;
+  // producer count, GEMM grid and column plan of the overlapped launch
   auto overlap_grid = [&](int* P, int* G) {
-    *P = producer_count(c, cg, tiles, nkb, p.chunk_bytes, split == 1);  // even for CTA pairs: clusters of two
+    *P = producer_count(c, p, cg, tiles, nkb, split);  // even for CTA pairs: clusters of two
     *G = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - *P, *P, tiles);
   };
   // The GEMM launch of modes 0-2 with G GEMM CTAs and P producer CTAs.
@@ -813,17 +895,23 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       if (st != TPO_OK) return st;
       p.cta_group = cg;
       int P = 0, G = gemm_grid(c, cg, gemm_want, 0, tiles);
-      if (split) overlap_grid(&P, &G);
+      if (split)
+        overlap_grid(&P, &G);
+      else
+        plan_columns(c, p);
       return gemm_launch(P, G, false, false);
     }
     case 2: {  // GEMM only: chunks published by an earlier call
       std::memcpy(p.target, c->target, sizeof(p.target));
       int P = 0, G = gemm_grid(c, cg, gemm_want, 0, tiles);
-      if (split) overlap_grid(&P, &G);
+      if (split)
+        overlap_grid(&P, &G);
+      else
+        plan_columns(c, p);
       return gemm_launch(P, G, false, false);
     }
     case 4: {  // split: per ring step a chunk copy, then a GEMM launch over that slot
-      const int P = producer_count(c, cg, tiles, nkb, p.chunk_bytes, false);
+      const int P = producer_count(c, p, cg, tiles, nkb, 0);
       const int G = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, P, tiles / c->tp);
       cudaError_t e = cudaEventRecord(c->ev_fork, s);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(c->copy, c->ev_fork, 0);
@@ -847,6 +935,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       Params gp = p;
       gp.gate = 0;
       gp.num_groups = 1;
+      tpo::set_columns(gp, c->m, nullptr);  // one slot per launch, fewest column tiles
       gp.num_producers = 0;
       gp.num_gemm = G;
       const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -869,7 +958,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
       return e == cudaSuccess ? TPO_OK : cuda_fail(e, "split join");
     }
     default: {  // producer only
-      const int P = producer_count(c, cg, tiles, nkb, p.chunk_bytes, c->tail_split != 0);
+      const int P = producer_count(c, p, cg, tiles, nkb, static_cast<int>(c->tail_split));
       if (P > c->max_coop_grid) return fail(TPO_ERR_INVALID_ARG, "producer_sms too large");
       advance_targets(c, p, P);
       p.num_producers = P;
@@ -926,7 +1015,6 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   p.part_rows = static_cast<int>(part_rows);
   p.tiles_per_part = static_cast<int>(ceil_div(part_rows, tpo::BM * cg));
   p.row_tiles = (op == tpo::OP_AR) ? c->tp * p.tiles_per_part : p.tiles_per_part;
-  p.col_tiles = static_cast<int>(ceil_div(c->m, tpo::BN));
   p.m = static_cast<int>(c->m);
   p.y_rows = static_cast<int>(part_rows);
   p.num_groups = groups;
@@ -940,7 +1028,8 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   // pairs with stage_kblocks 2: two K blocks per stage when every accumulation unit has an even count
   p.kps = (cg == 2 && c->stage_kblocks == 2 &&
            (p.reduce_mode ? p.kb_per_seg : p.num_segs * p.kb_per_seg) % 2 == 0) ? 2 : 1;
-  const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
+  tpo::set_columns(p, c->m, nullptr);
+  const int tiles = p.total_tiles;  // with the fewest column tiles (the grid follows this count)
   tpo_status st = reset_trace(c, s);
   if (st != TPO_OK) return st;
   {
@@ -953,14 +1042,16 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
       c->done_op = op;
       c->done_groups = groups;
     }
-    // one release per epilogue warp of every CTA of every tile of the chunk
-    c->done_target += static_cast<uint32_t>(p.row_tiles * cg * p.col_tiles * tpo::EPI_WARPS);
+    // every epilogue warp of every CTA adds its tile's strip count: per group,
+    // row tiles x CTAs x strips x warps, whatever the group's column tiling
+    c->done_target += static_cast<uint32_t>(p.row_tiles * cg * p.strips * tpo::EPI_WARPS);
     p.done_target = c->done_target;
   }
   p.num_producers = 0;
   p.num_gemm = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms, 0, tiles);
   // the running-sum workspace has one block per SM: at most one GEMM CTA per SM
   if (p.reduce_mode && p.num_gemm > c->num_sms) p.num_gemm = c->num_sms - c->num_sms % cg;
+  plan_columns(c, p);
   return launch(c, p, p.num_gemm, false, s);
 }
 

@@ -225,10 +225,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
 }
 
 // Instruction descriptor: dense, fp32 accumulator, K-major A and B,
-// A/B bf16 (kind::f16) or e4m3 (kind::f8f6f4), M = tile rows, N = BN.
+// A/B bf16 (kind::f16) or e4m3 (kind::f8f6f4), M = tile rows; the tile's
+// width N (a multiple of 32 up to BN) is added per tile with idesc_n.
 __host__ __device__ constexpr uint32_t make_idesc(bool fp8, int m) {
-  return (1u << 4) | ((fp8 ? 0u : 1u) << 7) | ((fp8 ? 0u : 1u) << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-         (static_cast<uint32_t>(m >> 4) << 24);
+  return (1u << 4) | ((fp8 ? 0u : 1u) << 7) | ((fp8 ? 0u : 1u) << 10) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t idesc_n(uint32_t idesc, int n) {
+  return idesc | (static_cast<uint32_t>(n >> 3) << 17);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -385,6 +388,7 @@ struct Tile {
   int y_row;  // row coordinate of the output tile in its map
   int y_z;    // slot coordinate of the output tile in its map
   int col;    // first output column (= first W row)
+  int ncols;  // tile width: a multiple of 32 up to BN (may reach past m at the right edge)
   int seg0;   // RS/AR: rank of the first K segment
   int group;  // AR: row chunk
 };
@@ -393,27 +397,20 @@ struct Tile {
 // chunk).  Inside a group, blocks of up to 2048 rows are swept column tile by
 // column tile, rows fastest: consecutive CTAs share a W tile, and a block's
 // rows of X stay in L2 while its sweep passes over all of W (a group with
-// more rows would otherwise stream X from memory once per column tile).
+// more rows would otherwise stream X from memory once per column tile).  A
+// group's column tiles split its 32-column strips evenly (widths differ by at
+// most one strip); groups may have different column-tile counts, which the
+// host chooses so that the round-robin rounds come out even.
 // Every role of a CTA walks the same sequence t = g, g+G, ...
 template <int TILE_M>
 __device__ __forceinline__ Tile tile_at(const Params& p, int t) {
-  constexpr int RB = 2048 / TILE_M;  // row tiles per swept block
-  const int per_group = p.row_tiles * p.col_tiles;
-  const int grp = t / per_group;
-  const int rem = t - grp * per_group;
-  const int full = p.row_tiles / RB;      // whole blocks of RB row tiles
-  int c, r;
-  if (rem < full * RB * p.col_tiles) {
-    const int b = rem / (RB * p.col_tiles), w = rem - b * RB * p.col_tiles;
-    c = w / RB;
-    r = b * RB + (w - c * RB);
-  } else {                                // the last, shorter block
-    const int h = p.row_tiles - full * RB, w = rem - full * RB * p.col_tiles;
-    c = w / h;
-    r = full * RB + (w - c * h);
-  }
+  const TileIndex ti = tile_index<TILE_M>(p, t);
+  const int grp = ti.group, r = ti.r;
+  const int cols = group_cols_of(p, grp);
+  const int s0 = tile_strip0(p, cols, ti.c), s1 = tile_strip0(p, cols, ti.c + 1);
   Tile T;
-  T.col = c * BN;
+  T.col = s0 * STRIP;
+  T.ncols = (s1 - s0) * STRIP;
   T.group = grp;
   if (p.op == OP_AG) {
     const int slot = ((p.self_rank - grp) % p.tp + p.tp) % p.tp;
@@ -707,7 +704,7 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
   const int kelems = p.fp8 ? BK_BYTES : BK_BYTES / 2;
   const uint32_t full0 = B.full0, empty0 = B.empty0;
   const uint32_t full0_leader = (CG == 2) ? map_to_rank(full0, 0) : full0;
-  const int a_off = BM * static_cast<int>(rank), b_off = PP::B_ROWS * static_cast<int>(rank);
+  const int a_off = BM * static_cast<int>(rank);
   constexpr uint32_t kps = KPS;
   constexpr uint32_t stage_bytes = kps * PP::STAGE_BYTES;
   constexpr uint32_t nstages = STAGE_AREA / stage_bytes;
@@ -727,7 +724,9 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
     }
     int r = AG ? T.a_map : T.seg0;  // tensor map of the current K segment
     int kk = sg.kb_lo;               // (RS/AR segments always start at K block 0)
-    const int a_row = T.a_row + a_off, a_z = T.a_z, b_row = T.col + b_off;
+    // each CTA of a pair loads half of the tile's B rows (its box may reach
+    // into the next tile's rows, which the MMA does not read)
+    const int a_row = T.a_row + a_off, a_z = T.a_z, b_row = T.col + (CG == 2 ? (T.ncols >> 1) * static_cast<int>(rank) : 0);
     for (int i = sg.kb_lo; i < sg.kb_hi; i += KPS) {  // one stage of KPS K blocks per pass
       const uint32_t sbase_stage = sbase + SMEM_STAGES + stage * stage_bytes;
       // wait until the MMAs released the stage, then arm its barrier
@@ -803,7 +802,7 @@ template <int CG, bool FP8, bool SPLIT, int KPS>
 __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
                          int total_tiles, int nkb, bool trace, const TailDesc* tail) {
   using PP = Pipe<CG>;
-  constexpr uint32_t idesc = make_idesc(FP8, PP::TILE_M);
+  constexpr uint32_t idesc0 = make_idesc(FP8, PP::TILE_M);
   constexpr uint32_t kps = KPS;
   const uint32_t stage_bytes = kps * PP::STAGE_BYTES;
   const uint32_t nstages = STAGE_AREA / stage_bytes;
@@ -824,7 +823,8 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   unsigned long long cyc_full = 0, cyc_tempty = 0;
   SegIter<SPLIT> it(p, g, G, total_tiles, nkb, tail);
   Seg sg;
-  while (ok && it.next(sg))
+  while (ok && it.next(sg)) {
+   const uint32_t idesc = idesc_n(idesc0, tile_at<PP::TILE_M>(p, sg.t).ncols);
    for (int u = 0; u < units; ++u, ++ul) {
     const uint32_t acc = ul & 1u;
     const uint32_t te = tempty0 + 8u * acc;
@@ -863,6 +863,7 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
     if (!ok) break;
     mma_commit_cg<CG>(tfull0 + 8u * acc);  // accumulator ready for the epilogue(s)
    }
+  }
   if (!ok) {  // every MMA issued so far must complete before tensor memory is freed
     mma_commit_local_cg<CG>(B.drain);
     mbar_wait(p, B.drain, 0u, SITE_DRAIN, false);
@@ -955,14 +956,15 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
       for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(h[e]));
     };
     uint32_t pa[32];
+    const int nch = T.ncols / EPI_COLS;
     if (!write && sg.nw > 0) load_part(0, 0, pa);
 #pragma unroll 1
-    for (int c = 0; c < BN / EPI_COLS; ++c) {
+    for (int c = 0; c < nch; ++c) {
       uint32_t pn[32];
-      if (!write && sg.nw > 0 && c + 1 < BN / EPI_COLS) load_part(0, c + 1, pn);
+      if (!write && sg.nw > 0 && c + 1 < nch) load_part(0, c + 1, pn);
       uint32_t r[32];
       tmem_ld32_sync(taddr + c * EPI_COLS, r);
-      if (c == BN / EPI_COLS - 1) {  // accumulator fully read: hand it back to the MMA issuer
+      if (c == nch - 1) {  // accumulator fully read: hand it back to the MMA issuer
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -1043,6 +1045,7 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
       mbar_wait(p, bar, par, SITE_TMEM_FULL, false);  // already complete: gives every lane its ordering
       tc_fence_after();
       const bool last = (u == units - 1);
+      const int nch = T.ncols / EPI_COLS;  // 32-column chunks of this tile
       const uint32_t lanes = static_cast<uint32_t>(quad * 32) << 16;
       const uint32_t taddr = tmem + lanes + acc * BN;
       // The running sum of this thread's row, 32 columns per chunk: fp32 in
@@ -1096,7 +1099,7 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
       auto chunk = [&](int c, const uint32_t(&q)[32], bool have_q) {
         uint32_t r[32];
         tmem_ld32_sync(taddr + c * EPI_COLS, r);
-        if (c == BN / EPI_COLS - 1) {  // accumulator fully read: hand it back to the MMA issuer
+        if (c == nch - 1) {  // accumulator fully read: hand it back to the MMA issuer
           tc_fence_before();
           __syncwarp();
           if (lane == 0) {
@@ -1162,23 +1165,27 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
         uint32_t qa[32], qb[32];
         load_sum(0, qa);
 #pragma unroll 1
-        for (int c = 0; c < BN / EPI_COLS; c += 2) {
-          load_sum(c + 1, qb);
+        for (int c = 0; c < nch; c += 2) {
+          const bool two = c + 1 < nch;
+          if (two) load_sum(c + 1, qb);
           chunk(c, qa, true);
-          if (c + 2 < BN / EPI_COLS) load_sum(c + 2, qa);
-          chunk(c + 1, qb, true);
+          if (c + 2 < nch) load_sum(c + 2, qa);
+          if (two) chunk(c + 1, qb, true);
         }
       } else {
         const uint32_t none[32] = {};
 #pragma unroll 1
-        for (int c = 0; c < BN / EPI_COLS; ++c) chunk(c, none, false);
+        for (int c = 0; c < nch; ++c) chunk(c, none, false);
       }
     }
     if (ok_all && p.op != OP_AG && lane == 0) {  // this warp's rows of the tile are in memory: count them
+      // one count per 32-column strip, so that every group's count ends at the
+      // same target whatever its column tiling
       bulk_wait<0>();
       fence_proxy_async_global();
-      const uint32_t old = atom_add_release(&p.words->done[T.group], 1u);
-      if (p.trace_on && old + 1u == p.done_target) p.words->trace[TPO_TRACE_CHUNK_DONE + T.group] = gtime();
+      const uint32_t add = static_cast<uint32_t>(T.ncols / EPI_COLS);
+      const uint32_t old = atom_add_release(&p.words->done[T.group], add);
+      if (p.trace_on && old + add == p.done_target) p.words->trace[TPO_TRACE_CHUNK_DONE + T.group] = gtime();
     }
   }
   if (lane == 0) bulk_wait<0>();
@@ -1204,7 +1211,7 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
   // GEMM CTAs are groups 0 .. G-1; producer CTAs that join afterwards follow
   const int bid = static_cast<int>(blockIdx.x), G = p.num_gemm / CG;
   const int g = bid >= p.num_producers ? (bid - p.num_producers) / CG : G + bid / CG;
-  const int total_tiles = p.num_groups * p.row_tiles * p.col_tiles;
+  const int total_tiles = p.total_tiles;
   const int nkb = p.num_segs * p.kb_per_seg;
   if (threadIdx.x == 0) {
     for (int s = 0; s < MAX_STAGES; ++s) {

@@ -189,15 +189,15 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
   p.self_rank = 0;
   p.rows_per_group = static_cast<int>(rows);
   p.row_tiles = static_cast<int>((rows + tpo::BM - 1) / tpo::BM);
-  p.col_tiles = static_cast<int>((m + tpo::BN - 1) / tpo::BN);
   p.m = static_cast<int>(m);
   p.y_rows = static_cast<int>(rows);
   p.num_groups = tp;
   p.kb_per_seg = static_cast<int>((k * elem + tpo::BK_BYTES - 1) / tpo::BK_BYTES);
   p.num_segs = 1;
   p.gate = 1;
+  tpo::set_columns(p, m, nullptr);  // every group: the fewest column tiles of at most 256 columns
   const int P = kProducers < s->num_sms - 1 ? kProducers : s->num_sms - 1;
-  const int tiles = p.num_groups * p.row_tiles * p.col_tiles;
+  const int tiles = p.total_tiles;
   int G = s->num_sms - P;
   if (G > tiles) G = tiles;
   if (P < 1 || G < 1 || P + G > s->max_coop_grid) return fail(TPO_ERR_UNSUPPORTED, "device too small");

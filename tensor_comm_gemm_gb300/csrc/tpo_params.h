@@ -35,6 +35,13 @@ constexpr int MAX_STAGES = 6;
 constexpr int NUM_THREADS = 192;              // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int EPI_WARPS = 4;
 constexpr int EPI_COLS = 32;                  // columns per epilogue store box
+// Tile widths are whole 32-column strips (one epilogue store box each): a
+// group's strips across m are split evenly into its column tiles, each of
+// MIN_TILE_STRIPS .. BN / STRIP strips.
+constexpr int STRIP = EPI_COLS;
+constexpr int MAX_TILE_STRIPS = BN / STRIP;   // 8: a full BN-column tile
+constexpr int MIN_TILE_STRIPS = 4;            // narrowest tile a column plan may choose (128 columns)
+constexpr int MAX_GROUPS = TPO_MAX_ROW_CHUNKS;  // tile groups of one launch (AG slots, RS blocks, AR chunks)
 constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;  // 32 rows x 32 bf16
 constexpr int TMEM_COLS = 512;                // two BN-column fp32 accumulators
 
@@ -131,7 +138,11 @@ struct Params {
   int num_gemm;           // CTAs [num_producers, +num_gemm) run the GEMM role
   int rows_per_group;     // AG: rows per slot; RS: rows per block; AR: rows per chunk
   int row_tiles;          // row tiles per group (the last one may be partial)
-  int col_tiles;          // BN tiles across m (the last one may be partial)
+  int strips;             // 32-column strips across m (the last one may be partial)
+  int uniform_cols;       // > 0: every group has this many column tiles (group_cols unused)
+  int total_tiles;        // tiles of the launch over all groups
+  int group_cols[MAX_GROUPS];      // column tiles of each group (strips split evenly among them)
+  int group_base[MAX_GROUPS + 1];  // first tile of each group
   int part_rows;          // AR: rows of one ring-order part of a chunk (rows_per_group / tp)
   int tiles_per_part;     // AR: row tiles per part
   int m;                  // output columns
@@ -158,6 +169,68 @@ struct Params {
   int copy_on;            // producer CTAs copy (0: they only run as late GEMM groups)
   int skip_part;          // test hook: this GEMM CTA never publishes its partial (-1: none)
 };
+
+// Column tiling of a launch with p.num_groups groups of p.row_tiles row tiles
+// over m columns.  extra[g] (or all zero if extra is null) adds column tiles
+// to group g beyond the fewest that keep every tile at most BN wide; the
+// caller keeps each group within [ceil(strips / 8), strips] tiles.
+inline void set_columns(Params& p, long long m, const int* extra) {
+  p.strips = static_cast<int>((m + STRIP - 1) / STRIP);
+  const int base = (p.strips + MAX_TILE_STRIPS - 1) / MAX_TILE_STRIPS;
+  bool uniform = true;
+  p.group_base[0] = 0;
+  for (int g = 0; g < p.num_groups; ++g) {
+    p.group_cols[g] = base + (extra ? extra[g] : 0);
+    uniform = uniform && p.group_cols[g] == base;
+    p.group_base[g + 1] = p.group_base[g] + p.row_tiles * p.group_cols[g];
+  }
+  p.uniform_cols = uniform ? base : 0;
+  p.total_tiles = p.group_base[p.num_groups];
+}
+
+// A tile of the launch (see tile_at in the kernel): its group, its column
+// index inside the group's column sweep and its row tile.  Host and device
+// share this arithmetic, so that the host's schedule model walks the tiles
+// the kernel computes.
+struct TileIndex {
+  int group, c, r;
+};
+template <int TILE_M>
+__host__ __device__ __forceinline__ TileIndex tile_index(const Params& p, int t) {
+  constexpr int RB = 2048 / TILE_M;  // row tiles per swept block
+  int grp, cols, rem;
+  if (p.uniform_cols > 0) {
+    const int per_group = p.row_tiles * p.uniform_cols;
+    grp = t / per_group;
+    rem = t - grp * per_group;
+    cols = p.uniform_cols;
+  } else {
+    grp = 0;
+    while (grp + 1 < p.num_groups && t >= p.group_base[grp + 1]) ++grp;
+    rem = t - p.group_base[grp];
+    cols = p.group_cols[grp];
+  }
+  const int full = p.row_tiles / RB;  // whole blocks of RB row tiles
+  TileIndex ti;
+  ti.group = grp;
+  if (rem < full * RB * cols) {
+    const int b = rem / (RB * cols), w = rem - b * RB * cols;
+    ti.c = w / RB;
+    ti.r = b * RB + (w - ti.c * RB);
+  } else {  // the last, shorter block
+    const int h = p.row_tiles - full * RB, w = rem - full * RB * cols;
+    ti.c = w / h;
+    ti.r = full * RB + (w - ti.c * h);
+  }
+  return ti;
+}
+// First strip of column tile c of a group with `cols` column tiles.
+__host__ __device__ __forceinline__ int tile_strip0(const Params& p, int cols, int c) {
+  return static_cast<int>(static_cast<long long>(c) * p.strips / cols);
+}
+__host__ __device__ __forceinline__ int group_cols_of(const Params& p, int grp) {
+  return p.uniform_cols > 0 ? p.uniform_cols : p.group_cols[grp];
+}
 
 // Zeroes a launch description and sets every field whose "off" value is not 0.
 inline void init_params(Params& p) {

@@ -326,10 +326,9 @@ def test_default_producer_count_follows_the_schedule_model(tp, n, k, m, dtype):
         t.tpo_ag_gemm(ctx, xs, w, y, sx, sx)
         assert t.tpo_sync_status(ctx) == 0, t.tpo_last_error()
         sms = torch.cuda.get_device_properties(0).multi_processor_count
-        nkb = -(-k * (1 if fp8 else 2) // 128)
-        tiles = tp * (n // tp // 256) * (m // 256)
-        want = producer_choice(tp, tiles, nkb, n // tp * k * (1 if fp8 else 2), cg=2, num_sms=sms)
-        assert t.tpo_get_opt(ctx, "last_producer_ctas") == want
+        P = producer_choice(tp, n // tp, k, m, elem=1 if fp8 else 2, cg=2, num_sms=sms)
+        assert t.tpo_get_opt(ctx, "last_producer_ctas") == P
+        assert t.tpo_get_opt(ctx, "last_col_plan") == 0        # whole tiles by default
         assert not torch.isnan(y).any()
     finally:
         t.tpo_ctx_destroy(ctx)

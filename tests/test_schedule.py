@@ -13,39 +13,70 @@ import pytest
 from tensor_comm_gemm_gb300 import synth
 
 BM, BN, BK_BYTES, COPY_PIECE, EPI_COLS = 128, 256, 128, 16384, 32
+STRIP, MAX_TILE_STRIPS, MIN_TILE_STRIPS = 32, 8, 4
 
 
 def cdiv(a, b):
     return -(-a // b)
 
 
-def tile_at(op, tp, self_rank, pl, t):
-    """The kernel's tile_at: A and output coordinates are (row, slot) pairs of
-    the 3-D [inner, rows, slot] tensor maps."""
-    row_tiles, col_tiles, tile_m, rpg = pl["row_tiles"], pl["col_tiles"], pl["tile_m"], pl["rows_per_group"]
-    per = row_tiles * col_tiles
-    grp, rem = divmod(t, per)
+def set_columns(pl, m, extra=None):
+    """The host's set_columns: 32-column strips across m, each group's column
+    tiles (the fewest of at most 8 strips, plus extra[g]), group start tiles."""
+    pl["strips"] = cdiv(m, STRIP)
+    base = cdiv(pl["strips"], MAX_TILE_STRIPS)
+    pl["base_cols"] = base
+    pl["group_cols"] = [base + (extra[g] if extra else 0) for g in range(pl["groups"])]
+    pl["group_base"] = [0]
+    for cols in pl["group_cols"]:
+        pl["group_base"].append(pl["group_base"][-1] + pl["row_tiles"] * cols)
+    pl["total"] = pl["group_base"][-1]
+    return pl
+
+
+def tile_index(pl, t):
+    """tile_index: (group, column tile, row tile) of tile t."""
+    row_tiles, tile_m = pl["row_tiles"], pl["tile_m"]
+    grp = max(g for g in range(pl["groups"]) if pl["group_base"][g] <= t)
+    rem, cols = t - pl["group_base"][grp], pl["group_cols"][grp]
     rb = 2048 // tile_m                    # row tiles per block swept column by column
     full = row_tiles // rb
-    if rem < full * rb * col_tiles:
-        b, w = divmod(rem, rb * col_tiles)
+    if rem < full * rb * cols:
+        b, w = divmod(rem, rb * cols)
         c, rr0 = divmod(w, rb)
         r = b * rb + rr0
     else:
         h = row_tiles - full * rb
-        c, rr0 = divmod(rem - full * rb * col_tiles, h)
+        c, rr0 = divmod(rem - full * rb * cols, h)
         r = full * rb + rr0
-    col = c * BN
+    return grp, c, r
+
+
+def tile_strips(pl, grp, c):
+    """First strip and strip count of column tile c of group grp (even split)."""
+    cols = pl["group_cols"][grp]
+    s0, s1 = c * pl["strips"] // cols, (c + 1) * pl["strips"] // cols
+    return s0, s1 - s0
+
+
+def tile_at(op, tp, self_rank, pl, t):
+    """The kernel's tile_at: A and output coordinates are (row, slot) pairs of
+    the 3-D [inner, rows, slot] tensor maps; col and ncols the tile's columns."""
+    tile_m, rpg = pl["tile_m"], pl["rows_per_group"]
+    grp, c, r = tile_index(pl, t)
+    s0, w = tile_strips(pl, grp, c)
+    col, ncols = s0 * STRIP, w * STRIP
     if op == "ag":
         slot = (self_rank - grp) % tp
         return dict(a_map=1 if grp == 0 else 0, a_row=r * tile_m, a_z=0 if grp == 0 else slot,
-                    gate=-1 if grp == 0 else slot, y_map=0, y_row=r * tile_m, y_z=slot, col=col, seg0=0, group=grp)
+                    gate=-1 if grp == 0 else slot, y_map=0, y_row=r * tile_m, y_z=slot, col=col, ncols=ncols,
+                    seg0=0, group=grp)
     if op == "rs":
         return dict(a_map=-1, a_row=grp * rpg + r * tile_m, a_z=0, gate=-1, y_map=grp, y_row=r * tile_m, y_z=0,
-                    col=col, seg0=(grp + 1) % tp, group=grp)
+                    col=col, ncols=ncols, seg0=(grp + 1) % tp, group=grp)
     part, rr = divmod(r, pl["tiles_per_part"])
     return dict(a_map=-1, a_row=grp * rpg + part * pl["part_rows"] + rr * tile_m, a_z=0, gate=-1, y_map=0,
-                y_row=rr * tile_m, y_z=grp * tp + part, col=col, seg0=(part + 1) % tp, group=grp)
+                y_row=rr * tile_m, y_z=grp * tp + part, col=col, ncols=ncols, seg0=(part + 1) % tp, group=grp)
 
 
 def choose_cg(op, tp, n, chunks):
@@ -64,9 +95,10 @@ def plan(op, tp, n, k, m, elem=2, chunks=1, cg=1):
     part_rows = rows // tp if op == "ar" else rows
     tpp = cdiv(part_rows, tile_m)
     kseg = k if op == "ag" else k // tp
-    return dict(rows_per_group=rows, part_rows=part_rows, tiles_per_part=tpp,
-                row_tiles=tp * tpp if op == "ar" else tpp, col_tiles=cdiv(m, BN), groups=groups,
-                kb=cdiv(kseg * elem, BK_BYTES), tile_m=tile_m, y_rows=part_rows)
+    pl = dict(rows_per_group=rows, part_rows=part_rows, tiles_per_part=tpp,
+              row_tiles=tp * tpp if op == "ar" else tpp, groups=groups,
+              kb=cdiv(kseg * elem, BK_BYTES), tile_m=tile_m, y_rows=part_rows)
+    return set_columns(pl, m)
 
 
 SHAPES = [("ag", 2, 256, 256, 256, 2, 1), ("ag", 4, 4096, 4096, 4096, 2, 1), ("ag", 8, 16384, 8192, 28672, 1, 1),
@@ -82,13 +114,27 @@ SHAPES = [("ag", 2, 256, 256, 256, 2, 1), ("ag", 4, 4096, 4096, 4096, 2, 1), ("a
           ("ar", 1, 5000, 64, 264, 2, 1)]
 
 
+def column_plans(pl, m):
+    """Column plans to check: the fewest tiles everywhere, the most every group
+    may take, and seeded random extras in between."""
+    import random
+    base, strips = pl["base_cols"], pl["strips"]
+    top = min(strips - base, 15)
+    plans = [None, [top] * pl["groups"]]
+    rnd = random.Random(pl["groups"] * 1000 + m)
+    plans += [[rnd.randint(0, top) for _ in range(pl["groups"])] for _ in range(2)]
+    return plans
+
+
 @pytest.mark.parametrize("op,tp,n,k,m,elem,chunks", SHAPES)
 @pytest.mark.parametrize("cg", [1, 2])
-def test_tiles_cover_output_once_in_bounds(op, tp, n, k, m, elem, chunks, cg):
+@pytest.mark.parametrize("cplan", range(4))
+def test_tiles_cover_output_once_in_bounds(op, tp, n, k, m, elem, chunks, cg, cplan):
     if cg == 2 and choose_cg(op, tp, n, chunks) != 2:
         pytest.skip("shape served by the single-SM variant")
     pl = plan(op, tp, n, k, m, elem, chunks, cg)
-    total = pl["groups"] * pl["row_tiles"] * pl["col_tiles"]
+    set_columns(pl, m, column_plans(pl, m)[cplan])
+    total = pl["total"]
     kel = BK_BYTES // elem
     kcols = k if op == "ag" else k // tp
     assert (kcols * elem) % 16 == 0 and (m * 2) % 16 == 0  # 16-byte row pitches
@@ -111,9 +157,14 @@ def test_tiles_cover_output_once_in_bounds(op, tp, n, k, m, elem, chunks, cg):
                     assert T["a_row"] == T["y_map"] * pl["rows_per_group"] + T["y_row"]
                 else:
                     assert T["a_row"] == T["y_z"] * pl["part_rows"] + T["y_row"]
-                assert T["a_row"] + off >= 0 and T["col"] + b_rows * rank >= 0
+                # the tile's width: whole strips, at most BN; each CTA of a pair
+                # loads half of its B rows, which its B box covers
+                assert T["ncols"] % STRIP == 0 and STRIP <= T["ncols"] <= BN and T["col"] < m
+                b0 = T["col"] + (T["ncols"] // 2) * rank if cg == 2 else T["col"]
+                assert b0 >= 0 and T["ncols"] // cg <= b_rows
+                assert T["a_row"] + off >= 0
                 for q in range(4):
-                    for c in range(BN // EPI_COLS):
+                    for c in range(T["ncols"] // EPI_COLS):
                         ox, oy = T["col"] + c * EPI_COLS, T["y_row"] + off + 32 * q
                         assert (ox * 2) % 16 == 0 and oy >= 0   # stores never start at a negative coordinate
                         if ox >= m or oy >= y_rows:
@@ -335,42 +386,86 @@ def gemm_grid(cg, want, P, tiles, max_pairs=76):
     return 2 * max(1, min(want // 2, max_pairs - P // 2, tiles))
 
 
-def overlap_end(tp, tiles, nkb, chunk_bytes, P, cg=2, num_sms=152):
-    """The host's model of an overlapped whole-tile launch (producer_count)."""
-    G = gemm_grid(cg, num_sms - P, P, tiles, max_pairs=num_sms // 2) // cg
-    per = max(1, tiles // tp)
-    rate = min(37e9, 705e9 / P) / 1.25
-    tau = chunk_bytes / (P * rate)
-    t_tile = nkb * 0.33e-6
-    end = tp * tau
-    for g in range(G):
-        t_end = 0.0
-        for t in range(g, tiles, G):
-            t_end = max(t_end, (t // per) * tau) + t_tile
-        end = max(end, t_end)
-    return end
+KB_US = 0.33
 
 
-def producer_choice(tp, tiles, nkb, chunk_bytes, cg=2, num_sms=152):
-    ends = {P: overlap_end(tp, tiles, nkb, chunk_bytes, P, cg, num_sms)
-            for P in range(cg, 33, cg) if P <= num_sms - 2 * cg}
+def tiles_end(pl, G, ready, nkb):
+    """The host's schedule model: G CTA groups take tiles round robin in the
+    kernel's order; a tile of group g starts no earlier than ready[g]; a tile
+    of w strips costs nkb K blocks of KB_US x (0.91 + 0.09 w / 8) microseconds
+    (measured: a K block of a 128- to 256-column tile pair costs 559 to 585 SM
+    cycles, so the width hardly matters)."""
+    ends = [0.0] * G
+    for t in range(pl["total"]):
+        grp, c, _ = tile_index(pl, t)
+        w = tile_strips(pl, grp, c)[1]
+        q = t % G
+        ends[q] = max(ends[q], ready[grp] if ready else 0.0) + nkb * KB_US * (0.91 + 0.09 * w / MAX_TILE_STRIPS)
+    return max(ends)
+
+
+def gemm_grid(cg, want, P, tiles, max_pairs=76):
+    """The host's GEMM grid: single CTAs up to the tile count, or pairs up to
+    the co-resident pairs left next to the producers."""
+    if cg == 1:
+        return max(1, min(want, tiles))
+    return 2 * max(1, min(want // 2, max_pairs - P // 2, tiles))
+
+
+def producer_choice(tp, rows, k, m, elem=2, cg=2, num_sms=152):
+    """The host's producer count of an overlapped AG launch (fewest column
+    tiles): the fewest producers whose modelled end is within 0.5 % of the
+    best, the end being the later of the GEMM's and the copy of all chunks."""
+    pl = plan("ag", tp, tp * rows, k, m, elem, 1, cg)
+    tiles, nkb = pl["total"], pl["kb"]
+    chunk = rows * k * elem
+    ends = {}
+    for P in range(cg, 33, cg):
+        if P > num_sms - 2 * cg:
+            break
+        G = gemm_grid(cg, num_sms - P, P, tiles, num_sms // 2) // cg
+        rate = min(37e9, 705e9 / P) / 1.25
+        tau = chunk / (P * rate) * 1e6
+        ends[P] = max(tp * tau, tiles_end(pl, G, [g * tau for g in range(tp)], nkb))
     best = min(ends.values())
-    return min(P for P, e in ends.items() if e <= best * 1.005)
+    return min(q for q, e in ends.items() if e <= best * 1.005)
+
+
+def packed(extra):
+    """The col_split option's encoding: 4 bits of extra column tiles per group."""
+    return sum(min(15, e) << (4 * g) for g, e in enumerate(extra[:16]))
 
 
 def test_producer_model_choices():
     """C2 (4096^3, 4 chunks of 8 MiB): the fewest producers whose copy keeps
     ahead of 4 rounds; C5 (e4m3, 8 chunks of 16 MiB, 7168 tiles): a handful,
     since the first gathered chunk is needed only after ~12 rounds."""
-    assert producer_choice(4, 256, 64, 1024 * 4096 * 2) == 14
-    assert producer_choice(8, 7168, 64, 2048 * 8192) == 4
+    assert producer_choice(4, 1024, 4096, 4096) == 14
+    assert producer_choice(8, 2048, 8192, 28672, elem=1) == 4
+
+
+def test_explicit_column_plans_keep_tiles_between_one_and_eight_strips():
+    """Any col_split value: every group's strips are split evenly into its
+    column tiles, each 1 to 8 strips wide, adding up to the group's strips."""
+    for m in (256, 264, 520, 1000, 4096):
+        pl = plan("ag", 4, 4096, 512, m, 2, 1, 2)
+        base = pl["base_cols"]
+        top = min(pl["strips"], base + 15) - base
+        for extra in ([0] * 4, [top] * 4, [1, 0, top, 2]):
+            set_columns(pl, m, extra)
+            for g in range(4):
+                widths = [tile_strips(pl, g, c)[1] for c in range(pl["group_cols"][g])]
+                assert sum(widths) == pl["strips"] and 1 <= min(widths) and max(widths) <= MAX_TILE_STRIPS
+                assert max(widths) - min(widths) <= 1
 
 
 def test_producer_model_properties():
-    # more producers never delay the chunks: the model's end is monotone in
-    # the copy time as long as the GEMM grid is unchanged
-    for P in (2, 4, 8):
-        assert overlap_end(4, 256, 64, 1 << 23, P) >= overlap_end(4, 256, 64, 1 << 23, P + 2) or \
-            gemm_grid(2, 152 - P - 2, P + 2, 256) != gemm_grid(2, 152 - P, P, 256)
-    # a group never starts a tile before that tile's chunk could have landed
-    assert overlap_end(2, 2, 64, 1 << 30, 2) >= 2 * (1 << 30) / (2 * 37e9 / 1.25)
+    # a group never starts a tile before its chunk could have landed
+    pl = plan("ag", 2, 2 * 256, 64, 256, 2, 1, 2)
+    ready = [0.0, 1e6]
+    assert tiles_end(pl, 1, ready, 1) >= 1e6
+    # more column tiles never lose work: the tiles' strips add up to the group's
+    for extra in ([0, 0], [1, 3], [2, 0]):
+        set_columns(pl, 256, extra)
+        for g in range(2):
+            assert sum(tile_strips(pl, g, c)[1] for c in range(pl["group_cols"][g])) == pl["strips"]
