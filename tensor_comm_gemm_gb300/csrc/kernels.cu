@@ -480,6 +480,7 @@ enum SegKind : int { SEG_WHOLE = 0, SEG_FINISH = 1, SEG_WRITE = 2 };
 struct Seg {
   int t, kb_lo, kb_hi, kind;
   int w0, nw;  // SEG_FINISH: the groups w0, ..., w0 + nw - 1 hold the tile's later parts
+  bool last;   // SEG_FINISH: no tile of this CTA group follows (its pipeline stages are then idle)
 };
 template <bool SPLIT>  // false: a kernel built without the split (round robin only)
 struct SegIter {
@@ -548,6 +549,7 @@ struct SegIter {
         o.kind = SEG_FINISH;
         o.w0 = fin_w0;
         o.nw = fin_nw;
+        o.last = !first || nfull == 0;
         return true;
       }
     }
@@ -556,6 +558,7 @@ struct SegIter {
   __device__ bool next(Seg& o) {
     if constexpr (SPLIT) {
       o.w0 = o.nw = 0;
+      o.last = false;
       if (first && tail_next(o)) return true;
     }
     if (s < nfull) {
@@ -898,6 +901,7 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
   using PP = Pipe<CG>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;  // tensor-memory lanes this warp may read: [32*quad, 32*quad+32)
+  const uint32_t sbase_smem = smem_u32(smem);
   const uint32_t ebase = smem_u32(smem + SMEM_EPI + (warp - 2) * 2 * EPI_BUF_BYTES);
   const float scale = p.fp8 ? (__ldg(p.scale_x) * __ldg(p.scale_w)) : 1.0f;
   const int row_off = BM * static_cast<int>(rank);
@@ -913,19 +917,29 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
   uint64_t ws_pol = 0;
   if (rmode || SPLIT) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(ws_pol));
   // Split tiles (AG tail split): a CTA's partial of a later part of a tile sits
-  // in its own workspace block in the same layout, unscaled fp32.
+  // in its own workspace block, unscaled fp32, laid out warp by warp: each
+  // epilogue warp's 32 rows are one contiguous 32 KiB run of [32-column chunk]
+  // [16-byte group][row] (512 coalesced bytes per chunk and group).
   const int cta = g * CG + static_cast<int>(rank);  // workspace block and partial flags of this CTA
-  const uint4* const part_lane = reinterpret_cast<const uint4*>(p.ws) + quad * 32 + lane;
-  uint32_t ul = 0, nst = 0;
+  auto part_at = [&](int blk, int c, int v) -> uint4* {
+    return reinterpret_cast<uint4*>(p.ws) + static_cast<size_t>(blk) * (BM * BN / 4) + quad * (32 * BN / 4) +
+           (c * 8 + v) * 32 + lane;
+  };
+  uint32_t ul = 0, nst = 0, pphase = 0;
   unsigned long long cyc_tfull = 0;
   bool ok_all = true;
   // A part of a split tile, on its own path so that whole tiles run the same
   // code as in the build without the split.  A later part (SEG_WRITE) goes to
   // this CTA's workspace block as unscaled fp32 and is published per warp; the
   // first part (SEG_FINISH) waits for the later parts' flags, adds them in K
-  // order and stores the tile like a whole one.
+  // order and stores the tile like a whole one.  When the finished tile is
+  // the CTA group's last (its MMAs and loads are over, so the pipeline stages
+  // are idle), each warp first copies its rows of the later parts into its
+  // quarter of the stage area with bulk copies, a few round trips in all;
+  // otherwise it reads them from global memory one chunk ahead.
   auto split_part = [&](const Tile& T, const Seg& sg, uint32_t ul_) -> bool {
     const bool write = sg.kind == SEG_WRITE;
+    const int nch = T.ncols / EPI_COLS;
     if (!write)
       for (int j = 0; j < sg.nw; ++j)
         if (!wait_partial(p, &p.words->part_ready[((sg.w0 + j) * CG + static_cast<int>(rank)) * EPI_WARPS + quad]))
@@ -937,31 +951,84 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
     mbar_wait(p, bar, par, SITE_TMEM_FULL, false);
     tc_fence_after();
     const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + acc * BN;
-    // the first later part's partial is fetched one chunk ahead of its use
+    auto add_part = [&](uint32_t(&r)[32], const uint32_t(&h)[32]) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(h[e]));
+    };
+    // staged path: this warp's quarter of the stage area holds `span` chunks of every later part
+    constexpr int kWarpArea = STAGE_AREA / EPI_WARPS;   // 48 KiB
+    constexpr int kChunkBytes = 32 * EPI_COLS * 4;      // one warp's 32 rows x 32 columns, fp32
+    const bool staged = !write && sg.nw > 0 && sg.last && sg.nw * kChunkBytes <= kWarpArea;
+    const int span = staged ? kWarpArea / (sg.nw * kChunkBytes) : 0;
+    const uint32_t pbuf = sbase_smem + SMEM_STAGES + static_cast<uint32_t>((warp - 2) * kWarpArea);
+    const uint32_t pbar = sbase_smem + SMEM_BARS + 8u * static_cast<uint32_t>(BAR_PART + (warp - 2));
+    int c_lo = 0, c_hi = 0;  // chunks now in shared memory
+    auto stage = [&](int c0) -> bool {  // bulk-copy chunks [c0, c0 + span) of every later part
+      const int cnt = min(span, nch - c0);
+      __syncwarp();  // every lane is done reading the previous range
+      if (lane == 0) {
+        if (c0 == 0)
+          fence_proxy_async_global();  // the acquired partials, read through the async proxy
+        else
+          fence_proxy_async_smem();    // the previous range's reads come before its overwrite
+        mbar_expect_tx(pbar, static_cast<uint32_t>(sg.nw * cnt * kChunkBytes));
+        for (int j = 0; j < sg.nw; ++j)
+          bulk_load(pbuf + static_cast<uint32_t>(j * span * kChunkBytes),
+                    reinterpret_cast<const uint8_t*>(p.ws) +
+                        (static_cast<size_t>((sg.w0 + j) * CG + static_cast<int>(rank)) * (BM * BN) +
+                         static_cast<size_t>(quad) * (32 * BN) + static_cast<size_t>(c0) * (32 * EPI_COLS)) * 4,
+                    static_cast<uint32_t>(cnt * kChunkBytes), pbar);
+      }
+      int okb = (lane == 0) ? (mbar_wait(p, pbar, pphase, SITE_PARTIAL, true) ? 1 : 0) : 0;
+      if (!__shfl_sync(0xffffffffu, okb, 0)) {
+        if (lane == 0) mbar_wait(p, pbar, pphase, SITE_DRAIN, false);  // copies in flight land first
+        return false;
+      }
+      mbar_wait(p, pbar, pphase, SITE_PARTIAL, false);  // every lane observes the completed phase
+      pphase ^= 1u;
+      c_lo = c0;
+      c_hi = c0 + cnt;
+      return true;
+    };
     auto load_part = [&](int j, int c, uint32_t(&h)[32]) {
-      const uint4* w4 =
-          part_lane + static_cast<size_t>((sg.w0 + j) * CG + static_cast<int>(rank)) * (BM * BN / 4) + c * 8 * BM;
+      if (staged) {
+        const uint32_t a = pbuf + static_cast<uint32_t>((j * span + (c - c_lo)) * kChunkBytes) + lane * 16u;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          uint32_t x0, x1, x2, x3;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3) : "r"(a + v * 512u) : "memory");
+          h[4 * v] = x0;
+          h[4 * v + 1] = x1;
+          h[4 * v + 2] = x2;
+          h[4 * v + 3] = x3;
+        }
+        return;
+      }
+      const int blk = (sg.w0 + j) * CG + static_cast<int>(rank);
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
         uint32_t x[4];
-        ld_global_v4_keep(w4 + v * BM, x, ws_pol);
+        ld_global_v4_keep(part_at(blk, c, v), x, ws_pol);
         h[4 * v] = x[0];
         h[4 * v + 1] = x[1];
         h[4 * v + 2] = x[2];
         h[4 * v + 3] = x[3];
       }
     };
-    auto add_part = [&](uint32_t(&r)[32], const uint32_t(&h)[32]) {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(h[e]));
-    };
     uint32_t pa[32];
-    const int nch = T.ncols / EPI_COLS;
-    if (!write && sg.nw > 0) load_part(0, 0, pa);
+    if (!write && sg.nw > 0 && !staged) load_part(0, 0, pa);
 #pragma unroll 1
     for (int c = 0; c < nch; ++c) {
       uint32_t pn[32];
-      if (!write && sg.nw > 0 && c + 1 < nch) load_part(0, c + 1, pn);
+      if (!write && sg.nw > 0) {
+        if (staged) {  // the chunk's later parts from shared memory, a new range when needed
+          if (c >= c_hi && !stage(c)) return false;
+          load_part(0, c, pa);
+        } else if (c + 1 < nch) {  // from global memory, one chunk ahead
+          load_part(0, c + 1, pn);
+        }
+      }
       uint32_t r[32];
       tmem_ld32_sync(taddr + c * EPI_COLS, r);
       if (c == nch - 1) {  // accumulator fully read: hand it back to the MMA issuer
@@ -975,9 +1042,9 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
         }
       }
       if (write) {
-        uint4* w4 = const_cast<uint4*>(part_lane) + static_cast<size_t>(cta) * (BM * BN / 4) + c * 8 * BM;
 #pragma unroll
-        for (int v = 0; v < 8; ++v) st_global_v4_keep(w4 + v * BM, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3], ws_pol);
+        for (int v = 0; v < 8; ++v)
+          st_global_v4_keep(part_at(cta, c, v), r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3], ws_pol);
         continue;
       }
       if (sg.nw > 0) add_part(r, pa);  // the later parts in K order
@@ -986,8 +1053,10 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
         load_part(j, c, h);
         add_part(r, h);
       }
+      if (!staged) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) pa[e] = pn[e];
+        for (int e = 0; e < 32; ++e) pa[e] = pn[e];
+      }
       const int ox = T.col + c * EPI_COLS, oy = T.y_row + row_off + quad * 32;
       if (ox >= p.m || oy >= p.y_rows) continue;  // wholly past the output's edge: no buffer, no store
       uint32_t packed[16];
@@ -1223,6 +1292,8 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
       mbar_init(B.tempty0 + 8u * a, CG * EPI_WARPS);  // one arrival per epilogue warp of the group
     }
     mbar_init(B.drain, 1);
+    if constexpr (SPLIT)
+      for (int w = 0; w < EPI_WARPS; ++w) mbar_init(B.full0 + 8u * (BAR_PART - BAR_FULL + w), 1);
     fence_barrier_init();
   }
   __syncwarp();

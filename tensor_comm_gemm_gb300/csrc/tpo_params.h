@@ -55,10 +55,10 @@ constexpr int SMEM_STAGES = 0;
 constexpr int SMEM_EPI = SMEM_STAGES + STAGE_AREA;                      // 196608
 constexpr int SMEM_BARS = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;     // 212992
 // barriers: full[MAX_STAGES], empty[MAX_STAGES], tmem_full[2], tmem_empty[2],
-// drain, copy[COPY_BUFS]
+// drain, copy[COPY_BUFS], part[EPI_WARPS] (split-tile finishers' bulk copies)
 constexpr int BAR_FULL = 0, BAR_EMPTY = MAX_STAGES, BAR_TFULL = 2 * MAX_STAGES, BAR_TEMPTY = BAR_TFULL + 2,
-              BAR_DRAIN = BAR_TEMPTY + 2, BAR_COPY = BAR_DRAIN + 1;
-constexpr int NUM_BARS = BAR_COPY + COPY_BUFS;
+              BAR_DRAIN = BAR_TEMPTY + 2, BAR_COPY = BAR_DRAIN + 1, BAR_PART = BAR_COPY + COPY_BUFS;
+constexpr int NUM_BARS = BAR_PART + EPI_WARPS;
 constexpr int SMEM_TMEM_SLOT = SMEM_BARS + NUM_BARS * 8;
 constexpr int SMEM_TAIL = SMEM_TMEM_SLOT + 16;   // split builds: the CTA group's schedule (64 bytes)
 constexpr int SMEM_USED = SMEM_TAIL + 64;
