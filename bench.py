@@ -427,6 +427,7 @@ def gpu_arm(args, rank, world, local_rank, dist):
                    "producer_ctas": t.tpo_get_opt(ctx, "last_producer_ctas"), "gemm_ctas": t.tpo_get_opt(ctx, "last_gemm_ctas"), "cta_group": t.tpo_get_opt(ctx, "last_cta_group"),
                    "stage_kblocks": t.tpo_get_opt(ctx, "last_stage_kblocks"),
                    "cooperative_launch": bool(t.tpo_get_opt(ctx, "cooperative") and t.tpo_get_opt(ctx, "coop_clusters")),
+                   "programmatic_dependent_launch": bool(t.tpo_get_opt(ctx, "pdl")),
                    "l2": "inputs larger than L2: %d rotating sets of X_r, W, Y (%d MiB), steps back to back" % (
                        ROTATE, ROTATE * 96),
                    "parallelism": "replicas only (simulated ranks in one GPU's memory)"},

@@ -232,11 +232,21 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *   "cta_group"        MMA variant: 0 automatic, 1 single-SM 128x256 tiles,
  *                      2 CTA pairs (2-SM MMA, 256x256 tiles; needs every tile
  *                      group a multiple of 256 rows).  Results are identical.
- *   "cooperative"      1 (default): overlapped AG is a cooperative launch, so
- *                      the driver guarantees producer and GEMM CTAs co-resident;
- *                      0: plain launch (the grid never exceeds the co-resident
- *                      CTA count either way), e.g. for profilers that reject
- *                      cooperative launches of CTA clusters
+ *   "cooperative"      0 (default): overlapped AG is a plain launch whose grid
+ *                      never exceeds the co-resident CTA count, so once no
+ *                      other work holds SMs every producer and GEMM CTA runs at
+ *                      once (if other work does, a GEMM CTA's wait for a chunk
+ *                      is bounded: TPO_ERR_TIMEOUT, never a hang); 1: a
+ *                      cooperative launch, whose co-residency the driver
+ *                      guarantees, but which cannot start before the launch
+ *                      ahead of it has ended (no "pdl" overlap)
+ *   "pdl"              1 (default): every kernel launch is marked for
+ *                      programmatic dependent launch: its CTAs may start their
+ *                      set-up (barriers, tensor memory) on SMs the previous
+ *                      launch on the stream has left and wait (griddepcontrol)
+ *                      for that launch's completion before touching global
+ *                      memory.  Measured on back-to-back 4096^3 AG calls:
+ *                      2.8-3.6 % faster.  0: ordinary stream order.
  *   "reduce"           GEMM+RS / GEMM+AR sum of the ranks' partial products:
  *                      0 (default) chain every rank's K-slice, in ring order,
  *                      into one fp32 accumulator; 1 compute each rank's partial

@@ -97,8 +97,8 @@ struct tpo_ctx {
   // options
   int64_t producer_sms = 0, gemm_ctas = 0, mode = 0, seq_copy_ctas = 0, self_rank = 0, wait_timeout_ms = 2000,
           trace = 0, debug_skip_chunk = -1, debug_delay_ns = 0, debug_last_step = -1, cta_group = 0,
-          cooperative = 1, reduce = 0, tail_split = 0, debug_skip_partial = -1, stage_kblocks = 1,
-          col_split = 0;
+          cooperative = 0, reduce = 0, tail_split = 0, debug_skip_partial = -1, stage_kblocks = 1,
+          col_split = 0, pdl = 1;
   // device memory
   uint8_t* staging = nullptr;
   size_t staging_bytes = 0;
@@ -165,6 +165,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
       {"debug_skip_partial", &tpo_ctx::debug_skip_partial, -1, tpo::MAX_GEMM_CTAS - 1},
       {"stage_kblocks", &tpo_ctx::stage_kblocks, 1, 2},
       {"col_split", &tpo_ctx::col_split, 0, INT64_MAX},
+      {"pdl", &tpo_ctx::pdl, 0, 1},
   };
   for (const E& e : table)
     if (std::strcmp(e.k, key) == 0) {
@@ -182,7 +183,7 @@ const char* kOptKeys[] = {"producer_sms",     "gemm_ctas",      "mode",         
                           "self_rank",        "wait_timeout_ms", "trace",          "debug_skip_chunk",
                           "debug_delay_ns",   "debug_last_step", "cta_group",      "cooperative",
                           "reduce",           "tail_split",     "debug_skip_partial", "stage_kblocks",
-                          "col_split"};
+                          "col_split",        "pdl"};
 
 void destroy_all(tpo_ctx* c) {
   if (!c) return;
@@ -215,6 +216,7 @@ void base_params(const tpo_ctx* c, Params& p) {
   p.self_rank = static_cast<int>(c->self_rank);
   p.tp = c->tp;
   p.fp8 = c->dtype == TPO_FP8_E4M3;
+  p.pdl = static_cast<int>(c->pdl);
 }
 
 tpo_status reset_trace(tpo_ctx* c, cudaStream_t s) {

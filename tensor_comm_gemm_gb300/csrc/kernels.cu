@@ -66,6 +66,16 @@ __device__ void raise_error(const Params& p, uint32_t code, uint32_t site, uint3
   }
 }
 
+// ------------------------------------------------------------------ launch order
+
+// Programmatic dependent launch: a launch that the host marks may begin its
+// set-up (barriers, tensor memory) while the launch before it on the stream is
+// still running; griddepcontrol.wait then holds the thread until that launch
+// has completed and its memory is visible, so nothing before it touches global
+// memory.  Without the mark both instructions return at once.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -623,6 +633,8 @@ __device__ void producer_role(const Params& p, uint8_t* smem) {
   const uint32_t bars = sbase + SMEM_BARS + 8u * BAR_COPY;
   for (int b = 0; b < COPY_BUFS; ++b) mbar_init(bars + 8u * b, 1);
   fence_barrier_init();
+  grid_dep_wait();  // the sources may come from the launch before
+  if (p.trace_on) atomicMin(&p.words->trace[TPO_TRACE_START], gtime());
 
   const long long pieces = (p.chunk_bytes + COPY_PIECE - 1) / COPY_PIECE;
   const long long P = p.num_producers, pid = blockIdx.x;
@@ -1302,14 +1314,17 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
     tmem_alloc_cg<CG>(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish_cg<CG>();
   }
-  if constexpr (SPLIT) {  // the group's schedule (host-built), fetched while the tensor memory is allocated
-    if (warp == 2 && lane < 16 && p.tail_split)
-      reinterpret_cast<int*>(tail)[lane] = __ldg(reinterpret_cast<const int*>(p.tail_tab + g) + lane);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  grid_dep_wait();  // set-up done: from here on global memory may depend on the launch before
+  if (p.trace_on && threadIdx.x == 0) atomicMin(&p.words->trace[TPO_TRACE_START], gtime());
+  if constexpr (SPLIT) {  // the group's schedule (host-built)
+    if (warp == 2 && lane < 16 && p.tail_split)
+      reinterpret_cast<int*>(tail)[lane] = __ldg(reinterpret_cast<const int*>(p.tail_tab + g) + lane);
+    __syncthreads();
+  }
 
   if (warp == 0) {
     if (lane == 0) tma_role<CG, SPLIT>(p, sbase, B, rank, g, G, total_tiles, nkb, tail);
@@ -1338,7 +1353,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_kernel(const __grid_cons
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  if (p.trace_on && threadIdx.x == 0) atomicMin(&p.words->trace[TPO_TRACE_START], gtime());
+  grid_dep_launch();  // the next launch may set up on SMs this one leaves
   if (static_cast<int>(blockIdx.x) < p.num_producers) {
     if (p.copy_on) producer_role(p, smem);
     if constexpr (SPLIT) {
@@ -1391,8 +1406,13 @@ cudaError_t launch_fused(const Params& p, int grid, bool cooperative, cudaStream
   cfg.blockDim = dim3(NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_ALLOC;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   int na = 0;
+  if (p.pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   if (cooperative) {
     attr[na].id = cudaLaunchAttributeCooperative;
     attr[na].val.cooperative = 1;

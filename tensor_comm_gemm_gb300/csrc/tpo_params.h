@@ -168,6 +168,7 @@ struct Params {
   int late_groups;        // producer CTA groups that join the GEMM after their copy
   int copy_on;            // producer CTAs copy (0: they only run as late GEMM groups)
   int skip_part;          // test hook: this GEMM CTA never publishes its partial (-1: none)
+  int pdl;                // host side: launch with programmatic dependent launch (set-up overlaps the launch before)
 };
 
 // Column tiling of a launch with p.num_groups groups of p.row_tiles row tiles

@@ -363,3 +363,36 @@ def test_two_contexts_on_two_streams():
     finally:
         ag.close()
         rs.close()
+
+
+def test_chained_calls_respect_the_launch_before():
+    """Back-to-back launches on one stream (with and without programmatic
+    dependent launch): the second AG call gathers the first call's output rows, with a
+    torch kernel between them, and no synchronisation until the end; its
+    result must be the oracle's on the first result."""
+    tp, n, k, m = 2, 512, 256, 256
+    wl1 = synth.make_ag(tp, n, k, m, seed=71, dist="normal", sigma=k ** -0.25)
+    r1 = AgRun(wl1)
+    w2_host = synth.make_ag(tp, n, m, m, seed=72, dist="normal", sigma=m ** -0.25).w[0]
+    w2 = torch.from_numpy(w2_host.view(np.int16)).view(torch.bfloat16).cuda()
+    y2 = torch.empty((n, m), dtype=torch.bfloat16, device="cuda")
+    ctx2 = t.tpo_ctx_create(tp, n, m, m, t.TPO_BF16)
+    try:
+      for pdl in (1, 0):
+        t.tpo_set_opt(r1.ctx, "pdl", pdl)
+        t.tpo_set_opt(ctx2, "pdl", pdl)
+        for rep in range(3):
+            r1.y.fill_(float("nan"))
+            y2.fill_(float("nan"))
+            torch.cuda.synchronize()
+            r1.run(sync=False)
+            y1 = r1.y * 1.0                        # a torch kernel in between
+            t.tpo_ag_gemm(ctx2, [y1[: n // tp], y1[n // tp:]], w2, y2)
+            assert t.tpo_sync_status(ctx2) == 0 and t.tpo_sync_status(r1.ctx) == 0
+            y1_bits = host_bits(y1)
+            assert_close(host_f64(y1), ref_ag(wl1))
+            ref2 = oracle.ag(oracle.gather([y1_bits[: n // tp], y1_bits[n // tp:]]), w2_host)
+            assert_close(host_f64(y2), ref2)
+    finally:
+        t.tpo_ctx_destroy(ctx2)
+        r1.close()
