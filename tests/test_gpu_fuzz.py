@@ -3,7 +3,7 @@
 Every case draws an operation (AG, RS, AR), a dtype, sizes that are ragged in
 rows, columns and K where the ABI allows it, and launch options (observer
 rank, schedule mode, CTA-pair or single-SM tiles, GEMM grid, producer count,
-tail split, epilogue-reduction mode, row chunks, column plan).  Outputs sit between
+tail split, epilogue-reduction mode, row chunks, column plan, launch kind).  Outputs sit between
 sentinel guards; every launch of a case is compared with the oracle, and a
 second launch of the same case must give the same bits.
 """
@@ -53,7 +53,8 @@ def draw(seed):
     tp = int(rng.choice([1, 2, 3, 4, 5, 8]))
     m = int(8 * rng.integers(1, 81))                      # up to 640 columns, 16-byte rows
     opts = {"gemm_ctas": int(rng.choice([0, 0, 2, 3, 5, 8])), "cta_group": int(rng.choice([0, 0, 1])),
-            "col_split": int(rng.choice([0, 0, 0, int(rng.integers(1, 1 << 16))]))}
+            "col_split": int(rng.choice([0, 0, 0, int(rng.integers(1, 1 << 16))])),
+            "pdl": int(rng.choice([1, 1, 0])), "cooperative": int(rng.choice([0, 0, 1]))}
     if op == "ag":
         rows = int(rng.choice([int(rng.integers(1, 300)), 256, 512]))
         n, k = tp * rows, int(kq * rng.integers(1, 48))
