@@ -752,7 +752,7 @@ def noalloc_row(t, torch, dev, to_dev, peak, calls=50):
     tf = synth.flops(HEADLINE) / (ms * 1e-3) / 1e12
     return {"workload": describe(HEADLINE), "ms_per_call_median": round(ms, 4), "tflops": round(tf, 2),
             "frac_of_peak": round(tf / peak, 4), "peak_kind": "burst",
-            "note": "tpo_ag_gemm_noalloc: 8 producer CTAs, single-SM 128x256 tiles, blocking call (host wall "
+            "note": "tpo_ag_gemm_noalloc: default launch shape (CTA pairs, modelled producer count), blocking call (host wall "
                     "time per call, median of %d, includes the launch and the read-back of the error word)" % calls}
 
 

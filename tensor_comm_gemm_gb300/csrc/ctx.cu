@@ -377,6 +377,30 @@ int64_t packed_columns(const Params& p) {
   return v;
 }
 
+// The fewest producer CTAs (even for CTA pairs; up to 32) whose modelled end
+// is within 0.5 % of the best, for an overlapped AG launch whose tiles (and
+// column tiles) p describes: grid_of(P) gives the GEMM's CTA groups next to P
+// producer CTAs; a producer CTA moves up to 37 GB/s of chunk data beside a
+// running GEMM and all of them together up to 705 GB/s, both taken 1.25
+// times slower for margin; ring step g's chunk is ready at g tau and the
+// launch lasts until the GEMM's end and the copy of all tp chunks.
+template <class GridOf>
+int best_producers(const Params& p, int cg, int tp, int num_sms, int nkb, int64_t chunk_bytes, GridOf grid_of) {
+  double ends[33] = {};
+  double best_end = 0;
+  double ready[TPO_MAX_TP];
+  for (int P = cg; P <= 32 && P <= num_sms - 2 * cg; P += cg) {
+    const double rate = std::min(37e9, 705e9 / P) / 1.25;
+    const double tau_us = static_cast<double>(chunk_bytes) / (P * rate) * 1e6;
+    for (int g = 0; g < tp; ++g) ready[g] = g * tau_us;
+    ends[P] = std::max(tp * tau_us, tiles_end(p, cg, grid_of(P), ready, nkb));
+    if (best_end == 0 || ends[P] < best_end) best_end = ends[P];
+  }
+  for (int P = cg; P <= 32 && P <= num_sms - 2 * cg; P += cg)
+    if (ends[P] <= best_end * 1.005) return P;
+  return 8;
+}
+
 // Producer CTAs of an overlapped AG call, and the column tiles of its GEMM
 // (set in p).  An explicit producer_sms option wins.  `split` is the tail-split
 // schedule (0 none): its launches keep the fewest column tiles.
@@ -402,20 +426,12 @@ int producer_count(tpo_ctx* c, Params& p, int cg, int tiles, int nkb, int split)
   auto grid_of = [&](int P) {
     return gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, P, tiles) / cg;
   };
-  auto ready_of = [&](int P, double* ready) {
-    const double rate = std::min(37e9, 705e9 / P) / 1.25;
-    const double tau_us = static_cast<double>(chunk_bytes) / (P * rate) * 1e6;
-    for (int g = 0; g < c->tp; ++g) ready[g] = g * tau_us;
-    return c->tp * tau_us;
-  };
-  // the model's end for P producers over the launch's column tiles (the
-  // tail split keeps the fewest)
-  auto model_end = [&](int P, const double* ready) {
+  // the launch's column tiles (the tail split keeps the fewest)
+  auto set_cols = [&]() {
     if (split)
       tpo::set_columns(p, c->m, nullptr);
     else
       plan_columns(c, p);
-    return tiles_end(p, cg, grid_of(P), ready, nkb);
   };
   if (split == 1 && c->producer_sms <= 0) {
     tpo::set_columns(p, c->m, nullptr);
@@ -441,34 +457,11 @@ int producer_count(tpo_ctx* c, Params& p, int cg, int tiles, int nkb, int split)
     }
   }
   const int64_t key[9] = {cg, c->gemm_ctas, c->producer_sms, c->col_split, tiles, nkb, chunk_bytes, c->m, split};
-  if (std::memcmp(key, c->pc_key, sizeof(key)) == 0) {
-    if (split)
-      tpo::set_columns(p, c->m, nullptr);
-    else
-      plan_columns(c, p);
-    return c->pc_val;
-  }
-  int best = 0;
-  double ready[TPO_MAX_TP];
-  if (c->producer_sms > 0) {
-    best = static_cast<int>(c->producer_sms) + ((cg == 2) ? static_cast<int>(c->producer_sms & 1) : 0);
-  } else {
-    double ends[33] = {};
-    double best_end = 0;
-    for (int P = cg; P <= 32 && P <= c->num_sms - 2 * cg; P += cg) {
-      const double copy_end = ready_of(P, ready);
-      ends[P] = std::max(copy_end, model_end(P, ready));
-      if (best_end == 0 || ends[P] < best_end) best_end = ends[P];
-    }
-    best = 8;
-    for (int P = cg; P <= 32 && P <= c->num_sms - 2 * cg; P += cg)
-      if (ends[P] <= best_end * 1.005) {
-        best = P;
-        break;
-      }
-  }
-  ready_of(best, ready);
-  model_end(best, ready);
+  set_cols();
+  if (std::memcmp(key, c->pc_key, sizeof(key)) == 0) return c->pc_val;
+  const int best = (c->producer_sms > 0)
+                       ? static_cast<int>(c->producer_sms) + ((cg == 2) ? static_cast<int>(c->producer_sms & 1) : 0)
+                       : best_producers(p, cg, c->tp, c->num_sms, nkb, chunk_bytes, grid_of);
   std::memcpy(c->pc_key, key, sizeof(key));
   c->pc_val = best;
   return best;
@@ -613,6 +606,15 @@ tpo_status check_ksplit(tpo_ctx* c, const void* const* x, const void* const* w) 
 
 namespace tpo {
 void set_last_error(const char* msg) { g_err = msg; }
+
+int model_producers(const Params& p, int cg, int tp, int num_sms, int max_pairs) {
+  const int tiles = p.total_tiles;
+  auto grid_of = [&](int P) {
+    if (cg == 1) return std::max(1, std::min(num_sms - P, tiles));
+    return std::max(1, std::min(std::min((num_sms - P) / 2, max_pairs - P / 2), tiles));
+  };
+  return best_producers(p, cg, tp, num_sms, p.kb_per_seg, p.chunk_bytes, grid_of);
+}
 }  // namespace tpo
 
 extern "C" {

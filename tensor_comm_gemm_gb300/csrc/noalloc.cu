@@ -20,6 +20,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -35,13 +36,15 @@ static_assert(kWordsBytes == TPO_NOALLOC_WORDS_BYTES, "the header states the siz
 static __device__ __align__(256) uint8_t g_noalloc_scratch[TPO_NOALLOC_MAX_STAGING_BYTES + kWordsBytes];
 
 constexpr int kMaxDevices = 64;
-constexpr int kProducers = 8;  // same producer share as a context's default
 
 struct DeviceSetup {
   bool done = false;
   uint8_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
   int num_sms = 0;
   int max_coop_grid = 0;
+  int max_pairs = 0;           // co-resident CTA pairs of the 2-SM variant (0: single-SM tiles only)
+  long long shape[5] = {-1, -1, -1, -1, -1};  // the latest call's (tp, n, k, m, dtype)
+  int producers = 0;           // and its producer CTA count from the schedule model
 };
 
 std::mutex g_mu;
@@ -88,9 +91,15 @@ tpo_status setup_device(int dev, DeviceSetup** out) {
         return fail(TPO_ERR_CUDA, "driver entry point cuTensorMapEncodeTiled unavailable");
       g_encode_fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
+    int pairs = 0;
+    if (tpo::max_active_pairs(&pairs) != cudaSuccess) {
+      cudaGetLastError();
+      pairs = 0;  // pairs cannot be placed: single-SM tiles serve every call
+    }
     s.scratch = static_cast<uint8_t*>(ptr);
     s.num_sms = sms;
     s.max_coop_grid = per_sm * sms;
+    s.max_pairs = pairs;
     s.done = true;
   }
   *out = &s;
@@ -164,15 +173,17 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
   tpo::DevWords* words = reinterpret_cast<tpo::DevWords*>(s->scratch + TPO_NOALLOC_MAX_STAGING_BYTES);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
-  // ---- launch parameters: overlapped schedule, observer rank 0
+  // ---- launch parameters: overlapped schedule, observer rank 0; CTA pairs
+  // (2-SM MMA) wherever every 256-row tile lies in one slot, as tpo_ag_gemm
   tpo::Params p;
   tpo::init_params(p);
   const int64_t rows = n / tp;
+  const int cg = (rows % (2 * tpo::BM) == 0 && s->max_pairs >= 1) ? 2 : 1;
   const int kel = tpo::BK_BYTES / elem;
   const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!(encode3(&p.mapA[0], staging, dt, elem, k, rows, tp, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
         encode3(&p.mapA[1], x[0], dt, elem, k, rows, 1, kel, tpo::BM, CU_TENSOR_MAP_SWIZZLE_128B) &&
-        encode(&p.mapB[0], w, dt, elem, k, m, kel, tpo::BN, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        encode(&p.mapB[0], w, dt, elem, k, m, kel, tpo::BN / cg, CU_TENSOR_MAP_SWIZZLE_128B) &&
         encode3(&p.mapY[0], y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, m, rows, tp, tpo::EPI_COLS, 32,
                 CU_TENSOR_MAP_SWIZZLE_64B)))
     return fail(TPO_ERR_INVALID_ARG, "tensor map encoding failed (pointer or size not TMA-compatible)");
@@ -187,8 +198,9 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
   p.fp8 = fp8 ? 1 : 0;
   p.tp = tp;
   p.self_rank = 0;
+  p.cta_group = cg;
   p.rows_per_group = static_cast<int>(rows);
-  p.row_tiles = static_cast<int>((rows + tpo::BM - 1) / tpo::BM);
+  p.row_tiles = static_cast<int>((rows + tpo::BM * cg - 1) / (tpo::BM * cg));
   p.m = static_cast<int>(m);
   p.y_rows = static_cast<int>(rows);
   p.num_groups = tp;
@@ -196,11 +208,17 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
   p.num_segs = 1;
   p.gate = 1;
   tpo::set_columns(p, m, nullptr);  // every group: the fewest column tiles of at most 256 columns
-  const int P = kProducers < s->num_sms - 1 ? kProducers : s->num_sms - 1;
+  // producer CTAs from the library's schedule model (kept for the latest shape on this device)
+  const long long shape[5] = {tp, n, k, m, dtype};
+  if (std::memcmp(shape, s->shape, sizeof(shape)) != 0) {
+    s->producers = tpo::model_producers(p, cg, tp, s->num_sms, s->max_pairs);
+    std::memcpy(s->shape, shape, sizeof(shape));
+  }
+  const int P = s->producers;
   const int tiles = p.total_tiles;
-  int G = s->num_sms - P;
-  if (G > tiles) G = tiles;
-  if (P < 1 || G < 1 || P + G > s->max_coop_grid) return fail(TPO_ERR_UNSUPPORTED, "device too small");
+  int G = (cg == 1) ? std::min(s->num_sms - P, tiles)
+                    : 2 * std::min(std::min((s->num_sms - P) / 2, s->max_pairs - P / 2), tiles);
+  if (P < 1 || G < cg || P + G > s->max_coop_grid) return fail(TPO_ERR_UNSUPPORTED, "device too small");
   for (int r = 0; r < TPO_MAX_TP; ++r) p.target[r] = static_cast<uint32_t>(P);  // counters start at zero
   p.num_producers = P;
   p.num_gemm = G;
@@ -209,7 +227,8 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
   // word must start at zero (the staging buffer is fully rewritten).
   e = cudaMemsetAsync(words, 0, offsetof(tpo::DevWords, pad), cs);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the counters");
-  e = tpo::launch_fused(p, P + G, true, cs);
+  // a plain launch: the grid never exceeds the co-resident CTA count
+  e = tpo::launch_fused(p, P + G, false, cs);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
 
   // Wait for the call and read its error word (16 bytes into host memory).
