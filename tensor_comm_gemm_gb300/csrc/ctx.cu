@@ -17,6 +17,7 @@
 #include <string>
 #include <vector>
 
+#include "schedule.h"
 #include "tpo_params.h"
 #include "tpoverlap.h"
 

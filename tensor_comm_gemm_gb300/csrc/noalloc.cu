@@ -24,6 +24,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "schedule.h"
 #include "tpo_params.h"
 #include "tpoverlap.h"
 

@@ -256,10 +256,4 @@ cudaError_t launch_fused(const Params& p, int grid, bool cooperative, cudaStream
 // Sets the thread-local message returned by tpo_last_error (ctx.cu).
 void set_last_error(const char* msg);
 
-// The host schedule model's producer CTA count for an overlapped AG launch
-// with default options, whose tiles (uniform column tiles), K blocks and chunk
-// size p describes, on num_sms SMs with max_pairs co-resident CTA pairs
-// (ctx.cu; the entry point without a context uses it).
-int model_producers(const Params& p, int cg, int tp, int num_sms, int max_pairs);
-
 }  // namespace tpo
