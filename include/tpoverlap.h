@@ -220,15 +220,21 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      even number of K blocks).  Results are identical; one
  *                      block per stage measured 1.4-2.6 % faster on 4096^3.
  *   "col_split"        column tiles per tile group (AG ring step, RS owner
- *                      block, AR row chunk): 0 (default) the fewest tiles of
- *                      at most 256 columns, the group's 32-column strips
- *                      split evenly among them; otherwise 4 bits per group g
- *                      < 16 ((v >> 4g) & 15) of extra tiles, splitting the
- *                      strips into narrower tiles (down to 32 columns).
- *                      Results are identical (the MMA computes every output
- *                      element the same way whatever the tile width); a K
- *                      block of a 128- to 256-column tile costs about the
- *                      same time, so narrower tiles do not pay.
+ *                      block, AR row chunk), the group's 32-column strips
+ *                      split evenly among them: -1 the fewest tiles of at
+ *                      most 256 columns; 0 (default) automatic: the fewest,
+ *                      unless the launch has at most half as many tiles as
+ *                      it can have GEMM CTA groups (the SMs, less 32 for the
+ *                      AG producers, per MMA variant), then as many narrower
+ *                      tiles per group (down to 32 columns) as still fit in
+ *                      one round; otherwise 4 bits per group g < 16
+ *                      ((v >> 4g) & 15) of extra tiles.  The GEMM grid
+ *                      follows the plan's tile count.  Results are identical
+ *                      (the MMA computes every output element the same way
+ *                      whatever the tile width).  A K block costs about the
+ *                      same at any width from 128 to 256 columns, so more
+ *                      tiles pay only where they all fit in one round: each
+ *                      tile's epilogue is then shorter.
  *   "cta_group"        MMA variant: 0 automatic, 1 single-SM 128x256 tiles,
  *                      2 CTA pairs (2-SM MMA, 256x256 tiles; needs every tile
  *                      group a multiple of 256 rows).  Results are identical.
@@ -265,7 +271,8 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  * "last_late_groups", "last_col_plan" (shape of the context's latest kernel
  * launch: producer CTAs, GEMM CTAs, 1 or 2 CTAs per MMA, K blocks per
  * pipeline stage, tiles split along K, producer CTA groups that joined the
- * GEMM, extra column tiles per group in the col_split encoding),
+ * GEMM, extra column tiles per group in the col_split encoding, each
+ * group's count capped at 15 in the report),
  * "coop_clusters" (0 once the driver refused a cooperative cluster launch),
  * "tp", "n", "k", "m", "dtype" (the sizes the context was created for).
  * Environment variables TPO_<KEY in upper case> override the defaults at

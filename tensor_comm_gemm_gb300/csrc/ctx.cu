@@ -165,7 +165,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
       {"tail_split", &tpo_ctx::tail_split, 0, 3},
       {"debug_skip_partial", &tpo_ctx::debug_skip_partial, -1, tpo::MAX_GEMM_CTAS - 1},
       {"stage_kblocks", &tpo_ctx::stage_kblocks, 1, 2},
-      {"col_split", &tpo_ctx::col_split, 0, INT64_MAX},
+      {"col_split", &tpo_ctx::col_split, -1, INT64_MAX},
       {"pdl", &tpo_ctx::pdl, 0, 1},
   };
   for (const E& e : table)
@@ -359,8 +359,15 @@ double tiles_end(const Params& p, int cg, int G, const double* ready_us, int nkb
 // wide; other values give group g (g < 16) ((v >> 4g) & 15) extra tiles,
 // splitting its strips evenly into narrower tiles.
 void plan_columns(const tpo_ctx* c, Params& p) {
+  if (c->col_split == 0) {  // automatic: the GEMM CTA groups a launch of this op can have
+    int64_t groups = (p.op == tpo::OP_AG ? c->num_sms - tpo::AUTO_COLS_PRODUCERS : c->num_sms) / p.cta_group;
+    if (c->gemm_ctas > 0) groups = std::min<int64_t>(groups, c->gemm_ctas / p.cta_group);
+    if (p.cta_group == 2) groups = std::min<int64_t>(groups, c->max_pairs);
+    tpo::auto_columns(p, c->m, static_cast<int>(std::max<int64_t>(groups, 1)));
+    return;
+  }
   tpo::set_columns(p, c->m, nullptr);
-  if (c->col_split <= 0) return;
+  if (c->col_split < 0) return;
   int extra[tpo::MAX_GROUPS] = {};
   const int most = std::min(p.strips, p.uniform_cols + 15);
   for (int g = 0; g < p.num_groups && g < 16; ++g)
@@ -608,6 +615,17 @@ tpo_status check_ksplit(tpo_ctx* c, const void* const* x, const void* const* w) 
 namespace tpo {
 void set_last_error(const char* msg) { g_err = msg; }
 
+void auto_columns(Params& p, long long m, int gemm_groups) {
+  set_columns(p, m, nullptr);
+  const int per_col = p.num_groups * p.row_tiles;  // tiles per column tile of every group
+  if (per_col <= 0 || 2 * p.total_tiles > gemm_groups) return;
+  const int cols = std::min(p.strips, gemm_groups / per_col);
+  if (cols <= p.uniform_cols) return;
+  int extra[MAX_GROUPS];
+  for (int g = 0; g < p.num_groups; ++g) extra[g] = cols - p.uniform_cols;
+  set_columns(p, m, extra);
+}
+
 int model_producers(const Params& p, int cg, int tp, int num_sms, int max_pairs) {
   const int tiles = p.total_tiles;
   auto grid_of = [&](int P) {
@@ -843,7 +861,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   // K blocks per pipeline stage: one (six stages) unless two are asked for (pairs, when they divide)
   p.kps = (cg == 2 && c->stage_kblocks == 2 && p.kb_per_seg % 2 == 0) ? 2 : 1;
   tpo::set_columns(p, c->m, nullptr);
-  const int tiles = p.total_tiles;  // with the fewest column tiles (the grid sizes follow this count)
+  const int tiles_fewest = p.total_tiles;  // the split mode's per-slot launches keep the fewest column tiles
 
   tpo_status st = reset_trace(c, s);
   if (st != TPO_OK) return st;
@@ -854,6 +872,8 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
   // then skip the copy and run their share at once): all three give the same
   // bits.
   const int split = (c->mode == 0 || c->mode == 1 || c->mode == 2) ? static_cast<int>(c->tail_split) : 0;
+  if (!split) plan_columns(c, p);  // the tail split keeps the fewest column tiles
+  const int tiles = p.total_tiles;  // the GEMM grid follows the launch's tile count
   const int nkb = p.kb_per_seg;
   // producer count, GEMM grid and column plan of the overlapped launch
   auto overlap_grid = [&](int* P, int* G) {
@@ -917,7 +937,7 @@ tpo_status tpo_ag_gemm(tpo_ctx* c, const void* const* x, const void* w, void* y,
     }
     case 4: {  // split: per ring step a chunk copy, then a GEMM launch over that slot
       const int P = producer_count(c, p, cg, tiles, nkb, 0);
-      const int G = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, P, tiles / c->tp);
+      const int G = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms - P, P, tiles_fewest / c->tp);
       cudaError_t e = cudaEventRecord(c->ev_fork, s);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(c->copy, c->ev_fork, 0);
       if (e != cudaSuccess) return cuda_fail(e, "split fork");
@@ -1033,8 +1053,8 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   // pairs with stage_kblocks 2: two K blocks per stage when every accumulation unit has an even count
   p.kps = (cg == 2 && c->stage_kblocks == 2 &&
            (p.reduce_mode ? p.kb_per_seg : p.num_segs * p.kb_per_seg) % 2 == 0) ? 2 : 1;
-  tpo::set_columns(p, c->m, nullptr);
-  const int tiles = p.total_tiles;  // with the fewest column tiles (the grid follows this count)
+  plan_columns(c, p);  // automatic or explicit column plan
+  const int tiles = p.total_tiles;  // the GEMM grid follows the plan's tile count
   tpo_status st = reset_trace(c, s);
   if (st != TPO_OK) return st;
   {
@@ -1056,7 +1076,6 @@ static tpo_status ksplit_common(tpo_ctx* c, int op, const void* const* x, const 
   p.num_gemm = gemm_grid(c, cg, c->gemm_ctas ? c->gemm_ctas : c->num_sms, 0, tiles);
   // the running-sum workspace has one block per SM: at most one GEMM CTA per SM
   if (p.reduce_mode && p.num_gemm > c->num_sms) p.num_gemm = c->num_sms - c->num_sms % cg;
-  plan_columns(c, p);
   return launch(c, p, p.num_gemm, false, s);
 }
 

@@ -208,7 +208,8 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
   p.kb_per_seg = static_cast<int>((k * elem + tpo::BK_BYTES - 1) / tpo::BK_BYTES);
   p.num_segs = 1;
   p.gate = 1;
-  tpo::set_columns(p, m, nullptr);  // every group: the fewest column tiles of at most 256 columns
+  // the automatic column plan of tpo_ag_gemm (more, narrower tiles for launches of few tiles)
+  tpo::auto_columns(p, m, std::min((s->num_sms - tpo::AUTO_COLS_PRODUCERS) / cg, cg == 2 ? s->max_pairs : s->num_sms));
   // producer CTAs from the library's schedule model (kept for the latest shape on this device)
   const long long shape[5] = {tp, n, k, m, dtype};
   if (std::memcmp(shape, s->shape, sizeof(shape)) != 0) {

@@ -1,7 +1,8 @@
 """Column plans on the GPU (option col_split): groups whose 32-column strips are
 split into more, narrower tiles (down to one strip) give the same bits as
 whole 256-column tiles in every mode, stay within the oracle's bar and keep
-the done counters' common target."""
+the done counters' common target.  The automatic plan (the default) is the
+one the host model restated in test_schedule picks."""
 
 import numpy as np
 import pytest
@@ -11,7 +12,7 @@ import oracle
 from tensor_comm_gemm_gb300 import synth
 from tensor_comm_gemm_gb300 import tpoverlap as t
 from gpu_util import AgRun, KsplitRun, assert_close, host_bits, host_f64
-from test_schedule import packed
+from test_schedule import auto_columns, auto_groups, choose_cg, packed, plan
 
 pytestmark = pytest.mark.gpu
 
@@ -23,9 +24,18 @@ def _built(cuda_ok):
 
 
 def explicit_plans(groups):
-    """col_split values: fewest tiles (the default) and packed extras (4 bits
-    per group) from one extra tile to 15."""
-    return [0, packed([1] * groups), packed([(3 * g + 1) % 16 for g in range(groups)]), packed([15] * groups)]
+    """col_split values: the fewest tiles (-1), the automatic plan (0, the
+    default) and packed extras (4 bits per group) from one extra tile to 15."""
+    return [-1, 0, packed([1] * groups), packed([(3 * g + 1) % 16 for g in range(groups)]), packed([15] * groups)]
+
+
+def expected_auto_plan(op, tp, n, k, m, chunks=1):
+    """last_col_plan of the automatic plan, from the host model's restatement."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cg = choose_cg(op, tp, n, chunks)
+    pl = plan(op, tp, n, k, m, 2, chunks, cg)
+    auto_columns(pl, m, auto_groups(op, cg, num_sms=sms, max_pairs=sms // 2))
+    return packed([c - pl["base_cols"] for c in pl["group_cols"]])
 
 
 @pytest.mark.parametrize("tp,n,k,m", [(4, 2048, 512, 1024), (3, 768, 192, 264), (2, 512, 256, 520),
@@ -50,6 +60,10 @@ def test_ag_column_plans_bit_identical(tp, n, k, m):
                 assert np.array_equal(bits, first), (cs, mode, t.tpo_get_opt(run.ctx, "last_col_plan"))
                 if cs > 0:
                     assert t.tpo_get_opt(run.ctx, "last_col_plan") != 0
+                if cs < 0:
+                    assert t.tpo_get_opt(run.ctx, "last_col_plan") == 0
+                if cs == 0:
+                    assert t.tpo_get_opt(run.ctx, "last_col_plan") == expected_auto_plan("ag", tp, n, k, m)
     finally:
         run.close()
 

@@ -469,3 +469,49 @@ def test_producer_model_properties():
         set_columns(pl, 256, extra)
         for g in range(2):
             assert sum(tile_strips(pl, g, c)[1] for c in range(pl["group_cols"][g])) == pl["strips"]
+
+
+AUTO_COLS_PRODUCERS = 32
+
+
+def auto_columns(pl, m, gemm_groups):
+    """The host's automatic column plan (col_split 0): the fewest column tiles,
+    unless the launch has at most half as many tiles as GEMM CTA groups; then
+    every group gets min(strips, groups // (groups x row tiles)) column tiles."""
+    set_columns(pl, m)
+    per_col = pl["groups"] * pl["row_tiles"]
+    if per_col <= 0 or 2 * pl["total"] > gemm_groups:
+        return pl
+    cols = min(pl["strips"], gemm_groups // per_col)
+    if cols <= pl["base_cols"]:
+        return pl
+    return set_columns(pl, m, [cols - pl["base_cols"]] * pl["groups"])
+
+
+def auto_groups(op, cg, num_sms=152, max_pairs=76):
+    g = (num_sms - AUTO_COLS_PRODUCERS if op == "ag" else num_sms) // cg
+    return min(g, max_pairs) if cg == 2 else g
+
+
+def test_auto_column_plan():
+    """Launches of many tiles keep the fewest (C2, C5, the long-K RS); small
+    launches split their columns into more, narrower tiles that still fit in
+    one round: C1 (tp=2, 256^3, single-SM tiles) from 2 tiles of 8 strips to
+    16 tiles of one strip."""
+    for op, tp, n, k, m, elem, chunks, cg in [("ag", 4, 4096, 4096, 4096, 2, 1, 2), ("ag", 8, 16384, 8192, 28672, 1, 1, 2),
+                                              ("rs", 8, 16384, 28672, 8192, 2, 1, 2), ("ar", 2, 8192, 8192, 8192, 2, 4, 2)]:
+        pl = plan(op, tp, n, k, m, elem, chunks, cg)
+        fewest = list(pl["group_cols"])
+        assert auto_columns(pl, m, auto_groups(op, cg))["group_cols"] == fewest
+    pl = auto_columns(plan("ag", 2, 256, 256, 256, 2, 1, 1), 256, auto_groups("ag", 1))
+    assert pl["group_cols"] == [8, 8] and pl["total"] == 16
+    for op, tp, n, k, m, elem, chunks in SHAPES:
+        for cg in (1, 2):
+            pl = plan(op, tp, n, k, m, elem, chunks, cg)
+            fewest_total, G = pl["total"], auto_groups(op, cg)
+            auto_columns(pl, m, G)
+            if pl["total"] != fewest_total:          # split only launches of at most half a round
+                assert 2 * fewest_total <= G and pl["total"] <= G
+            for g in range(pl["groups"]):            # every tile 1..8 strips, the strips covered once
+                widths = [tile_strips(pl, g, c)[1] for c in range(pl["group_cols"][g])]
+                assert sum(widths) == pl["strips"] and 1 <= min(widths) and max(widths) <= MAX_TILE_STRIPS
