@@ -341,8 +341,9 @@ const char* tpo_version(void);
  *
  * Computes what tpo_ag_gemm computes for observer rank 0 in one overlapped
  * launch with the launch shape tpo_ag_gemm picks under default options (CTA
- * pairs wherever n/tp is a multiple of 256, the schedule model's producer
- * count, 2 s wait bound).  The result is bit-identical to tpo_ag_gemm's whenever that call computes whole
+ * pairs wherever n/tp is a multiple of 256, the automatic column plan, the
+ * schedule model's producer count, 2 s wait bound).  The result is
+ * bit-identical to tpo_ag_gemm's whenever that call computes whole
  * tiles (option tail_split 0, the default), in any mode and with either MMA
  * variant; the tail-split schedules (tail_split 1 to 3) add K-split partials
  * in an order that depends on their launch shape and agree with it only
