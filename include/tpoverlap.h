@@ -235,6 +235,14 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      same at any width from 128 to 256 columns, so more
  *                      tiles pay only where they all fit in one round: each
  *                      tile's epilogue is then shorter.
+ *   "sched"            which CTA group computes which tile: 1 round robin
+ *                      (group g takes tiles g, g+G, g+2G, ...); 2 dynamic
+ *                      (each group claims its next tile from a launch-wide
+ *                      counter, so that faster groups take more tiles and
+ *                      the tiles in flight stay a contiguous run of the tile
+ *                      order); 0 (default) automatic: dynamic for launches of
+ *                      at least 8 rounds, round robin otherwise and with the
+ *                      AG tail split.  Results are identical either way.
  *   "cta_group"        MMA variant: 0 automatic, 1 single-SM 128x256 tiles,
  *                      2 CTA pairs (2-SM MMA, 256x256 tiles; needs every tile
  *                      group a multiple of 256 rows).  Results are identical.
@@ -268,11 +276,11 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      mode 2), so the MMAs never wait for the additions.
  * Read-only keys for tpo_get_opt: "last_producer_ctas", "last_gemm_ctas",
  * "last_cta_group", "last_stage_kblocks", "last_split_tiles",
- * "last_late_groups", "last_col_plan" (shape of the context's latest kernel
+ * "last_late_groups", "last_col_plan", "last_sched" (shape of the context's latest kernel
  * launch: producer CTAs, GEMM CTAs, 1 or 2 CTAs per MMA, K blocks per
  * pipeline stage, tiles split along K, producer CTA groups that joined the
  * GEMM, extra column tiles per group in the col_split encoding, each
- * group's count capped at 15 in the report),
+ * group's count capped at 15 in the report, 1 round robin or 2 dynamic tiles),
  * "coop_clusters" (0 once the driver refused a cooperative cluster launch),
  * "tp", "n", "k", "m", "dtype" (the sizes the context was created for).
  * Environment variables TPO_<KEY in upper case> override the defaults at

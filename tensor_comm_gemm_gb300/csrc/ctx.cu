@@ -99,7 +99,7 @@ struct tpo_ctx {
   int64_t producer_sms = 0, gemm_ctas = 0, mode = 0, seq_copy_ctas = 0, self_rank = 0, wait_timeout_ms = 2000,
           trace = 0, debug_skip_chunk = -1, debug_delay_ns = 0, debug_last_step = -1, cta_group = 0,
           cooperative = 0, reduce = 0, tail_split = 0, debug_skip_partial = -1, stage_kblocks = 1,
-          col_split = 0, pdl = 1;
+          col_split = 0, pdl = 1, sched = 0;
   // device memory
   uint8_t* staging = nullptr;
   size_t staging_bytes = 0;
@@ -127,6 +127,8 @@ struct tpo_ctx {
   int pc_val = 0;                // its producer count
   int64_t last_col_plan = 0;     // packed extra column tiles of the latest kernel launch (col_split encoding)
   int64_t last_late_groups = 0;  // producer CTA groups that joined its GEMM
+  int64_t last_dyn = 0;          // 1 when the latest kernel launch claimed its tiles dynamically
+  uint32_t sched_base = 0;       // value of the device's tile-claim counter after the launches so far
   uint32_t part_epoch = 0;       // launches with the AG tail split so far (part_ready value of this launch)
   // tensor-map cache: the maps of the latest kCacheWays pointer sets of each op
   static constexpr int kCacheWays = 4;
@@ -167,6 +169,7 @@ int64_t* opt_slot(tpo_ctx* c, const char* key, int64_t* lo, int64_t* hi) {
       {"stage_kblocks", &tpo_ctx::stage_kblocks, 1, 2},
       {"col_split", &tpo_ctx::col_split, -1, INT64_MAX},
       {"pdl", &tpo_ctx::pdl, 0, 1},
+      {"sched", &tpo_ctx::sched, 0, 2},
   };
   for (const E& e : table)
     if (std::strcmp(e.k, key) == 0) {
@@ -184,7 +187,7 @@ const char* kOptKeys[] = {"producer_sms",     "gemm_ctas",      "mode",         
                           "self_rank",        "wait_timeout_ms", "trace",          "debug_skip_chunk",
                           "debug_delay_ns",   "debug_last_step", "cta_group",      "cooperative",
                           "reduce",           "tail_split",     "debug_skip_partial", "stage_kblocks",
-                          "col_split",        "pdl"};
+                          "col_split",        "pdl",           "sched"};
 
 void destroy_all(tpo_ctx* c) {
   if (!c) return;
@@ -231,7 +234,20 @@ tpo_status reset_trace(tpo_ctx* c, cudaStream_t s) {
 
 int64_t packed_columns(const Params& p);
 
-tpo_status launch(tpo_ctx* c, const Params& p, int grid, bool coop, cudaStream_t s) {
+// Dynamic tiles (option sched: 0 automatic, 1 round robin, 2 dynamic) for a
+// GEMM launch of `groups` CTA groups: automatic takes them for launches of at
+// least 8 rounds, where the groups' speeds drift apart over a round-robin
+// schedule.  The tail-split build keeps its own schedule.
+bool want_dynamic(const tpo_ctx* c, const Params& p, int groups) {
+  if (groups <= 0 || p.tail_split || p.late_groups || c->sched == 1) return false;
+  return c->sched == 2 || p.total_tiles >= 8 * groups;
+}
+
+tpo_status launch(tpo_ctx* c, Params& p, int grid, bool coop, cudaStream_t s) {
+  const int groups = p.cta_group > 0 ? p.num_gemm / p.cta_group : 0;
+  p.dyn = want_dynamic(c, p, groups) ? 1 : 0;
+  p.sched_base = c->sched_base;
+  c->last_dyn = p.dyn;
   c->last_producers = p.num_producers;
   c->last_gemm_ctas = p.num_gemm;
   c->last_cta_group = p.cta_group;
@@ -252,6 +268,7 @@ tpo_status launch(tpo_ctx* c, const Params& p, int grid, bool coop, cudaStream_t
     e = tpo::launch_fused(p, grid, false, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  if (p.dyn) c->sched_base += static_cast<uint32_t>(p.total_tiles + groups);  // every group's claims, one past the end each
   e = cudaEventRecord(c->last, s);
   if (e != cudaSuccess) return cuda_fail(e, "event record");
   c->has_last = true;
@@ -791,6 +808,7 @@ tpo_status tpo_get_opt(tpo_ctx* c, const char* key, int64_t* value) {
   if (std::strcmp(key, "last_split_tiles") == 0) return *value = c->last_split_tiles, TPO_OK;
   if (std::strcmp(key, "last_late_groups") == 0) return *value = c->last_late_groups, TPO_OK;
   if (std::strcmp(key, "last_col_plan") == 0) return *value = c->last_col_plan, TPO_OK;
+  if (std::strcmp(key, "last_sched") == 0) return *value = c->last_dyn ? 2 : 1, TPO_OK;
   if (std::strcmp(key, "coop_clusters") == 0) return *value = c->coop_clusters ? 1 : 0, TPO_OK;
   if (std::strcmp(key, "tp") == 0) return *value = c->tp, TPO_OK;
   if (std::strcmp(key, "n") == 0) return *value = c->n, TPO_OK;
@@ -1132,6 +1150,7 @@ tpo_status tpo_sync_status(tpo_ctx* c) {
   c->done_target = 0;
   c->done_op = -1;
   c->done_groups = 0;
+  c->sched_base = 0;
   return fail(TPO_ERR_TIMEOUT, "device wait timed out (site %u, block %u, extra %u)", err[1], err[2], err[3]);
 }
 

@@ -114,6 +114,34 @@ __device__ bool mbar_wait(const Params& p, uint32_t bar, uint32_t parity, uint32
     }
   }
 }
+// mbar_wait whose completion acquires at cluster scope: arrivals from the
+// other CTA of a pair (with release at cluster scope) order that CTA's earlier
+// writes before this thread's later accesses.
+__device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+__device__ bool mbar_wait_cluster(const Params& p, uint32_t bar, uint32_t parity, uint32_t site) {
+  if (mbar_test_cluster(bar, parity)) return true;
+  const unsigned long long t0 = gtime();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_cluster(bar, parity)) return true;
+    if ((i & 15u) == 0u) {
+      if (aborted(p)) return false;
+      if (gtime() - t0 > p.timeout_ns) {
+        raise_error(p, DEV_TIMEOUT, site, blockIdx.x);
+        return false;
+      }
+    }
+  }
+}
 // mbar_wait that adds the SM cycles spent blocked to *cycles (trace runs only).
 __device__ __forceinline__ bool mbar_wait_timed(const Params& p, uint32_t bar, uint32_t parity, uint32_t site,
                                                 bool honor_abort, unsigned long long* cycles) {
@@ -298,6 +326,17 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
 }
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
@@ -492,10 +531,26 @@ struct Seg {
   int w0, nw;  // SEG_FINISH: the groups w0, ..., w0 + nw - 1 hold the tile's later parts
   bool last;   // SEG_FINISH: no tile of this CTA group follows (its pipeline stages are then idle)
 };
+// Dynamic tiles (builds without the split, p.dyn): instead of the fixed round
+// robin, a CTA group's TMA thread (the even CTA's, for pairs) claims each next
+// tile with an atomic add on a launch-wide counter, so that groups that run
+// faster take more tiles and the tiles in flight stay a contiguous run of the
+// tile order (their shared operands stay in L2 together).  It passes every
+// index to the group's other roles (its MMA thread, the epilogue warps and,
+// for pairs, the odd CTA's TMA thread and epilogue warps) through a ring of
+// TQ_DEPTH shared-memory words: a full barrier per slot in each CTA (one
+// arrival from the claiming thread) and an empty barrier per slot in the even
+// CTA (one arrival from every reading thread or warp).  A claim at or past
+// the launch's tile count ends the group's work; each group makes exactly one
+// such claim, so a launch advances the counter by tiles + groups.
 template <bool SPLIT>  // false: a kernel built without the split (round robin only)
 struct SegIter {
   int g, s, nfull, G, whole_base, slot, kbu, kps;
   bool first;
+  // dynamic tiles: 0 round robin, 1 the claiming thread, 2 a reading thread, 3 a reading warp
+  int dyn = 0, T = 0, cg = 1;
+  uint32_t q = 0, ring = 0, full0 = 0, empty0 = 0, peer_ring = 0, peer_full0 = 0, rank = 0, pre = 0;
+  const Params* pp = nullptr;
   int tail_base, ts, wr_t, wr_lo, wr_hi, tw0, tw1, fin_t, fin_hi, fin_w0, fin_nw;
   bool has_wr, has_fin;
   // `tail`: the CTA's TailDesc in shared memory (split builds with the split on)
@@ -528,6 +583,73 @@ struct SegIter {
     fin_hi = d.fin_hi;
     fin_w0 = d.fin_w0;
     fin_nw = d.fin_nw;
+  }
+  // Switches this iterator to dynamic tiles in role `role` (see above) for a
+  // CTA of group size cg_ whose shared memory starts at sbase.
+  __device__ void set_dynamic(const Params& p, int role, uint32_t sbase, uint32_t rank_, int cg_, int T_) {
+    dyn = role;
+    pp = &p;
+    T = T_;
+    cg = cg_;
+    rank = rank_;
+    ring = sbase + SMEM_TQ;
+    full0 = sbase + SMEM_BARS + 8u * BAR_TQ_FULL;
+    empty0 = sbase + SMEM_BARS + 8u * BAR_TQ_EMPTY;
+    if (cg == 2) {
+      peer_ring = map_to_rank(ring, 1);
+      peer_full0 = map_to_rank(full0, 1);
+      if (rank != 0) empty0 = map_to_rank(empty0, 0);  // the odd CTA's readers arrive on the even CTA's barrier
+    }
+  }
+  __device__ bool dyn_next(Seg& o) {
+    const Params& p = *pp;
+    const uint32_t slot_q = q % TQ_DEPTH, par = (q / TQ_DEPTH) & 1u;
+    uint32_t t = 0;
+    if (dyn == 1) {
+      // the slot's previous index has been read by every role of the group
+      // (cluster-scope acquire: the odd CTA's reads of the slot come before the overwrite below)
+      if (q >= TQ_DEPTH && !mbar_wait_cluster(p, empty0 + 8u * slot_q, par ^ 1u, SITE_TILE)) return false;
+      // The claim for the tile after this one goes out now and is read at the
+      // next call, so its round trip overlaps this tile's work.
+      if (q == 0) pre = atomicAdd(&p.words->sched, 1u) - p.sched_base;
+      t = pre < static_cast<uint32_t>(T) ? pre : static_cast<uint32_t>(T);
+      if (t < static_cast<uint32_t>(T)) pre = atomicAdd(&p.words->sched, 1u) - p.sched_base;
+      st_shared_u32(ring + 4u * slot_q, t);
+      mbar_arrive(full0 + 8u * slot_q);
+      if (cg == 2) {
+        st_shared_cluster_u32(peer_ring + 4u * slot_q, t);
+        mbar_arrive_cluster(peer_full0 + 8u * slot_q);  // release: the index is visible first
+      }
+    } else {
+      const int lane = threadIdx.x & 31;
+      int ok = 1;
+      if (dyn == 2 || lane == 0) {
+        // (in the odd CTA the index was written from the even CTA: cluster-scope acquire)
+        ok = (rank != 0 ? mbar_wait_cluster(p, full0 + 8u * slot_q, par, SITE_TILE)
+                        : mbar_wait(p, full0 + 8u * slot_q, par, SITE_TILE, true)) ? 1 : 0;
+        if (ok) {
+          t = ld_shared_u32(ring + 4u * slot_q);
+          if (rank != 0)
+            mbar_arrive_cluster(empty0 + 8u * slot_q);
+          else
+            mbar_arrive(empty0 + 8u * slot_q);
+        }
+      }
+      if (dyn == 3) {
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        t = __shfl_sync(0xffffffffu, t, 0);
+      }
+      if (!ok) return false;
+    }
+    ++q;
+    if (t >= static_cast<uint32_t>(T)) return false;
+    o.t = static_cast<int>(t);
+    o.kb_lo = 0;
+    o.kb_hi = kbu * kps;
+    o.kind = SEG_WHOLE;
+    o.w0 = o.nw = 0;
+    o.last = false;
+    return true;
   }
   __device__ bool tail_next(Seg& o) {
     if (ts == 0) {
@@ -566,6 +688,9 @@ struct SegIter {
     return false;
   }
   __device__ bool next(Seg& o) {
+    if constexpr (!SPLIT) {
+      if (dyn) return dyn_next(o);
+    }
     if constexpr (SPLIT) {
       o.w0 = o.nw = 0;
       o.last = false;
@@ -727,6 +852,9 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
   bool ok = true;
   unsigned long long cyc_empty = 0;
   SegIter<SPLIT> it(p, g, G, total_tiles, nkb, tail);
+  if constexpr (!SPLIT) {
+    if (p.dyn) it.set_dynamic(p, (CG == 1 || rank == 0) ? 1 : 2, sbase, rank, CG, total_tiles);
+  }
   Seg sg;
   while (ok && it.next(sg)) {
     const Tile T = tile_at<PP::TILE_M>(p, sg.t);
@@ -837,6 +965,9 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   bool ok = true;
   unsigned long long cyc_full = 0, cyc_tempty = 0;
   SegIter<SPLIT> it(p, g, G, total_tiles, nkb, tail);
+  if constexpr (!SPLIT) {
+    if (p.dyn) it.set_dynamic(p, 2, sbase, 0, CG, total_tiles);
+  }
   Seg sg;
   while (ok && it.next(sg)) {
    const uint32_t idesc = idesc_n(idesc0, tile_at<PP::TILE_M>(p, sg.t).ncols);
@@ -1104,6 +1235,9 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
     return true;
   };
   SegIter<SPLIT> it(p, g, G, total_tiles, p.num_segs * p.kb_per_seg, tail);
+  if constexpr (!SPLIT) {
+    if (p.dyn) it.set_dynamic(p, 3, sbase_smem, rank, CG, total_tiles);
+  }
   Seg sg;
   while (ok_all && it.next(sg)) {
     const Tile T = tile_at<PP::TILE_M>(p, sg.t);
@@ -1304,6 +1438,10 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
       mbar_init(B.tempty0 + 8u * a, CG * EPI_WARPS);  // one arrival per epilogue warp of the group
     }
     mbar_init(B.drain, 1);
+    for (int s = 0; s < TQ_DEPTH; ++s) {  // dynamic tiles: the index ring's barriers
+      mbar_init(sbase + SMEM_BARS + 8u * (BAR_TQ_FULL + s), 1);
+      mbar_init(sbase + SMEM_BARS + 8u * (BAR_TQ_EMPTY + s), CG * (1 + EPI_WARPS));
+    }
     if constexpr (SPLIT)
       for (int w = 0; w < EPI_WARPS; ++w) mbar_init(B.full0 + 8u * (BAR_PART - BAR_FULL + w), 1);
     fence_barrier_init();

@@ -224,6 +224,10 @@ extern "C" tpo_status tpo_ag_gemm_noalloc(int tp, int64_t n, int64_t k, int64_t 
   for (int r = 0; r < TPO_MAX_TP; ++r) p.target[r] = static_cast<uint32_t>(P);  // counters start at zero
   p.num_producers = P;
   p.num_gemm = G;
+  // dynamic tiles for launches of at least 8 rounds, as tpo_ag_gemm's default; the claim counter
+  // starts at zero with the other words
+  p.dyn = (tiles >= 8 * (G / cg)) ? 1 : 0;
+  p.sched_base = 0;
 
   // The array keeps the previous call's contents: the counters and the error
   // word must start at zero (the staging buffer is fully rewritten).

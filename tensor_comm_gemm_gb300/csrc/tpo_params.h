@@ -55,13 +55,17 @@ constexpr int SMEM_STAGES = 0;
 constexpr int SMEM_EPI = SMEM_STAGES + STAGE_AREA;                      // 196608
 constexpr int SMEM_BARS = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;     // 212992
 // barriers: full[MAX_STAGES], empty[MAX_STAGES], tmem_full[2], tmem_empty[2],
-// drain, copy[COPY_BUFS], part[EPI_WARPS] (split-tile finishers' bulk copies)
+// drain, copy[COPY_BUFS], part[EPI_WARPS] (split-tile finishers' bulk copies),
+// tile_full[TQ_DEPTH], tile_empty[TQ_DEPTH] (the dynamic tiles' index ring)
+constexpr int TQ_DEPTH = 4;  // tile indices a CTA group's claiming thread may run ahead of its slowest role
 constexpr int BAR_FULL = 0, BAR_EMPTY = MAX_STAGES, BAR_TFULL = 2 * MAX_STAGES, BAR_TEMPTY = BAR_TFULL + 2,
-              BAR_DRAIN = BAR_TEMPTY + 2, BAR_COPY = BAR_DRAIN + 1, BAR_PART = BAR_COPY + COPY_BUFS;
-constexpr int NUM_BARS = BAR_PART + EPI_WARPS;
+              BAR_DRAIN = BAR_TEMPTY + 2, BAR_COPY = BAR_DRAIN + 1, BAR_PART = BAR_COPY + COPY_BUFS,
+              BAR_TQ_FULL = BAR_PART + EPI_WARPS, BAR_TQ_EMPTY = BAR_TQ_FULL + TQ_DEPTH;
+constexpr int NUM_BARS = BAR_TQ_EMPTY + TQ_DEPTH;
 constexpr int SMEM_TMEM_SLOT = SMEM_BARS + NUM_BARS * 8;
 constexpr int SMEM_TAIL = SMEM_TMEM_SLOT + 16;   // split builds: the CTA group's schedule (64 bytes)
-constexpr int SMEM_USED = SMEM_TAIL + 64;
+constexpr int SMEM_TQ = SMEM_TAIL + 64;          // dynamic tiles: the ring of claimed tile indices
+constexpr int SMEM_USED = SMEM_TQ + 4 * TQ_DEPTH;
 constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for aligning the base
 static_assert(COPY_BUFS * COPY_PIECE <= STAGE_AREA, "copy ring must fit the stage area");
 static_assert(Pipe<1>::STAGES * Pipe<1>::STAGE_BYTES <= STAGE_AREA && Pipe<2>::STAGES <= MAX_STAGES, "stages");
@@ -84,7 +88,8 @@ enum Site : uint32_t {
   SITE_TMEM_FULL = 5,  // epilogue waiting for a finished accumulator
   SITE_COPY = 6,       // producer waiting for a bulk load
   SITE_DRAIN = 7,      // clean-up waits after a failure
-  SITE_PARTIAL = 8     // epilogue waiting for a split tile's partial
+  SITE_PARTIAL = 8,    // epilogue waiting for a split tile's partial
+  SITE_TILE = 9        // a role waiting for its pair's next tile index (dynamic tiles)
 };
 
 // A CTA group's schedule with the AG tail split (see SegIter in the kernel),
@@ -106,7 +111,8 @@ struct DevWords {
   uint32_t err[4];
   uint32_t done[TPO_MAX_ROW_CHUNKS];    // per output group done counters (RS owner block, AR row chunk; monotonic)
   uint32_t part_ready[MAX_GEMM_CTAS * 4];  // per GEMM CTA and epilogue warp: launch number of its last stored partial
-  uint32_t pad[12];
+  uint32_t sched;                        // dynamic tiles: claims of every launch so far (monotonic)
+  uint32_t pad[11];
   unsigned long long trace[TPO_TRACE_WORDS];
 };
 
@@ -129,7 +135,7 @@ struct Params {
   uint32_t target[TPO_MAX_TP];  // per slot: counter value once this call has published it
   uint32_t done_target;   // RS/AR done-counter value once this call stored the whole group
   uint32_t part_target;   // AG tail split: this launch's number (part_ready value of a stored partial)
-  uint32_t pad1;
+  uint32_t sched_base;    // dynamic tiles: words->sched at this launch's start (claims minus this = tile index)
   int op;
   int fp8;
   int tp;
@@ -169,6 +175,8 @@ struct Params {
   int copy_on;            // producer CTAs copy (0: they only run as late GEMM groups)
   int skip_part;          // test hook: this GEMM CTA never publishes its partial (-1: none)
   int pdl;                // host side: launch with programmatic dependent launch (set-up overlaps the launch before)
+  int dyn;                // builds without the split: each CTA group claims its next tile from words->sched
+                          // (1) instead of taking tiles g, g+G, ... (0)
 };
 
 // Column tiling of a launch with p.num_groups groups of p.row_tiles row tiles

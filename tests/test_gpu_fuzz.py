@@ -72,6 +72,8 @@ def draw(seed):
             chunks = int(rng.integers(1, 4))
             n = chunks * tp * int(rng.choice([int(rng.integers(1, 200)), 256]))
             opts["chunks"] = chunks
+    # tile claiming (drawn apart so that the draws above stay as they were)
+    opts["sched"] = int(np.random.default_rng(seed + 7919).choice([0, 1, 2, 2]))
     return op, dtype, tp, n, k, m, opts
 
 
