@@ -23,10 +23,12 @@
 //    GEMM+RS / GEMM+AR the K loop of a tile walks the ranks' K-slices in a
 //    fixed ring order into one accumulator.
 //
-// The kernel is built twice per tile variant: fused_kernel<CG, false> (the
-// default) and fused_kernel<CG, true> with the optional AG tail split (K-split
-// tiles, fp32 partials, producer CTAs joining the GEMM), launched only when a
-// call uses the split, so the default build carries none of its code.
+// The kernel is built three times per tile variant: fused_kernel<CG, false,
+// false> (round-robin tiles), fused_kernel<CG, false, true> (dynamic tiles,
+// claimed from a launch-wide counter) and fused_kernel<CG, true, false> with
+// the optional AG tail split (K-split tiles, fp32 partials, producer CTAs
+// joining the GEMM), each launched only when a call asks for its schedule, so
+// no build carries the others' code.
 //
 // Every wait (mbarrier, chunk counter) is bounded by the device global timer.
 // On expiry the waiting thread records the failure in the context's error word
@@ -36,6 +38,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "tpo_params.h"
 
@@ -543,14 +547,18 @@ struct Seg {
 // CTA (one arrival from every reading thread or warp).  A claim at or past
 // the launch's tile count ends the group's work; each group makes exactly one
 // such claim, so a launch advances the counter by tiles + groups.
-template <bool SPLIT>  // false: a kernel built without the split (round robin only)
-struct SegIter {
+struct DynTiles {  // the dynamic instantiation's ring state (role 1 the claiming thread, 2 a reading thread, 3 a reading warp)
+  int dyn, T, cg;
+  uint32_t q, ring, full0, empty0, peer_ring, peer_full0, rank, pre;
+  const Params* pp;
+};
+struct NoDynTiles {};
+// SPLIT: the build with the tail split; DYN: the build with dynamic tiles
+// (kernels built without either take the round robin only).
+template <bool SPLIT, bool DYN = false>
+struct SegIter : std::conditional_t<DYN, DynTiles, NoDynTiles> {
   int g, s, nfull, G, whole_base, slot, kbu, kps;
   bool first;
-  // dynamic tiles: 0 round robin, 1 the claiming thread, 2 a reading thread, 3 a reading warp
-  int dyn = 0, T = 0, cg = 1;
-  uint32_t q = 0, ring = 0, full0 = 0, empty0 = 0, peer_ring = 0, peer_full0 = 0, rank = 0, pre = 0;
-  const Params* pp = nullptr;
   int tail_base, ts, wr_t, wr_lo, wr_hi, tw0, tw1, fin_t, fin_hi, fin_w0, fin_nw;
   bool has_wr, has_fin;
   // `tail`: the CTA's TailDesc in shared memory (split builds with the split on)
@@ -587,22 +595,28 @@ struct SegIter {
   // Switches this iterator to dynamic tiles in role `role` (see above) for a
   // CTA of group size cg_ whose shared memory starts at sbase.
   __device__ void set_dynamic(const Params& p, int role, uint32_t sbase, uint32_t rank_, int cg_, int T_) {
-    dyn = role;
-    pp = &p;
-    T = T_;
-    cg = cg_;
-    rank = rank_;
-    ring = sbase + SMEM_TQ;
-    full0 = sbase + SMEM_BARS + 8u * BAR_TQ_FULL;
-    empty0 = sbase + SMEM_BARS + 8u * BAR_TQ_EMPTY;
-    if (cg == 2) {
-      peer_ring = map_to_rank(ring, 1);
-      peer_full0 = map_to_rank(full0, 1);
-      if (rank != 0) empty0 = map_to_rank(empty0, 0);  // the odd CTA's readers arrive on the even CTA's barrier
+    auto& d = *static_cast<DynTiles*>(this);
+    d.dyn = role;
+    d.pp = &p;
+    d.T = T_;
+    d.cg = cg_;
+    d.rank = rank_;
+    d.q = d.pre = 0;
+    d.ring = sbase + SMEM_TQ;
+    d.full0 = sbase + SMEM_BARS + 8u * BAR_TQ_FULL;
+    d.empty0 = sbase + SMEM_BARS + 8u * BAR_TQ_EMPTY;
+    d.peer_ring = d.peer_full0 = 0;
+    if (d.cg == 2) {
+      d.peer_ring = map_to_rank(d.ring, 1);
+      d.peer_full0 = map_to_rank(d.full0, 1);
+      if (d.rank != 0) d.empty0 = map_to_rank(d.empty0, 0);  // the odd CTA's readers arrive on the even CTA's barrier
     }
   }
   __device__ bool dyn_next(Seg& o) {
-    const Params& p = *pp;
+    auto& d = *static_cast<DynTiles*>(this);
+    const Params& p = *d.pp;
+    const int dyn = d.dyn, T = d.T, cg = d.cg;
+    const uint32_t q = d.q, ring = d.ring, full0 = d.full0, empty0 = d.empty0, rank = d.rank;
     const uint32_t slot_q = q % TQ_DEPTH, par = (q / TQ_DEPTH) & 1u;
     uint32_t t = 0;
     if (dyn == 1) {
@@ -611,14 +625,14 @@ struct SegIter {
       if (q >= TQ_DEPTH && !mbar_wait_cluster(p, empty0 + 8u * slot_q, par ^ 1u, SITE_TILE)) return false;
       // The claim for the tile after this one goes out now and is read at the
       // next call, so its round trip overlaps this tile's work.
-      if (q == 0) pre = atomicAdd(&p.words->sched, 1u) - p.sched_base;
-      t = pre < static_cast<uint32_t>(T) ? pre : static_cast<uint32_t>(T);
-      if (t < static_cast<uint32_t>(T)) pre = atomicAdd(&p.words->sched, 1u) - p.sched_base;
+      if (q == 0) d.pre = atomicAdd(&p.words->sched, 1u) - p.sched_base;
+      t = d.pre < static_cast<uint32_t>(T) ? d.pre : static_cast<uint32_t>(T);
+      if (t < static_cast<uint32_t>(T)) d.pre = atomicAdd(&p.words->sched, 1u) - p.sched_base;
       st_shared_u32(ring + 4u * slot_q, t);
       mbar_arrive(full0 + 8u * slot_q);
       if (cg == 2) {
-        st_shared_cluster_u32(peer_ring + 4u * slot_q, t);
-        mbar_arrive_cluster(peer_full0 + 8u * slot_q);  // release: the index is visible first
+        st_shared_cluster_u32(d.peer_ring + 4u * slot_q, t);
+        mbar_arrive_cluster(d.peer_full0 + 8u * slot_q);  // release: the index is visible first
       }
     } else {
       const int lane = threadIdx.x & 31;
@@ -641,7 +655,7 @@ struct SegIter {
       }
       if (!ok) return false;
     }
-    ++q;
+    d.q = q + 1;
     if (t >= static_cast<uint32_t>(T)) return false;
     o.t = static_cast<int>(t);
     o.kb_lo = 0;
@@ -688,9 +702,7 @@ struct SegIter {
     return false;
   }
   __device__ bool next(Seg& o) {
-    if constexpr (!SPLIT) {
-      if (dyn) return dyn_next(o);
-    }
+    if constexpr (DYN) return dyn_next(o);
     if constexpr (SPLIT) {
       o.w0 = o.nw = 0;
       o.last = false;
@@ -833,7 +845,7 @@ struct Bars {
 // The TMA issuer: one thread keeps every stage of the pipeline in flight.  Like
 // the MMA issuer it runs from registers only (tensor-map addresses, ring
 // position, stage and phase), so that refills follow stage releases closely.
-template <int CG, bool AG, bool SPLIT, int KPS>
+template <int CG, bool AG, bool SPLIT, int KPS, bool DYN>
 __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_t rank, int g, int G,
                          int total_tiles, int nkb, bool trace, const TailDesc* tail) {
   using PP = Pipe<CG>;
@@ -851,10 +863,8 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
   uint32_t ready = 0, stage = 0, phase = 0, armed = 0;
   bool ok = true;
   unsigned long long cyc_empty = 0;
-  SegIter<SPLIT> it(p, g, G, total_tiles, nkb, tail);
-  if constexpr (!SPLIT) {
-    if (p.dyn) it.set_dynamic(p, (CG == 1 || rank == 0) ? 1 : 2, sbase, rank, CG, total_tiles);
-  }
+  SegIter<SPLIT, DYN> it(p, g, G, total_tiles, nkb, tail);
+  if constexpr (DYN) it.set_dynamic(p, (CG == 1 || rank == 0) ? 1 : 2, sbase, rank, CG, total_tiles);
   Seg sg;
   while (ok && it.next(sg)) {
     const Tile T = tile_at<PP::TILE_M>(p, sg.t);
@@ -922,16 +932,16 @@ __device__ void tma_loop(const Params& p, uint32_t sbase, const Bars& B, uint32_
   if (trace) atomicAdd(&p.words->trace[TPO_TRACE_CYC_TMA_EMPTY], cyc_empty);
 }
 
-template <int CG, bool SPLIT>
+template <int CG, bool SPLIT, bool DYN>
 __device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, uint32_t rank, int g, int G,
                          int total_tiles, int nkb, const TailDesc* tail) {
   const bool trace = p.trace_on != 0;
   if (p.op == OP_AG)
-    (CG == 2 && p.kps == 2) ? tma_loop<CG, true, SPLIT, 2>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail)
-                            : tma_loop<CG, true, SPLIT, 1>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail);
+    (CG == 2 && p.kps == 2) ? tma_loop<CG, true, SPLIT, 2, DYN>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail)
+                            : tma_loop<CG, true, SPLIT, 1, DYN>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail);
   else
-    (CG == 2 && p.kps == 2) ? tma_loop<CG, false, false, 2>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail)
-                            : tma_loop<CG, false, false, 1>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail);
+    (CG == 2 && p.kps == 2) ? tma_loop<CG, false, false, 2, DYN>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail)
+                            : tma_loop<CG, false, false, 1, DYN>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail);
 }
 
 // The MMA issuer.  tcgen05.mma issue returns only once the tensor core can take
@@ -941,7 +951,7 @@ __device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, uint32_
 // barrier inline and only falls back to the bounded wait when it is not ready.
 // KPS: K blocks per pipeline stage (p.kps), fixed at compile time so that a
 // stage's MMAs issue back to back with no per-block bookkeeping between them.
-template <int CG, bool FP8, bool SPLIT, int KPS>
+template <int CG, bool FP8, bool SPLIT, int KPS, bool DYN>
 __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
                          int total_tiles, int nkb, bool trace, const TailDesc* tail) {
   using PP = Pipe<CG>;
@@ -964,10 +974,8 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   uint32_t stage = 0, phase = 0, ul = 0, issued = 0;
   bool ok = true;
   unsigned long long cyc_full = 0, cyc_tempty = 0;
-  SegIter<SPLIT> it(p, g, G, total_tiles, nkb, tail);
-  if constexpr (!SPLIT) {
-    if (p.dyn) it.set_dynamic(p, 2, sbase, 0, CG, total_tiles);
-  }
+  SegIter<SPLIT, DYN> it(p, g, G, total_tiles, nkb, tail);
+  if constexpr (DYN) it.set_dynamic(p, 2, sbase, 0, CG, total_tiles);
   Seg sg;
   while (ok && it.next(sg)) {
    const uint32_t idesc = idesc_n(idesc0, tile_at<PP::TILE_M>(p, sg.t).ncols);
@@ -1021,24 +1029,24 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   }
 }
 
-template <int CG, bool SPLIT>
+template <int CG, bool SPLIT, bool DYN>
 __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
                          int total_tiles, int nkb, const TailDesc* tail) {
   const bool trace = p.trace_on != 0;
   if (CG == 2 && p.kps == 2) {
     if (p.fp8)
-      mma_loop<CG, true, SPLIT, 2>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace, tail);
+      mma_loop<CG, true, SPLIT, 2, DYN>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace, tail);
     else
-      mma_loop<CG, false, SPLIT, 2>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace, tail);
+      mma_loop<CG, false, SPLIT, 2, DYN>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace, tail);
   } else {
     if (p.fp8)
-      mma_loop<CG, true, SPLIT, 1>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace, tail);
+      mma_loop<CG, true, SPLIT, 1, DYN>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace, tail);
     else
-      mma_loop<CG, false, SPLIT, 1>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace, tail);
+      mma_loop<CG, false, SPLIT, 1, DYN>(p, sbase, tmem, B, g, G, total_tiles, nkb, trace, tail);
   }
 }
 
-template <int CG, bool SPLIT>
+template <int CG, bool SPLIT, bool DYN>
 __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, const Bars& B, uint32_t rank, int g,
                               int G, int total_tiles, const TailDesc* tail) {
   using PP = Pipe<CG>;
@@ -1234,10 +1242,8 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
     }
     return true;
   };
-  SegIter<SPLIT> it(p, g, G, total_tiles, p.num_segs * p.kb_per_seg, tail);
-  if constexpr (!SPLIT) {
-    if (p.dyn) it.set_dynamic(p, 3, sbase_smem, rank, CG, total_tiles);
-  }
+  SegIter<SPLIT, DYN> it(p, g, G, total_tiles, p.num_segs * p.kb_per_seg, tail);
+  if constexpr (DYN) it.set_dynamic(p, 3, sbase_smem, rank, CG, total_tiles);
   Seg sg;
   while (ok_all && it.next(sg)) {
     const Tile T = tile_at<PP::TILE_M>(p, sg.t);
@@ -1408,7 +1414,7 @@ __device__ void epilogue_role(const Params& p, uint8_t* smem, uint32_t tmem, con
   __syncwarp();
 }
 
-template <int CG, bool SPLIT>
+template <int CG, bool SPLIT, bool DYN>
 __device__ void gemm_role(const Params& p, uint8_t* smem) {
   using PP = Pipe<CG>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1438,10 +1444,11 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
       mbar_init(B.tempty0 + 8u * a, CG * EPI_WARPS);  // one arrival per epilogue warp of the group
     }
     mbar_init(B.drain, 1);
-    for (int s = 0; s < TQ_DEPTH; ++s) {  // dynamic tiles: the index ring's barriers
-      mbar_init(sbase + SMEM_BARS + 8u * (BAR_TQ_FULL + s), 1);
-      mbar_init(sbase + SMEM_BARS + 8u * (BAR_TQ_EMPTY + s), CG * (1 + EPI_WARPS));
-    }
+    if constexpr (DYN)
+      for (int s = 0; s < TQ_DEPTH; ++s) {  // the tile index ring's barriers
+        mbar_init(sbase + SMEM_BARS + 8u * (BAR_TQ_FULL + s), 1);
+        mbar_init(sbase + SMEM_BARS + 8u * (BAR_TQ_EMPTY + s), CG * (1 + EPI_WARPS));
+      }
     if constexpr (SPLIT)
       for (int w = 0; w < EPI_WARPS; ++w) mbar_init(B.full0 + 8u * (BAR_PART - BAR_FULL + w), 1);
     fence_barrier_init();
@@ -1465,13 +1472,13 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
   }
 
   if (warp == 0) {
-    if (lane == 0) tma_role<CG, SPLIT>(p, sbase, B, rank, g, G, total_tiles, nkb, tail);
+    if (lane == 0) tma_role<CG, SPLIT, DYN>(p, sbase, B, rank, g, G, total_tiles, nkb, tail);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_role<CG, SPLIT>(p, sbase, tmem, B, g, G, total_tiles, nkb, tail);
+    if (lane == 0 && rank == 0) mma_role<CG, SPLIT, DYN>(p, sbase, tmem, B, g, G, total_tiles, nkb, tail);
     __syncwarp();
   } else {
-    epilogue_role<CG, SPLIT>(p, smem, tmem, B, rank, g, G, total_tiles, tail);
+    epilogue_role<CG, SPLIT, DYN>(p, smem, tmem, B, rank, g, G, total_tiles, tail);
   }
   tc_fence_before();
   __syncthreads();
@@ -1486,7 +1493,7 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
 
 // SPLIT: the build with the AG tail split (launched only when p.tail_split is
 // set); the default build carries none of its code.
-template <int CG, bool SPLIT>
+template <int CG, bool SPLIT, bool DYN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) fused_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -1497,11 +1504,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_kernel(const __grid_cons
     if constexpr (SPLIT) {
       if (p.late_groups > 0) {  // the copy is done: join the GEMM (its ring buffers are free)
         __syncthreads();
-        gemm_role<CG, SPLIT>(p, smem);
+        gemm_role<CG, SPLIT, DYN>(p, smem);
       }
     }
   } else if (static_cast<int>(blockIdx.x) < p.num_producers + p.num_gemm) {
-    gemm_role<CG, SPLIT>(p, smem);
+    gemm_role<CG, SPLIT, DYN>(p, smem);
   }
   if (p.trace_on && threadIdx.x == 0) atomicMax(&p.words->trace[TPO_TRACE_END], gtime());
 }
@@ -1509,18 +1516,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fused_kernel(const __grid_cons
 // ------------------------------------------------------------------ host side launch
 
 cudaError_t configure_kernel() {
-  cudaError_t e = cudaFuncSetAttribute(fused_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  cudaError_t e = cudaFuncSetAttribute(fused_kernel<1, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fused_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    e = cudaFuncSetAttribute(fused_kernel<2, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fused_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    e = cudaFuncSetAttribute(fused_kernel<1, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fused_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    e = cudaFuncSetAttribute(fused_kernel<2, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused_kernel<1, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fused_kernel<2, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
   return e;
 }
 
 cudaError_t max_blocks_per_sm(int* n) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fused_kernel<1, false>, NUM_THREADS, SMEM_ALLOC);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, fused_kernel<1, false, false>, NUM_THREADS, SMEM_ALLOC);
 }
 
 cudaError_t max_active_pairs(int* n) {
@@ -1535,7 +1546,7 @@ cudaError_t max_active_pairs(int* n) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(n, fused_kernel<2, false>, &cfg);
+  return cudaOccupancyMaxActiveClusters(n, fused_kernel<2, false, false>, &cfg);
 }
 
 cudaError_t launch_fused(const Params& p, int grid, bool cooperative, cudaStream_t stream) {
@@ -1566,11 +1577,15 @@ cudaError_t launch_fused(const Params& p, int grid, bool cooperative, cudaStream
   cfg.attrs = attr;
   cfg.numAttrs = na;
   if (p.tail_split) {
-    if (p.cta_group == 2) return cudaLaunchKernelEx(&cfg, fused_kernel<2, true>, p);
-    return cudaLaunchKernelEx(&cfg, fused_kernel<1, true>, p);
+    if (p.cta_group == 2) return cudaLaunchKernelEx(&cfg, fused_kernel<2, true, false>, p);
+    return cudaLaunchKernelEx(&cfg, fused_kernel<1, true, false>, p);
   }
-  if (p.cta_group == 2) return cudaLaunchKernelEx(&cfg, fused_kernel<2, false>, p);
-  return cudaLaunchKernelEx(&cfg, fused_kernel<1, false>, p);
+  if (p.dyn) {
+    if (p.cta_group == 2) return cudaLaunchKernelEx(&cfg, fused_kernel<2, false, true>, p);
+    return cudaLaunchKernelEx(&cfg, fused_kernel<1, false, true>, p);
+  }
+  if (p.cta_group == 2) return cudaLaunchKernelEx(&cfg, fused_kernel<2, false, false>, p);
+  return cudaLaunchKernelEx(&cfg, fused_kernel<1, false, false>, p);
 }
 
 }  // namespace tpo
