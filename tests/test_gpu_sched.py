@@ -50,7 +50,7 @@ def test_ag_dynamic_tiles_bit_identical(tp, n, k, m, dtype):
     try:
         first = _ag_bits(run, 1, 0)
         assert_close(host_f64(run.y), ref, dtype)
-        for mode in (0, 1, 2):
+        for mode in (0, 1, 2, 4):
             for gemm_ctas in (2, 4, 6, 0):
                 for rep in range(2):  # repeated calls: the claim counter runs on
                     bits = _ag_bits(run, 2, gemm_ctas, mode)

@@ -43,6 +43,7 @@ def _noalloc(run: AgRun, y):
     [(4, 1024, 512, 768, "bf16", 61), (2, 512, 256, 512, "bf16", 62)],   # different shapes back to back
     [(4, 4096, 4096, 4096, "bf16", 1), (4, 4096, 4096, 4096, "bf16", 1)],  # the 32 MiB limit, twice
     [(8, 2048, 384, 768, "e4m3", 63), (3, 768, 128, 256, "e4m3", 64)],
+    [(4, 2048, 1024, 20480, "bf16", 65)],   # 640 pair tiles: at least 8 rounds, dynamic tiles in both entry points
 ])
 def test_noalloc_matches_context_entry_point_on_consecutive_calls(cases):
     for tp, n, k, m, dtype, seed in cases:
@@ -54,6 +55,8 @@ def test_noalloc_matches_context_entry_point_on_consecutive_calls(cases):
         try:
             t.tpo_set_opt(run.ctx, "tail_split", 0)     # the no-alloc entry point computes whole tiles
             run.run()                                   # existing entry point, through a context
+            if m >= 16384:                              # many rounds: the context took dynamic tiles
+                assert t.tpo_get_opt(run.ctx, "last_sched") == 2
             ref = host_f64(run.y)
             y = torch.full_like(run.y, float("nan"))
             _noalloc(run, y)                            # returns once the GPU work is done
