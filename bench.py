@@ -262,7 +262,8 @@ def gpu_arm(args, rank, world, local_rank, dist):
     if args.producer_sms:
         t.tpo_set_opt(ctx, "producer_sms", args.producer_sms)
     lib = t.lib()
-    raw_args = [(t._ptr_array(xs_sets[j]), w_sets[j].data_ptr(), y_sets[j].data_ptr()) for j in range(ROTATE)]
+    ptr_arrays = [t._ptr_array(xs_sets[j]) for j in range(ROTATE)]  # kept alive: the calls read them
+    raw_args = [(t._addr(ptr_arrays[j]), w_sets[j].data_ptr(), y_sets[j].data_ptr()) for j in range(ROTATE)]
     sh = stream.cuda_stream
 
     def call(i=0):
@@ -607,7 +608,8 @@ def other_workloads(args, dev, to_dev, time_steps, time_row, mean, peak, peak_su
     w = to_dev(wl.w[0])
     y = torch.empty((wl.n, wl.m), dtype=torch.bfloat16, device=dev)
     ctx = t.tpo_ctx_create(wl.tp, wl.n, wl.k, wl.m, t.TPO_BF16)
-    lib, xa, sh = t.lib(), t._ptr_array(xs), torch.cuda.current_stream().cuda_stream
+    lib, xarr, sh = t.lib(), t._ptr_array(xs), torch.cuda.current_stream().cuda_stream
+    xa = t._addr(xarr)
 
     def raw(i=0):
         st = lib.tpo_ag_gemm(ctx, xa, w.data_ptr(), y.data_ptr(), None, None, sh)

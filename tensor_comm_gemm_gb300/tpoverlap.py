@@ -9,6 +9,7 @@ load, importing this module's functions raises; there is no fallback path.
 
 from __future__ import annotations
 
+import array
 import ctypes
 import os
 from typing import Optional, Sequence
@@ -97,8 +98,14 @@ def _ptr(t) -> int:
     return t.data_ptr()
 
 
-def _ptr_array(ts: Sequence):
-    return (ctypes.c_void_p * len(ts))(*[_ptr(t) for t in ts])
+def _ptr_array(ts: Sequence) -> array.array:
+    """The pointers as a C array of 64-bit words (pass _addr of it; keep the
+    array referenced until the call returns)."""
+    return array.array("Q", [_ptr(t) for t in ts])
+
+
+def _addr(a: array.array) -> int:
+    return a.buffer_info()[0]
 
 
 def _check_tensor(name, t, shape, elem_bytes):
@@ -107,6 +114,8 @@ def _check_tensor(name, t, shape, elem_bytes):
     were row-major.  Raw integer pointers pass unchecked to the library's own
     argument checks.  A mismatch raises TpoError with TPO_ERR_INVALID_ARG."""
     if t is None or isinstance(t, int):
+        return
+    if t.is_cuda and t.element_size() == elem_bytes and t.numel() == shape[0] * shape[1] and t.is_contiguous():
         return
     why = None
     if not t.is_cuda:
@@ -134,10 +143,23 @@ def _sizes(ctx):
 def _stream(stream) -> int:
     if stream is None:
         import torch
+        if _RAW_STREAM is not None:  # the current stream of the current device, as a raw handle
+            return _RAW_STREAM(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+def _raw_stream_getter():
+    try:
+        import torch
+        return getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    except Exception:
+        return None
+
+
+_RAW_STREAM = _raw_stream_getter()
 
 
 def tpo_version() -> str:
@@ -166,7 +188,8 @@ def tpo_ag_gemm(ctx: int, x: Sequence, w, y, scale_inv_x=None, scale_inv_w=None,
         _check_tensor("x[%d]" % r, xr, (n // tp, k), eb)
     _check_tensor("w", w, (m, k), eb)
     _check_tensor("y", y, (n, m), 2)
-    _check(lib().tpo_ag_gemm(ctx, _ptr_array(x), _ptr(w), _ptr(y), _ptr(scale_inv_x), _ptr(scale_inv_w),
+    xa = _ptr_array(x)
+    _check(lib().tpo_ag_gemm(ctx, _addr(xa), _ptr(w), _ptr(y), _ptr(scale_inv_x), _ptr(scale_inv_w),
                              _stream(stream)))
 
 
@@ -187,13 +210,15 @@ def tpo_gemm_rs(ctx: int, x: Sequence, w: Sequence, y: Sequence, stream=None) ->
         raise TpoError(TPO_ERR_INVALID_ARG, "y must hold tp=%d row blocks" % tp)
     for b, yb in enumerate(y):
         _check_tensor("y[%d]" % b, yb, (n // tp, m), 2)
-    _check(lib().tpo_gemm_rs(ctx, _ptr_array(x), _ptr_array(w), _ptr_array(y), _stream(stream)))
+    xa, wa, ya = _ptr_array(x), _ptr_array(w), _ptr_array(y)
+    _check(lib().tpo_gemm_rs(ctx, _addr(xa), _addr(wa), _addr(ya), _stream(stream)))
 
 
 def tpo_gemm_ar(ctx: int, x: Sequence, w: Sequence, y, n_row_chunks: int, stream=None) -> None:
     tp, n, m = _check_ksplit(ctx, x, w)
     _check_tensor("y", y, (n, m), 2)
-    _check(lib().tpo_gemm_ar(ctx, _ptr_array(x), _ptr_array(w), _ptr(y), n_row_chunks, _stream(stream)))
+    xa, wa = _ptr_array(x), _ptr_array(w)
+    _check(lib().tpo_gemm_ar(ctx, _addr(xa), _addr(wa), _ptr(y), n_row_chunks, _stream(stream)))
 
 
 def tpo_set_fp8_scales(ctx: int, scale_inv_x, scale_inv_w) -> None:
@@ -242,5 +267,6 @@ def tpo_ag_gemm_noalloc(tp: int, n: int, k: int, m: int, dtype: int, x: Sequence
                         scale_inv_w=None, stream=None) -> None:
     """AG+GEMM with no device allocation (scratch in the library's static
     array); blocks until the call's work on the stream has finished."""
-    _check(lib().tpo_ag_gemm_noalloc(tp, n, k, m, dtype, _ptr_array(x), _ptr(w), _ptr(y), _ptr(scale_inv_x),
+    xa = _ptr_array(x)
+    _check(lib().tpo_ag_gemm_noalloc(tp, n, k, m, dtype, _addr(xa), _ptr(w), _ptr(y), _ptr(scale_inv_x),
                                      _ptr(scale_inv_w), _stream(stream)))
