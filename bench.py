@@ -602,7 +602,8 @@ def other_workloads(args, dev, to_dev, time_steps, time_row, mean, peak, peak_su
     measured peak (FP8 rows: twice each, the nominal dense ratio)."""
     out = {}
     steps = min(40, max(5, args.steps // 2))
-    # the small AG workload: latency-bound (2 output tiles), reported in microseconds per call
+    # the small AG workload: latency-bound (a few output tiles), reported in microseconds per call of
+    # back-to-back calls (one event pair around the whole run, so no per-call event joins the timing)
     wl = synth.workload(0)
     xs = [to_dev(x) for x in wl.x]
     w = to_dev(wl.w[0])
@@ -616,8 +617,8 @@ def other_workloads(args, dev, to_dev, time_steps, time_row, mean, peak, peak_su
         if st:
             raise t.TpoError(st, t.tpo_last_error())
     t0 = time.time()
-    ms = mean(time_steps(raw, 200, 10))
-    ms_py = mean(time_steps(lambda i=0: t.tpo_ag_gemm(ctx, xs, w, y), 200, 10))
+    ms = time_row(raw, 2000, 20, 0.02)[0]
+    ms_py = time_row(lambda i=0: t.tpo_ag_gemm(ctx, xs, w, y), 2000, 20, 0.02)[0]
     check(ctx)
     # us_per_call: the C ABI call; us_per_call_python adds the binding's argument checks
     out[wl.name] = {"workload": describe(0), "us_per_call": round(ms * 1e3, 2),
