@@ -515,3 +515,47 @@ def test_auto_column_plan():
             for g in range(pl["groups"]):            # every tile 1..8 strips, the strips covered once
                 widths = [tile_strips(pl, g, c)[1] for c in range(pl["group_cols"][g])]
                 assert sum(widths) == pl["strips"] and 1 <= min(widths) and max(widths) <= MAX_TILE_STRIPS
+
+
+def simulate_dynamic_claims(T, G, speeds, base=0):
+    """The dynamic tile protocol on the host: each group claims its first tile,
+    then, whenever it starts a tile, claims the one after it (the claim goes
+    out one tile ahead); a claim at or past T ends the group.  Claims are
+    served in time order from one counter starting at `base`.  Returns the
+    tiles each group computed and the counter's final value."""
+    import heapq
+    counter = base
+    tiles = [[] for _ in range(G)]
+    events = [(0.0, g) for g in range(G)]   # (time the group asks for its next claim, group)
+    heapq.heapify(events)
+    pending = [None] * G                     # the claim a group holds for its next tile
+    while events:
+        now, g = heapq.heappop(events)
+        if pending[g] is None:               # first claim
+            pending[g] = counter - base
+            counter += 1
+        t = pending[g]
+        if t >= T:
+            continue                         # the group's one claim past the end
+        tiles[g].append(t)
+        pending[g] = counter - base          # the next claim, issued as this tile starts
+        counter += 1
+        heapq.heappush(events, (now + speeds[g], g))
+    return tiles, counter
+
+
+def test_dynamic_claims_cover_every_tile_once():
+    """Every tile is claimed by exactly one group, each group makes exactly one
+    claim past the end, so a launch advances the counter by tiles + groups
+    (what the host adds to the next launch's base), whatever the groups'
+    speeds; with equal speeds the claims follow the tile order."""
+    import random
+    rnd = random.Random(7)
+    for T, G in [(1, 1), (5, 8), (64, 2), (256, 69), (2048, 76), (100, 100)]:
+        speeds = [1.0 + 0.2 * rnd.random() for _ in range(G)]
+        base = rnd.randrange(1 << 32)
+        tiles, counter = simulate_dynamic_claims(T, G, speeds, base)
+        assert sorted(t for ts in tiles for t in ts) == list(range(T))
+        assert counter - base == T + G
+        for ts in tiles:
+            assert ts == sorted(ts)          # a group's tiles come in claim order
