@@ -156,6 +156,18 @@ __device__ __forceinline__ bool mbar_wait_timed(const Params& p, uint32_t bar, u
   *cycles += static_cast<unsigned long long>(clock64() - c0);
   return ok;
 }
+// mbar_wait for all 32 lanes of a converged warp: the same result in every
+// lane (the slow path runs in lane 0; afterwards every lane observes the
+// completed phase itself).
+__device__ __forceinline__ bool mbar_wait_warp(const Params& p, uint32_t bar, uint32_t parity, uint32_t site,
+                                               unsigned long long* cycles) {
+  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_timed(p, bar, parity, site, true, cycles) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)mbar_test(bar, parity);
+  return ok != 0;
+}
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -276,24 +288,6 @@ __device__ __forceinline__ uint32_t idesc_n(uint32_t idesc, int n) {
   return idesc | (static_cast<uint32_t>(n >> 3) << 17);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred P;\n\t"
-      "setp.ne.b32 P, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, P;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void mma_e4m3(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred P;\n\t"
-      "setp.ne.b32 P, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, P;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 // Loads 32 columns of the warp's 32 tensor-memory lanes and waits for them in
 // one statement: the compiler never sees the registers before the data landed
 // (a separate wait would let it copy them while the load is still in flight).
@@ -386,48 +380,69 @@ __device__ __forceinline__ void tmem_dealloc_cg(uint32_t taddr, uint32_t ncols) 
   else
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-// One MMA of K = 32 bytes; CG = 2 issues the 2-SM form (M = 256 over the pair).
-template <int CG>
-__device__ __forceinline__ void mma_cg(bool fp8, uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// The MMA issuer is a whole converged warp; inside each asm statement
+// elect.sync picks the one lane that issues.  (Issued from one thread of a
+// diverged warp, a tcgen05.mma took ~53 cycles of that thread and a K block's
+// four ~213, against ~73 for the four from a converged warp: with the stage
+// test and commit around them the single thread needed ~450 cycles per K
+// block, more than the tensor core's 384 at N = 192 or 256 at N = 128.)
+#define TPO_MMA_KBLOCK(CGS, KIND)                                                                         \
+  asm volatile("{\n\t.reg .pred E, A, T;\n\t.reg .b32 r;\n\t"                                              \
+               "setp.ne.b32 A, %4, 0;\n\tsetp.ne.b32 T, %5, 0;\n\t"                                        \
+               "elect.sync r|E, 0xffffffff;\n\t"                                                          \
+               "@E tcgen05.mma.cta_group::" CGS ".kind::" KIND " [%0], %1, %2, %3, A;\n\t"                 \
+               "@E tcgen05.mma.cta_group::" CGS ".kind::" KIND " [%0], %6, %7, %3, T;\n\t"                 \
+               "@E tcgen05.mma.cta_group::" CGS ".kind::" KIND " [%0], %8, %9, %3, T;\n\t"                 \
+               "@E tcgen05.mma.cta_group::" CGS ".kind::" KIND " [%0], %10, %11, %3, T;\n\t}" ::"r"(d),    \
+               "l"(a), "l"(b), "r"(idesc), "r"(acc0), "r"(1u), "l"(a + 2u), "l"(b + 2u), "l"(a + 4u),     \
+               "l"(b + 4u), "l"(a + 6u), "l"(b + 6u))
+// One 128-byte K block: four MMAs of K = 32 bytes (descriptor start addresses
+// 32 bytes apart); acc0 = 0 overwrites the accumulator with the first.
+// CG = 2 issues the 2-SM form (M = 256 over the pair).
+template <int CG, bool FP8>
+__device__ __forceinline__ void mma_kblock(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc0) {
   if constexpr (CG == 1) {
-    if (fp8)
-      mma_e4m3(d, a, b, idesc, acc);
+    if constexpr (FP8)
+      TPO_MMA_KBLOCK("1", "f8f6f4");
     else
-      mma_bf16(d, a, b, idesc, acc);
+      TPO_MMA_KBLOCK("1", "f16");
   } else {
-    if (fp8)
-      asm volatile(
-          "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %4, 0;\n\t"
-          "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, P;\n\t}" ::"r"(d),
-          "l"(a), "l"(b), "r"(idesc), "r"(acc));
+    if constexpr (FP8)
+      TPO_MMA_KBLOCK("2", "f8f6f4");
     else
-      asm volatile(
-          "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %4, 0;\n\t"
-          "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, P;\n\t}" ::"r"(d),
-          "l"(a), "l"(b), "r"(idesc), "r"(acc));
+      TPO_MMA_KBLOCK("2", "f16");
   }
 }
-// Arrive on `bar` (same offset in every CTA of the group) once all prior MMAs completed.
+#undef TPO_MMA_KBLOCK
+// Arrive on `bar` (same offset in every CTA of the group) once all prior MMAs
+// completed; a whole converged warp executes it, one elected lane commits.
 template <int CG>
 __device__ __forceinline__ void mma_commit_cg(uint32_t bar) {
   if constexpr (CG == 1) {
-    mma_commit(bar);
+    asm volatile(
+        "{\n\t.reg .pred E;\n\t.reg .b32 r;\n\telect.sync r|E, 0xffffffff;\n\t"
+        "@E tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
   } else {
     const uint16_t mask = 0x3;
     asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+        "{\n\t.reg .pred E;\n\t.reg .b32 r;\n\telect.sync r|E, 0xffffffff;\n\t"
+        "@E tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
             bar),
         "h"(mask)
         : "memory");
   }
 }
-// Commit that arrives on this CTA's barrier only.
+// Commit that arrives on this CTA's barrier only (whole warp, one elected lane).
 template <int CG>
 __device__ __forceinline__ void mma_commit_local_cg(uint32_t bar) {
   if constexpr (CG == 1)
-    mma_commit(bar);
+    mma_commit_cg<1>(bar);
   else
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+    asm volatile(
+        "{\n\t.reg .pred E;\n\t.reg .b32 r;\n\telect.sync r|E, 0xffffffff;\n\t"
+        "@E tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
 }
 
 // ------------------------------------------------------------------ tile schedule
@@ -944,13 +959,15 @@ __device__ void tma_role(const Params& p, uint32_t sbase, const Bars& B, uint32_
                             : tma_loop<CG, false, false, 1, DYN>(p, sbase, B, rank, g, G, total_tiles, nkb, trace, tail);
 }
 
-// The MMA issuer.  tcgen05.mma issue returns only once the tensor core can take
-// the instruction, so about one MMA is ever queued: every cycle the issuing
-// thread spends between two MMAs is tensor-pipe idle time.  The loop therefore
-// keeps all state in registers (no parameter reloads), tests each stage's
-// barrier inline and only falls back to the bounded wait when it is not ready.
-// KPS: K blocks per pipeline stage (p.kps), fixed at compile time so that a
-// stage's MMAs issue back to back with no per-block bookkeeping between them.
+// The MMA issuer: the whole of warp 1 of the group's even CTA, converged (one
+// elected lane issues each MMA and commit).  tcgen05.mma issue returns only
+// once the tensor core can take the instruction, so only a few MMAs are ever
+// queued: every cycle the issuer spends between two MMAs is tensor-pipe idle
+// time.  The loop therefore keeps all state in registers (no parameter
+// reloads), tests each stage's barrier inline (a warp vote, so that every
+// branch is uniform) and only falls back to the bounded wait when it is not
+// ready.  KPS: K blocks per pipeline stage (p.kps), fixed at compile time so
+// that a stage's MMAs issue back to back with no per-block bookkeeping.
 template <int CG, bool FP8, bool SPLIT, int KPS, bool DYN>
 __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const Bars& B, int g, int G,
                          int total_tiles, int nkb, bool trace, const TailDesc* tail) {
@@ -975,7 +992,7 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   bool ok = true;
   unsigned long long cyc_full = 0, cyc_tempty = 0;
   SegIter<SPLIT, DYN> it(p, g, G, total_tiles, nkb, tail);
-  if constexpr (DYN) it.set_dynamic(p, 2, sbase, 0, CG, total_tiles);
+  if constexpr (DYN) it.set_dynamic(p, 3, sbase, 0, CG, total_tiles);
   Seg sg;
   while (ok && it.next(sg)) {
    const uint32_t idesc = idesc_n(idesc0, tile_at<PP::TILE_M>(p, sg.t).ncols);
@@ -983,7 +1000,7 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
     const uint32_t acc = ul & 1u;
     const uint32_t te = tempty0 + 8u * acc;
     const uint32_t tpar = ((ul >> 1) & 1u) ^ 1u;
-    if (!mbar_test(te, tpar) && !mbar_wait_timed(p, te, tpar, SITE_TMEM_EMPTY, true, &cyc_tempty)) {
+    if (!mbar_wait_warp(p, te, tpar, SITE_TMEM_EMPTY, &cyc_tempty)) {
       ok = false;
       break;
     }
@@ -992,21 +1009,15 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
     const int nk = per_rank ? kpu : sg.kb_hi - sg.kb_lo;  // a multiple of KPS
     for (int i = 0; i < nk; i += KPS) {
       const uint32_t fb = full0 + 8u * stage;
-      if (!mbar_test(fb, phase) && !mbar_wait_timed(p, fb, phase, SITE_FULL, true, &cyc_full)) {
+      if (!mbar_wait_warp(p, fb, phase, SITE_FULL, &cyc_full)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint64_t das = da0 + kStageDesc * stage, dbs = db0 + kStageDesc * stage;
 #pragma unroll
-      for (int b = 0; b < KPS; ++b) {
-        const uint64_t da = das + kBlkA * b, db = dbs + kBlkB * b;
-        // four MMAs of K = 32 bytes each cover the 128-byte K block
-        mma_cg<CG>(FP8, d, da, db, idesc, (i + b) > 0 ? 1u : 0u);
-        mma_cg<CG>(FP8, d, da + 2u, db + 2u, idesc, 1u);
-        mma_cg<CG>(FP8, d, da + 4u, db + 4u, idesc, 1u);
-        mma_cg<CG>(FP8, d, da + 6u, db + 6u, idesc, 1u);
-      }
+      for (int b = 0; b < KPS; ++b)
+        mma_kblock<CG, FP8>(d, das + kBlkA * b, dbs + kBlkB * b, idesc, (i + b) > 0 ? 1u : 0u);
       issued += KPS;
       mma_commit_cg<CG>(empty0 + 8u * stage);  // frees the stage (in both CTAs) once read
       if (++stage == nstages) {
@@ -1020,9 +1031,10 @@ __device__ void mma_loop(const Params& p, uint32_t sbase, uint32_t tmem, const B
   }
   if (!ok) {  // every MMA issued so far must complete before tensor memory is freed
     mma_commit_local_cg<CG>(B.drain);
-    mbar_wait(p, B.drain, 0u, SITE_DRAIN, false);
+    if ((threadIdx.x & 31) == 0) mbar_wait(p, B.drain, 0u, SITE_DRAIN, false);
+    __syncwarp();
   }
-  if (trace) {
+  if (trace && (threadIdx.x & 31) == 0) {
     atomicAdd(&p.words->trace[TPO_TRACE_CYC_MMA_FULL], cyc_full);
     atomicAdd(&p.words->trace[TPO_TRACE_CYC_MMA_TEMPTY], cyc_tempty);
     atomicAdd(&p.words->trace[TPO_TRACE_KBLOCKS], static_cast<unsigned long long>(issued));
@@ -1475,7 +1487,7 @@ __device__ void gemm_role(const Params& p, uint8_t* smem) {
     if (lane == 0) tma_role<CG, SPLIT, DYN>(p, sbase, B, rank, g, G, total_tiles, nkb, tail);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) mma_role<CG, SPLIT, DYN>(p, sbase, tmem, B, g, G, total_tiles, nkb, tail);
+    if (rank == 0) mma_role<CG, SPLIT, DYN>(p, sbase, tmem, B, g, G, total_tiles, nkb, tail);  // the whole warp
     __syncwarp();
   } else {
     epilogue_role<CG, SPLIT, DYN>(p, smem, tmem, B, rank, g, G, total_tiles, tail);
