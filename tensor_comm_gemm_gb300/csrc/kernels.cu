@@ -13,8 +13,8 @@
 //
 //  * GEMM CTAs: a persistent tcgen05 GEMM.  Warp 0 issues TMA loads (after an
 //    acquire-wait on the slot's counter for gathered rows), warp 1 issues
-//    tcgen05.mma from one thread into a double-buffered fp32 accumulator in
-//    tensor memory, warps 2..5 drain the accumulator (tcgen05.ld), round to
+//    tcgen05.mma (one elected lane of the converged warp) into a double-
+//    buffered fp32 accumulator in tensor memory, warps 2..5 drain the accumulator (tcgen05.ld), round to
 //    bf16 and TMA-store the tile.  In the pair variant (CG = 2) two CTAs of a
 //    cluster share one 256 x 256 tile through the 2-SM MMA: each loads its own
 //    128 rows of A and half of the B tile, the even CTA issues the MMAs, and
@@ -555,7 +555,7 @@ struct Seg {
 // tile with an atomic add on a launch-wide counter, so that groups that run
 // faster take more tiles and the tiles in flight stay a contiguous run of the
 // tile order (their shared operands stay in L2 together).  It passes every
-// index to the group's other roles (its MMA thread, the epilogue warps and,
+// index to the group's other roles (its MMA warp, the epilogue warps and,
 // for pairs, the odd CTA's TMA thread and epilogue warps) through a ring of
 // TQ_DEPTH shared-memory words: a full barrier per slot in each CTA (one
 // arrival from the claiming thread) and an empty barrier per slot in the even

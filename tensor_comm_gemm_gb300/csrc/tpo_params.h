@@ -83,8 +83,8 @@ enum DevErr : uint32_t { DEV_OK = 0, DEV_TIMEOUT = 1 };
 enum Site : uint32_t {
   SITE_COUNTER = 1,    // GEMM TMA thread waiting on a chunk counter
   SITE_EMPTY = 2,      // TMA thread waiting for a free stage
-  SITE_FULL = 3,       // MMA thread waiting for a loaded stage
-  SITE_TMEM_EMPTY = 4, // MMA thread waiting for a drained accumulator
+  SITE_FULL = 3,       // MMA warp waiting for a loaded stage
+  SITE_TMEM_EMPTY = 4, // MMA warp waiting for a drained accumulator
   SITE_TMEM_FULL = 5,  // epilogue waiting for a finished accumulator
   SITE_COPY = 6,       // producer waiting for a bulk load
   SITE_DRAIN = 7,      // clean-up waits after a failure
