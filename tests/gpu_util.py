@@ -150,11 +150,15 @@ def wire_expectation(wl, op: str, chunks: int):
     sum_q |x_q w_q| (four times the first-order bound of a recursive fp32 sum
     of kr products, plus the fp32 scale multiplies).  Where no partial is at
     risk, every rounded partial equals the oracle's and the same fp32 hops on
-    the same values give the same bits.  Elsewhere each rounding of a partial
-    or a running sum can land one bf16 spacing away, and later hops carry the
-    difference: |result - ref| <= sum_r (u(P_r) + u(S_r)), S_r the exact
-    running sums in the row's ring order and u(v) = 2^-6 |v| + 2^-133 (one
-    spacing at |v| and in the binade above)."""
+    the same values give the same bits.  Elsewhere a rounded partial can be
+    off by the partial's own fp32 error plus one bf16 spacing at its computed
+    magnitude, eps_r + u(|P_r| + eps_r), and each rounded running sum by one
+    spacing at its computed magnitude, u(|S_r| + E_r), E_r the error carried
+    into it; later hops carry every difference.  So |result - ref| <= E, E
+    accumulated hop by hop in the row's ring order from these terms, S_r the
+    exact running sums and u(v) = 2^-6 |v| + 2^-133 (one spacing at |v| and in
+    the binade above).  The fp32 error matters where the partial nearly
+    cancels: it can then exceed a spacing of the exact value."""
     import oracle
 
     tp, n = wl.tp, wl.n
@@ -172,12 +176,15 @@ def wire_expectation(wl, op: str, chunks: int):
     for b in range(tp):
         rows = owners == b
         run = np.zeros((int(rows.sum()), ref.shape[1]))
+        err = np.zeros_like(run)   # E: what the result may differ by after this hop
         for j in range(tp):
             r = (b + 1 + j) % tp
-            p = parts[r][rows]
+            p, e = parts[r][rows], eps[r][rows]
             run = run + p
-            risky[rows] |= near_bf16_boundary(p, eps[r][rows])
-            bound[rows] += 2.0 ** -6 * (np.abs(p) + np.abs(run)) + 2 * 2.0 ** -133
+            risky[rows] |= near_bf16_boundary(p, e)
+            err = err + e + 2.0 ** -6 * (np.abs(p) + e) + 2.0 ** -133   # the rounded partial
+            err = err + 2.0 ** -6 * (np.abs(run) + err) + 2.0 ** -133   # the rounded running sum
+        bound[rows] = err
     return ref, risky, bound
 
 
