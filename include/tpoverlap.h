@@ -231,10 +231,11 @@ tpo_status tpo_set_fp8_scales(tpo_ctx* ctx, const float* d_scale_inv_x, const fl
  *                      ((v >> 4g) & 15) of extra tiles.  The GEMM grid
  *                      follows the plan's tile count.  Results are identical
  *                      (the MMA computes every output element the same way
- *                      whatever the tile width).  A K block costs about the
- *                      same at any width from 128 to 256 columns, so more
- *                      tiles pay only where they all fit in one round: each
- *                      tile's epilogue is then shorter.
+ *                      whatever the tile width).  A K block of a narrower
+ *                      tile costs less, but not in proportion (at 192
+ *                      columns ~0.86 of a 256-column one: the operand loads
+ *                      bound it), so more tiles pay only where they all fit
+ *                      in one round: each tile's epilogue is then shorter.
  *   "sched"            which CTA group computes which tile: 1 round robin
  *                      (group g takes tiles g, g+G, g+2G, ...); 2 dynamic
  *                      (each group claims its next tile from a launch-wide

@@ -345,10 +345,13 @@ int gemm_grid(const tpo_ctx* c, int cg, int64_t want, int producers, int tiles) 
 // robin, each group one tile after another, in the kernel's tile order; a
 // tile of AG ring step g waits until that step's chunk has landed
 // (ready_us[g]).  A tile costs nkb 128-byte K blocks of kKbUs x (0.91 + 0.09
-// w / 8) microseconds for w 32-column strips: measured on 256-row tile pairs,
-// a K block of a tile 128 to 256 columns wide costs 559 to 585 SM cycles,
-// with or without its operand loads (tcgen05.mma issue takes ~140 cycles per
-// instruction whatever its N), so narrower tiles save almost nothing.
+// w / 8) microseconds for w 32-column strips: measured on 256-row tile pairs
+// while the MMAs were issued from a single thread, when a K block of a tile
+// 128 to 256 columns wide cost 559 to 585 SM cycles whatever its width.
+// Issued from a converged warp, narrower tiles now cost somewhat less (a
+// 192-column tile's K block ~0.86 of a 256-column one's; the operand loads
+// then bound it); the model keeps the older figures, which shape only the
+// producer count and column plan of launches with narrow tiles.
 constexpr double kKbUs = 0.33;
 
 template <int TILE_M>
